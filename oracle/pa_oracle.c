@@ -1,0 +1,343 @@
+/*
+ * pa_oracle.c -- plain, slow, fp64 CPU oracle for paged KV-cache decode.
+ *
+ * TEST INFRASTRUCTURE, NOT PART OF THE PRODUCT.  Only the test-suite, the smoke
+ * check and the benchmark's CPU-baseline / reference leg may load this code.  It
+ * shares no header, helper, table or constant with the CUDA library: every
+ * format, layout and formula below is written out again from its definition.
+ *
+ * What it computes, and where that is stated:
+ *
+ *  - Bytes per token of a KV cache, 2 * n_layers * n_kv_heads * d_head * bytes
+ *    ("Optimización de KV Cache con PagedAttention y Cuantización FP8 para
+ *    Contextos Largos (128K)", section 2).
+ *  - A flat pool of fixed-size blocks (16 tokens) addressed through a per-
+ *    sequence block table: logical block j of a sequence lives in physical
+ *    block table[j] ("Capítulo 8 -- Gestión de caché KV de nueva generación",
+ *    section 8.1; "PagedAttention y Gestión de KV-Cache", section 2 figure).
+ *    Pool layout, per layer: K and V separate, each [num_blocks][n_kv_heads]
+ *    [block_size][head_dim] elements.
+ *  - Writing a new token's K/V into its slot (slot = block * block_size +
+ *    offset), converting 16-bit values to 8-bit FP8 on the fly when the cache is
+ *    FP8 ("Optimización de KV Cache ...", section 4).  FP8 is OCP E4M3FN:
+ *    code = e4m3_rne_satfinite( fl32(x / scale) ), with a static per-tensor
+ *    scale (same page, section 8, static calibration).
+ *  - Decode attention: gather a sequence's pages in logical order into
+ *    contiguous K, V, then textbook softmax attention per query head, with
+ *    query head g reading kv head floor(g / G), G = n_q_heads / n_kv_heads.
+ *    Everything in fp64.  A sequence of context length 0 yields a zero output.
+ *  - Copy of whole blocks (K and V tiles of every kv head), the copy-on-write
+ *    step of shared prefixes ("PagedAttention y Gestión de KV-Cache", section
+ *    3.01; "KV Cache y PagedAttention", "Cómo PagedAttention soluciona esto").
+ *
+ * Dtype codes used by this file (its own, passed in by its Python wrapper):
+ *   0 = IEEE binary16, 1 = bfloat16, 2 = FP8 E4M3FN.
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+#define OR_F16 0
+#define OR_BF16 1
+#define OR_E4M3 2
+
+/* ---------------------------------------------------------------------------
+ * Number formats, decoded from their bit-level definitions.
+ * ------------------------------------------------------------------------- */
+
+/* IEEE 754 binary16: 1 sign bit, 5 exponent bits (bias 15), 10 fraction bits. */
+double or_f16_value(uint16_t bits) {
+  int sign = (bits >> 15) & 1;
+  int e = (bits >> 10) & 0x1F;
+  int f = bits & 0x3FF;
+  double v;
+  if (e == 0) {
+    v = ldexp((double)f, -24); /* subnormal: f * 2^-14 * 2^-10 */
+  } else if (e == 31) {
+    v = (f == 0) ? INFINITY : NAN;
+  } else {
+    v = ldexp((double)(1024 + f), e - 25); /* (1 + f/1024) * 2^(e-15) */
+  }
+  return sign ? -v : v;
+}
+
+/* bfloat16: the upper 16 bits of an IEEE binary32. */
+double or_bf16_value(uint16_t bits) {
+  uint32_t w = ((uint32_t)bits) << 16;
+  float f;
+  memcpy(&f, &w, sizeof f);
+  return (double)f;
+}
+
+/* OCP FP8 E4M3FN: 1 sign bit, 4 exponent bits (bias 7), 3 mantissa bits.
+ * No infinities; S.1111.111 is NaN; exponent field 0 holds subnormals
+ * m * 2^-9; largest finite value 1.75 * 2^8 = 448. */
+double or_e4m3_value(uint8_t code) {
+  int sign = (code >> 7) & 1;
+  int e = (code >> 3) & 0xF;
+  int m = code & 0x7;
+  double v;
+  if (e == 15 && m == 7) return NAN;
+  if (e == 0) {
+    v = ldexp((double)m, -9);
+  } else {
+    v = ldexp((double)(8 + m), e - 10); /* (1 + m/8) * 2^(e-7) */
+  }
+  return sign ? -v : v;
+}
+
+/* Round a non-negative real q to an integer, ties to the even integer. */
+static double round_half_even(double q) {
+  double fl = floor(q);
+  double r = q - fl; /* exact: q has at most 53 significant bits */
+  if (r > 0.5) return fl + 1.0;
+  if (r < 0.5) return fl;
+  return (fmod(fl, 2.0) == 0.0) ? fl : fl + 1.0;
+}
+
+/* E4M3 encoding of an fp32 value y: round to the nearest point of the E4M3
+ * grid, ties to the even mantissa (subnormals included), then saturate any
+ * magnitude above 448 to 448 ("satfinite").  The sign is kept, so -0 -> 0x80.
+ * NaN maps to 0x7F (this case is outside every workload here). */
+uint8_t or_e4m3_encode(float y) {
+  if (isnan(y)) return 0x7F;
+  uint8_t sign = signbit(y) ? 0x80 : 0x00;
+  double a = fabs((double)y);
+  if (a >= 448.0) return sign | 0x7E;
+  if (a < ldexp(1.0, -6)) {
+    /* subnormal binade: grid step 2^-9; n == 8 is the smallest normal 2^-6,
+     * whose code (exponent 1, mantissa 0) is also 8. */
+    double n = round_half_even(a * 512.0);
+    return sign | (uint8_t)n;
+  }
+  int k;
+  frexp(a, &k); /* a = f * 2^k, f in [0.5, 1): a lies in binade 2^(k-1) */
+  int ebin = k - 1;                 /* unbiased exponent, -6 .. 8 */
+  double step = ldexp(1.0, ebin - 3); /* 3 mantissa bits */
+  double n = round_half_even(a / step); /* in [8, 16]; 16 carries up a binade */
+  int code = ((ebin + 7) << 3) + ((int)n - 8);
+  if (code > 0x7E) code = 0x7E; /* cannot happen for a < 448; kept for clarity */
+  return sign | (uint8_t)code;
+}
+
+/* Quantise one stored 16-bit value x with the per-tensor scale s:
+ * y = fl32(x / s) (the fp64 quotient rounded once to fp32 equals the IEEE fp32
+ * quotient, since 53 >= 2*24 + 2), then E4M3 with saturation. */
+uint8_t or_quantize_e4m3(double x, float s) {
+  float y = (float)(x / (double)s);
+  return or_e4m3_encode(y);
+}
+
+double or_value16(int dtype, uint16_t bits) {
+  return dtype == OR_BF16 ? or_bf16_value(bits) : or_f16_value(bits);
+}
+
+/* Closed form of the KV-cache size per token (one K and one V vector per kv
+ * head per layer). */
+long long or_kv_bytes_per_token(int n_layers, int n_kv_heads, int d_head, int precision_bytes) {
+  return 2LL * n_layers * n_kv_heads * d_head * precision_bytes;
+}
+
+/* Bytes of one element of the pool for a cache dtype. */
+static int elem_bytes(int kv_dtype) { return kv_dtype == OR_E4M3 ? 1 : 2; }
+
+/* Element index of (block, kv head, offset within block, dim) in one layer's
+ * K or V pool of layout [num_blocks][n_kv_heads][block_size][head_dim]. */
+static long long pool_index(int block, int h, int off, int i, int n_kv_heads, int block_size,
+                            int head_dim) {
+  return (((long long)block * n_kv_heads + h) * block_size + off) * head_dim + i;
+}
+
+/* Value of pool element idx (already dequantised for FP8). */
+static double pool_value(int kv_dtype, const uint8_t* pool, long long idx, float scale) {
+  if (kv_dtype == OR_E4M3) return or_e4m3_value(pool[idx]) * (double)scale;
+  uint16_t bits;
+  memcpy(&bits, pool + 2 * idx, 2);
+  return or_value16(kv_dtype, bits);
+}
+
+/* ---------------------------------------------------------------------------
+ * Writing new tokens into their slots.
+ *   k_in, v_in : [T][n_kv_heads][head_dim] 16-bit bit patterns (input dtype:
+ *                binary16 for a binary16 cache, bfloat16 otherwise)
+ *   slot_mapping[t] = block * block_size + offset, or negative to skip token t
+ * Returns 0, or -1 if some slot lies beyond the pool (nothing is written for it).
+ * ------------------------------------------------------------------------- */
+int or_reshape_and_cache(int kv_dtype, int num_blocks, int block_size, int n_kv_heads,
+                         int head_dim, const uint16_t* k_in, const uint16_t* v_in,
+                         const int64_t* slot_mapping, int T, float k_scale, float v_scale,
+                         uint8_t* k_pool, uint8_t* v_pool) {
+  int status = 0;
+  int in_dtype = (kv_dtype == OR_F16) ? OR_F16 : OR_BF16;
+  for (int t = 0; t < T; ++t) {
+    int64_t slot = slot_mapping[t];
+    if (slot < 0) continue;
+    if (slot >= (int64_t)num_blocks * block_size) {
+      status = -1;
+      continue;
+    }
+    int block = (int)(slot / block_size);
+    int off = (int)(slot % block_size);
+    for (int h = 0; h < n_kv_heads; ++h) {
+      for (int i = 0; i < head_dim; ++i) {
+        long long src = ((long long)t * n_kv_heads + h) * head_dim + i;
+        long long dst = pool_index(block, h, off, i, n_kv_heads, block_size, head_dim);
+        if (kv_dtype == OR_E4M3) {
+          k_pool[dst] = or_quantize_e4m3(or_value16(in_dtype, k_in[src]), k_scale);
+          v_pool[dst] = or_quantize_e4m3(or_value16(in_dtype, v_in[src]), v_scale);
+        } else {
+          memcpy(k_pool + 2 * dst, &k_in[src], 2);
+          memcpy(v_pool + 2 * dst, &v_in[src], 2);
+        }
+      }
+    }
+  }
+  return status;
+}
+
+/* Copy whole blocks: for each pair (src, dst), the K and V tiles of every kv
+ * head of one layer.  pairs: [n][2].  Returns -1 if an id is out of range. */
+int or_copy_blocks(int kv_dtype, int num_blocks, int block_size, int n_kv_heads, int head_dim,
+                   const int32_t* pairs, int n, uint8_t* k_pool, uint8_t* v_pool) {
+  long long blk = (long long)n_kv_heads * block_size * head_dim * elem_bytes(kv_dtype);
+  int status = 0;
+  for (int p = 0; p < n; ++p) {
+    int src = pairs[2 * p], dst = pairs[2 * p + 1];
+    if (src < 0 || src >= num_blocks || dst < 0 || dst >= num_blocks) {
+      status = -1;
+      continue;
+    }
+    memmove(k_pool + dst * blk, k_pool + src * blk, (size_t)blk);
+    memmove(v_pool + dst * blk, v_pool + src * blk, (size_t)blk);
+  }
+  return status;
+}
+
+/* ---------------------------------------------------------------------------
+ * Textbook softmax attention of one query vector q[head_dim] over n keys and
+ * values (row r of K at K + r*ld, of V at V + r*ld), all fp64.
+ * Writes out[head_dim] and, if probs != NULL, probs[n].
+ * ------------------------------------------------------------------------- */
+static void attend(const double* q, const double* K, const double* V, long long ld, int n,
+                   int head_dim, double softmax_scale, double* out, double* probs) {
+  for (int i = 0; i < head_dim; ++i) out[i] = 0.0;
+  if (n == 0) return;
+  double* z = (double*)malloc(sizeof(double) * (size_t)n);
+  double zmax = -INFINITY;
+  for (int r = 0; r < n; ++r) {
+    double dot = 0.0;
+    for (int i = 0; i < head_dim; ++i) dot += q[i] * K[r * ld + i];
+    z[r] = softmax_scale * dot;
+    if (z[r] > zmax) zmax = z[r];
+  }
+  double sum = 0.0;
+  for (int r = 0; r < n; ++r) {
+    z[r] = exp(z[r] - zmax);
+    sum += z[r];
+  }
+  for (int r = 0; r < n; ++r) {
+    double p = z[r] / sum;
+    if (probs) probs[r] = p;
+    for (int i = 0; i < head_dim; ++i) out[i] += p * V[r * ld + i];
+  }
+  free(z);
+}
+
+/* ---------------------------------------------------------------------------
+ * Paged decode attention.
+ *   q            : [S][n_q_heads][head_dim] 16-bit bit patterns (q_dtype)
+ *   block_tables : [S][max_blocks_per_seq] physical block ids
+ *   ctx_lens     : [S] context length of each sequence (tokens)
+ *   out          : [S][n_q_heads][head_dim] fp64
+ *   probs        : optional [S][n_q_heads][max_ctx] fp64 (max_ctx = the
+ *                  largest ctx_lens entry), softmax probabilities; NULL to skip
+ * Returns 0, -1 on an invalid block id or context length (that sequence's
+ * output is then left zero), -2 if n_q_heads is not a multiple of n_kv_heads.
+ * ------------------------------------------------------------------------- */
+int or_paged_attention(int kv_dtype, int q_dtype, int num_blocks, int block_size, int n_kv_heads,
+                       int head_dim, const uint8_t* k_pool, const uint8_t* v_pool,
+                       float k_scale, float v_scale, const uint16_t* q, int n_q_heads,
+                       const int32_t* block_tables, int max_blocks_per_seq,
+                       const int32_t* ctx_lens, int S, double softmax_scale, double* out,
+                       double* probs) {
+  if (n_kv_heads <= 0 || n_q_heads % n_kv_heads != 0) return -2;
+  int G = n_q_heads / n_kv_heads;
+  int status = 0;
+  int max_ctx = 0;
+  for (int s = 0; s < S; ++s)
+    if (ctx_lens[s] > max_ctx) max_ctx = ctx_lens[s];
+  double* qv = (double*)malloc(sizeof(double) * (size_t)head_dim);
+  for (int s = 0; s < S; ++s) {
+    int n = ctx_lens[s];
+    double* o_seq = out + (long long)s * n_q_heads * head_dim;
+    for (long long i = 0; i < (long long)n_q_heads * head_dim; ++i) o_seq[i] = 0.0;
+    int nblk = (n + block_size - 1) / block_size;
+    if (n < 0 || nblk > max_blocks_per_seq) {
+      status = -1;
+      continue;
+    }
+    int bad = 0;
+    for (int j = 0; j < nblk; ++j) {
+      int b = block_tables[(long long)s * max_blocks_per_seq + j];
+      if (b < 0 || b >= num_blocks) bad = 1;
+    }
+    if (bad) {
+      status = -1;
+      continue;
+    }
+    /* Step 1: gather the sequence's pages, in logical order, into contiguous
+     * K[n][n_kv_heads][head_dim] and V[...] (dequantising FP8 codes). */
+    long long row = (long long)n_kv_heads * head_dim;
+    double* K = (double*)malloc(sizeof(double) * (size_t)(n > 0 ? n * row : 1));
+    double* V = (double*)malloc(sizeof(double) * (size_t)(n > 0 ? n * row : 1));
+    for (int tok = 0; tok < n; ++tok) {
+      int j = tok / block_size, off = tok % block_size;
+      int b = block_tables[(long long)s * max_blocks_per_seq + j];
+      for (int h = 0; h < n_kv_heads; ++h) {
+        for (int i = 0; i < head_dim; ++i) {
+          long long idx = pool_index(b, h, off, i, n_kv_heads, block_size, head_dim);
+          K[tok * row + h * head_dim + i] = pool_value(kv_dtype, k_pool, idx, k_scale);
+          V[tok * row + h * head_dim + i] = pool_value(kv_dtype, v_pool, idx, v_scale);
+        }
+      }
+    }
+    /* Step 2: softmax attention per query head against its kv head. */
+    for (int g = 0; g < n_q_heads; ++g) {
+      int h = g / G;
+      const uint16_t* qg = q + ((long long)s * n_q_heads + g) * head_dim;
+      for (int i = 0; i < head_dim; ++i) qv[i] = or_value16(q_dtype, qg[i]);
+      double* pr = probs ? probs + ((long long)s * n_q_heads + g) * max_ctx : NULL;
+      attend(qv, K + h * head_dim, V + h * head_dim, row, n, head_dim, softmax_scale,
+             o_seq + (long long)g * head_dim, pr);
+    }
+    free(K);
+    free(V);
+  }
+  free(qv);
+  return status;
+}
+
+/* ---------------------------------------------------------------------------
+ * Attention over a contiguous slab: K, V are [S][max_ctx][n_kv_heads][head_dim]
+ * fp64 values, sequence s using its first ctx_lens[s] rows.  No pages, no
+ * tables: the layout that paging replaces.  q is fp64 [S][n_q_heads][head_dim].
+ * ------------------------------------------------------------------------- */
+int or_slab_attention(const double* K, const double* V, int max_ctx, int n_kv_heads, int head_dim,
+                      const double* q, int n_q_heads, const int32_t* ctx_lens, int S,
+                      double softmax_scale, double* out) {
+  if (n_kv_heads <= 0 || n_q_heads % n_kv_heads != 0) return -2;
+  int G = n_q_heads / n_kv_heads;
+  long long row = (long long)n_kv_heads * head_dim;
+  for (int s = 0; s < S; ++s) {
+    const double* Ks = K + (long long)s * max_ctx * row;
+    const double* Vs = V + (long long)s * max_ctx * row;
+    for (int g = 0; g < n_q_heads; ++g) {
+      int h = g / G;
+      attend(q + ((long long)s * n_q_heads + g) * head_dim, Ks + h * head_dim, Vs + h * head_dim,
+             row, ctx_lens[s], head_dim, softmax_scale,
+             out + ((long long)s * n_q_heads + g) * head_dim, NULL);
+    }
+  }
+  return 0;
+}
