@@ -1,0 +1,559 @@
+#!/usr/bin/env python
+"""Paged decode benchmark on GB300: KV-read HBM GB/s and decode tokens/s.
+
+Workload (default): Llama-3.1-70B-shaped single-layer decode over an FP8 E4M3
+paged KV cache -- 64 query heads, 8 KV heads, head dim 128, 16-token blocks,
+block tables random permutations of the pool -- in two batches:
+  A: 4 sequences x 131,072 tokens  (long context; split along the pages)
+  B: 256 sequences x 4,096 tokens
+One step = for each batch: pa_reshape_and_cache of the step's new token of
+every sequence (quantised into its slot) then pa_decode of one query token per
+sequence against its whole context.  The pool (3 GiB) is larger than L2, so
+no flush is needed between steps.
+
+Output: one JSON line (rank 0).  `value` = K+V bytes the decode reads per
+step / step time.  `e2e` = the same metric measured through the C ABI with the
+step's inputs copied from pinned host memory and the output read back, every
+step.  `--impl reference` times the fp64 CPU oracle on a bounded sample of the
+same workload instead.
+"""
+from __future__ import annotations
+
+import argparse
+import ctypes
+import hashlib
+import json
+import math
+import multiprocessing as mp
+import os
+import statistics
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+METRIC = ("paged decode: KV-read HBM GB/s (% of GB300 peak) and decode tokens/s, 1 GPU")
+SPEC_HBM_GBS = 8000.0
+FALLBACK_HBM_GBS = 6800.0
+
+WORKLOADS = {
+    "llama3_70b_fp8": ["llama3_70b_fp8_a", "llama3_70b_fp8_b"],
+    "llama3_70b_fp8_a": ["llama3_70b_fp8_a"],
+    "llama3_70b_fp8_b": ["llama3_70b_fp8_b"],
+    "llama3_8b_bf16": ["llama3_8b_bf16"],
+    "llama3_8b_fp8": ["llama3_8b_fp8"],
+}
+DESCRIPTION = {
+    "llama3_70b_fp8": "Llama-3.1-70B-shaped single-layer decode, FP8 E4M3 paged KV (per-tensor "
+                      "scales amax/448), Hq 64 / Hkv 8 / d 128, 16-token blocks, random block "
+                      "tables; batch A 4 x 131072 tokens + batch B 256 x 4096 tokens",
+    "llama3_70b_fp8_a": "Llama-3.1-70B-shaped FP8 decode, 4 x 131072 tokens",
+    "llama3_70b_fp8_b": "Llama-3.1-70B-shaped FP8 decode, 256 x 4096 tokens",
+    "llama3_8b_bf16": "Llama-3.1-8B-shaped bf16 decode, 64 seqs, ctx U[512,4096]",
+    "llama3_8b_fp8": "Llama-3.1-8B-shaped FP8 decode, 64 seqs, ctx U[512,4096], 1% K outliers",
+}
+
+# DRAM traffic per decode launch from one ncu capture, valid only while the
+# decode source is byte-identical to the one measured.
+NCU_TRAFFIC = {"source_sha256": None, "bytes_per_launch": {}}
+
+
+# --------------------------------------------------------------------- workers
+def _gen_amax(args):
+    name, s, lo, hi = args
+    from paged_kv_cache_270_gb300 import workloads as W
+    w = W.make(name)
+    k, v = w.kv_bits(s, lo, hi)
+    return (float(np.abs(W.bits_to_f32(k, w.in_dtype)).max(initial=0)),
+            float(np.abs(W.bits_to_f32(v, w.in_dtype)).max(initial=0)))
+
+
+def _gen_bits(args):
+    name, s, lo, hi = args
+    from paged_kv_cache_270_gb300 import workloads as W
+    w = W.make(name)
+    k, v = w.kv_bits(s, lo, hi)
+    return s, lo, hi, k, v
+
+
+def _oracle_worker(args):
+    """Times the fp64 oracle (gather + textbook attention) on some sequences of
+    a workload; returns (kv bytes, t_start, t_end)."""
+    name, seqs, k_scale, v_scale = args
+    import oracle
+    from paged_kv_cache_270_gb300 import workloads as W
+    w = W.make(name)
+    w.k_scale, w.v_scale = k_scale, v_scale
+    ids = []
+    for s in seqs:
+        ids += list(w.block_tables[s, : -(-int(w.ctx_lens[s]) // 16)])
+    remap = {b: i for i, b in enumerate(ids)}
+    tables = np.zeros((len(seqs), w.max_blocks), np.int32)
+    nbytes = oracle.pool_bytes(w.kv_dtype, len(ids), 16, w.n_kv_heads, w.head_dim)
+    kp, vp = np.zeros(nbytes, np.uint8), np.zeros(nbytes, np.uint8)
+    for r, s in enumerate(seqs):
+        n = int(w.ctx_lens[s])
+        nb = -(-n // 16)
+        tables[r, :nb] = [remap[b] for b in w.block_tables[s, :nb]]
+        k, v = w.kv_bits(s, 0, n)
+        pos = np.arange(n, dtype=np.int64)
+        slots = tables[r, pos // 16].astype(np.int64) * 16 + pos % 16
+        oracle.reshape_and_cache(w.kv_dtype, len(ids), 16, w.n_kv_heads, w.head_dim, k, v, slots,
+                                 w.k_scale, w.v_scale, kp, vp)
+    q = w.q_bits()[list(seqs)]
+    ctx = w.ctx_lens[list(seqs)]
+    t0 = time.time()
+    oracle.paged_attention(w.kv_dtype, w.in_dtype, len(ids), 16, w.n_kv_heads, w.head_dim, kp, vp,
+                           w.k_scale, w.v_scale, q, tables, ctx, w.softmax_scale)
+    t1 = time.time()
+    return w.kv_bytes(ctx), t0, t1
+
+
+# ------------------------------------------------------------------- helpers
+def _env_rank():
+    return (int(os.environ.get("RANK", 0)), int(os.environ.get("WORLD_SIZE", 1)),
+            int(os.environ.get("LOCAL_RANK", 0)))
+
+
+def _measured_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def _source_sha():
+    h = hashlib.sha256()
+    for f in ("pa_decode.cu", "pa_device.cuh"):
+        with open(os.path.join(ROOT, "paged_kv_cache_270_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()
+
+
+class ClockSampler:
+    """Samples SM clock, power and clock-event reasons through NVML while the
+    timed region runs (read-only queries)."""
+    REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown",
+               0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown",
+               0x2: "applications_clocks_setting", 0x1: "gpu_idle"}
+
+    def __init__(self, device_index: int):
+        self.samples = []
+        self.ok = False
+        self.max_mhz = None
+        try:
+            import torch
+            self.nvml = ctypes.CDLL("libnvidia-ml.so.1")
+            if self.nvml.nvmlInit_v2() != 0:
+                return
+            props = torch.cuda.get_device_properties(device_index)
+            bus = f"{props.pci_domain_id:08x}:{props.pci_bus_id:02x}:{props.pci_device_id:02x}.0"
+            self.h = ctypes.c_void_p()
+            if self.nvml.nvmlDeviceGetHandleByPciBusId_v2(bus.encode(), ctypes.byref(self.h)) != 0:
+                return
+            mx = ctypes.c_uint()
+            if self.nvml.nvmlDeviceGetMaxClockInfo(self.h, 1, ctypes.byref(mx)) == 0:
+                self.max_mhz = mx.value
+            self._reasons = getattr(self.nvml, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+                getattr(self.nvml, "nvmlDeviceGetCurrentClocksThrottleReasons")
+            self.ok = True
+        except Exception:
+            self.ok = False
+
+    def _sample(self):
+        c, p, r = ctypes.c_uint(), ctypes.c_uint(), ctypes.c_ulonglong()
+        self.nvml.nvmlDeviceGetClockInfo(self.h, 1, ctypes.byref(c))
+        self.nvml.nvmlDeviceGetPowerUsage(self.h, ctypes.byref(p))
+        self._reasons(self.h, ctypes.byref(r))
+        self.samples.append((c.value, p.value / 1000.0, r.value))
+
+    def __enter__(self):
+        self._stop = threading.Event()
+        if self.ok:
+            self._sample()
+
+            def loop():
+                while not self._stop.is_set():
+                    self._sample()
+                    time.sleep(0.002)
+            self._t = threading.Thread(target=loop, daemon=True)
+            self._t.start()
+        return self
+
+    def __exit__(self, *exc):
+        self._stop.set()
+        if self.ok:
+            self._t.join()
+            self._sample()
+
+    def summary(self):
+        if not self.ok or not self.samples:
+            return {"sm_mhz": None, "sm_max_mhz": self.max_mhz, "reasons": ["nvml unavailable"]}
+        reasons = set()
+        for _, _, r in self.samples:
+            for bit, name in self.REASONS.items():
+                if r & bit and name != "gpu_idle":
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(s[0] for s in self.samples),
+                "sm_max_mhz": self.max_mhz, "reasons": sorted(reasons),
+                "power_w_max": max(s[1] for s in self.samples), "samples": len(self.samples)}
+
+
+# --------------------------------------------------------------- GPU batches
+class Batch:
+    """One workload batch resident on the GPU: filled pool plus the step's inputs."""
+
+    def __init__(self, name, pool_procs):
+        import torch
+
+        from paged_kv_cache_270_gb300 import _native as N
+        from paged_kv_cache_270_gb300 import workloads as W
+        from paged_kv_cache_270_gb300.pool import KVPool
+        self.N = N
+        w = W.make(name)
+        self.w = w
+        S, Hq, D = w.S, w.n_q_heads, w.head_dim
+        chunks = []
+        for s in range(S):
+            n = int(w.final_ctx()[s])
+            for lo in range(0, n, 16384):
+                chunks.append((name, s, lo, min(n, lo + 16384)))
+        if w.kv_dtype == "fp8_e4m3":
+            ka = va = 0.0
+            for a, b in pool_procs.imap_unordered(_gen_amax, chunks, chunksize=4):
+                ka, va = max(ka, a), max(va, b)
+            w.k_scale = float(np.float32(ka) / np.float32(448.0))
+            w.v_scale = float(np.float32(va) / np.float32(448.0))
+        self.pool = KVPool(1, w.num_blocks, w.n_kv_heads, D, w.kv_dtype, w.k_scale, w.v_scale)
+        in_t = torch.float16 if w.in_dtype == "fp16" else torch.bfloat16
+        self.in_t = in_t
+        ctx = w.ctx_lens
+        last_k = np.zeros((S, w.n_kv_heads, D), np.uint16)
+        last_v = np.zeros_like(last_k)
+        for s, lo, hi, k, v in pool_procs.imap(_gen_bits, chunks, chunksize=2):
+            pos = np.arange(lo, hi, dtype=np.int64)
+            slots = w.block_tables[s, pos // 16].astype(np.int64) * 16 + pos % 16
+            self.pool.reshape_and_cache(
+                torch.from_numpy(k.view(np.int16)).view(in_t).cuda(non_blocking=False),
+                torch.from_numpy(v.view(np.int16)).view(in_t).cuda(non_blocking=False),
+                torch.from_numpy(slots).cuda())
+            if lo <= ctx[s] - 1 < hi:
+                last_k[s] = k[ctx[s] - 1 - lo]
+                last_v[s] = v[ctx[s] - 1 - lo]
+        torch.cuda.synchronize()
+        self.S, self.Hq, self.D = S, Hq, D
+        self.max_blocks = w.max_blocks
+        # host copies (pinned) of every per-step input, for the end-to-end run
+        q_bits = w.q_bits()
+        new_slots = (w.block_tables[np.arange(S), (ctx - 1) // 16].astype(np.int64) * 16 +
+                     (ctx - 1) % 16)
+        pin = lambda a: torch.from_numpy(np.ascontiguousarray(a)).pin_memory()  # noqa: E731
+        self.h_q = pin(q_bits.view(np.int16)).view(in_t)
+        self.h_k = pin(last_k.view(np.int16)).view(in_t)
+        self.h_v = pin(last_v.view(np.int16)).view(in_t)
+        self.h_slots = pin(new_slots)
+        self.h_tables = pin(w.block_tables.astype(np.int32))
+        self.h_ctx = pin(ctx.astype(np.int32))
+        self.d_q = self.h_q.cuda()
+        self.d_k = self.h_k.cuda()
+        self.d_v = self.h_v.cuda()
+        self.d_slots = self.h_slots.cuda()
+        self.d_tables = self.h_tables.cuda()
+        self.d_ctx = self.h_ctx.cuda()
+        self.d_out = torch.empty((S, Hq, D), dtype=in_t, device="cuda")
+        self.h_out = torch.empty((S, Hq, D), dtype=in_t).pin_memory()
+        self.splits = self.pool.num_splits(S, Hq, self.max_blocks)
+        self.ws_bytes = self.pool.workspace_bytes(S, Hq, self.max_blocks, 0)
+        self.ws = torch.empty(max(self.ws_bytes, 16), dtype=torch.uint8, device="cuda")
+        self.kv_bytes = w.kv_bytes()
+        self.h2d_bytes = sum(t.numel() * t.element_size() for t in
+                             (self.h_q, self.h_k, self.h_v, self.h_slots, self.h_tables,
+                              self.h_ctx))
+        self.d2h_bytes = self.h_out.numel() * self.h_out.element_size()
+        self.launches = 2 + (1 if self.splits > 1 else 0)
+        self.softmax_scale = w.softmax_scale
+        self.out_code = N.PA_FP16 if w.in_dtype == "fp16" else N.PA_BF16
+
+    def reshape(self, stream):
+        self.N.pa_reshape_and_cache(self.pool.handle, 0, self.d_k.data_ptr(), self.d_v.data_ptr(),
+                                    self.d_slots.data_ptr(), self.S, stream)
+
+    def decode(self, stream):
+        self.N.pa_decode(self.pool.handle, 0, self.d_out.data_ptr(), self.out_code,
+                         self.d_q.data_ptr(), self.d_tables.data_ptr(), self.max_blocks,
+                         self.d_ctx.data_ptr(), self.S, self.Hq, self.softmax_scale, 0,
+                         self.ws.data_ptr(), self.ws_bytes, stream)
+
+    def upload(self):
+        for d, h in ((self.d_q, self.h_q), (self.d_k, self.h_k), (self.d_v, self.h_v),
+                     (self.d_slots, self.h_slots), (self.d_tables, self.h_tables),
+                     (self.d_ctx, self.h_ctx)):
+            d.copy_(h, non_blocking=True)
+
+    def download(self):
+        self.h_out.copy_(self.d_out, non_blocking=True)
+
+
+def _barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def _max_over_ranks(x, world):
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def cpu_baseline(names, scales, seconds, procs, pool):
+    """Time the oracle on a bounded sample of the workload's sequences."""
+    # calibrate: one short sequence set first, then size the sample
+    from paged_kv_cache_270_gb300 import workloads as W
+    jobs = []
+    for name in names[-1:]:  # the batch with the most sequences: short ones sample evenly
+        w = W.make(name)
+        order = np.random.default_rng(17).permutation(w.S)
+        jobs.append((name, w, order))
+    name, w, order = jobs[-1]
+    probe = pool.map(_oracle_worker, [(name, [int(order[0])], *scales[name])])
+    b, t0, t1 = probe[0]
+    per_byte = (t1 - t0) / b
+    results, sample_desc = [], []
+    budget = seconds * procs
+    for name, w, order in jobs:
+        per_seq = w.kv_bytes(w.ctx_lens[:1]) * per_byte
+        n = max(1, min(w.S, int(budget / len(jobs) / max(per_seq, 1e-9))))
+        seqs = [int(s) for s in order[:n]]
+        groups = [seqs[i::procs] for i in range(procs) if seqs[i::procs]]
+        results += pool.map(_oracle_worker, [(name, g, *scales[name]) for g in groups])
+        sample_desc.append(f"{name}: {n} of {w.S} sequences")
+    total = sum(r[0] for r in results)
+    wall = max(r[2] for r in results) - min(r[1] for r in results)
+    return {"value": total / wall / 1e9, "unit": "GB/s", "cores": procs, "kind": "oracle",
+            "sample": "; ".join(sample_desc) + f" ({total / 1e6:.0f} MB of K+V, "
+                      f"{wall:.1f} s wall, fp64 gather + softmax attention)"}
+
+
+# ------------------------------------------------------------------- arms
+def run_gb300(args, rank, world, local_rank):
+    import torch
+    torch.cuda.set_device(local_rank)
+    names = WORKLOADS[args.workload]
+    ctx_mp = mp.get_context("spawn")
+    procs = max(1, min(os.cpu_count() or 1, 16))
+    with ctx_mp.Pool(procs) as pool_procs:
+        batches = [Batch(n, pool_procs) for n in names]
+        scales = {b.w.name: (b.w.k_scale, b.w.v_scale) for b in batches}
+        stream = torch.cuda.current_stream()
+        sh = int(stream.cuda_stream)
+
+        def step(evs=None):
+            for i, b in enumerate(batches):
+                b.reshape(sh)
+                if evs is not None:
+                    evs[i][0].record(stream)
+                b.decode(sh)
+                if evs is not None:
+                    evs[i][1].record(stream)
+
+        for _ in range(args.warmup):
+            step()
+        torch.cuda.synchronize()
+        for b in batches:
+            err = b.pool.device_error()
+            if err:
+                raise RuntimeError(f"device error {err} in {b.w.name}")
+        K = args.steps
+        evs = [[[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in batches]
+               for _ in range(K)]
+        start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        sampler = ClockSampler(local_rank)
+        _barrier(world)
+        torch.cuda.synchronize()
+        with sampler:
+            start.record(stream)
+            for k in range(K):
+                step(evs[k])
+            end.record(stream)
+            torch.cuda.synchronize()
+        _barrier(world)
+        t = start.elapsed_time(end) / 1e3
+        t_max = _max_over_ranks(t, world)
+        dec_ms = [[evs[k][i][0].elapsed_time(evs[k][i][1]) for k in range(K)]
+                  for i in range(len(batches))]
+
+        # end to end through the C ABI: pinned host inputs in, result out, every step
+        e2e = None
+        if not args.no_e2e:
+            for _ in range(max(1, args.warmup // 2)):
+                for b in batches:
+                    b.upload()
+                step()
+                for b in batches:
+                    b.download()
+                torch.cuda.synchronize()
+            _barrier(world)
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            for _ in range(K):
+                for b in batches:
+                    b.upload()
+                step()
+                for b in batches:
+                    b.download()
+                stream.synchronize()
+            e1.record(stream)
+            torch.cuda.synchronize()
+            te = _max_over_ranks(e0.elapsed_time(e1) / 1e3, world)
+            kv = sum(b.kv_bytes for b in batches)
+            e2e = {"value": world * kv * K / te / 1e9, "unit": "GB/s",
+                   "h2d_bytes_per_step": sum(b.h2d_bytes for b in batches),
+                   "d2h_bytes_per_step": sum(b.d2h_bytes for b in batches),
+                   "ms_per_step": te / K * 1e3}
+        for b in batches:
+            err = b.pool.device_error()
+            if err:
+                raise RuntimeError(f"device error {err} in {b.w.name}")
+
+        cpu = None
+        if rank == 0 and world == 1 and not args.no_cpu:
+            cpu = cpu_baseline(names, scales, args.cpu_seconds, procs, pool_procs)
+
+    if rank != 0:
+        return
+    kv = sum(b.kv_bytes for b in batches)
+    value = world * kv * K / t_max / 1e9
+    peak, peak_kind = _measured_peak()
+    dec_avg = [statistics.fmean(d) / 1e3 for d in dec_ms]  # s per launch, per batch
+    achieved = kv / sum(dec_avg) / 1e9
+    sha = _source_sha()
+    traffic = None
+    if NCU_TRAFFIC["source_sha256"] == sha and all(
+            b.w.name in NCU_TRAFFIC["bytes_per_launch"] for b in batches):
+        traffic = sum(NCU_TRAFFIC["bytes_per_launch"][b.w.name] for b in batches)
+    per_batch = {}
+    for b, d in zip(batches, dec_ms):
+        per_batch[b.w.name] = {
+            "sequences": b.S, "tokens_per_seq": int(b.w.ctx_lens.max()), "kv_bytes": b.kv_bytes,
+            "splits": b.splits, "decode_ms_median": statistics.median(d),
+            "decode_kv_gbs": b.kv_bytes / (statistics.median(d) / 1e3) / 1e9}
+    launches = K * sum(b.launches for b in batches)
+    line = {
+        "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world, "steps": K,
+        "warmup": args.warmup, "ms_per_step": round(t_max / K * 1e3, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "e4m3 KV / f16 tensor-core MMA / f32 accumulate"
+        if batches[0].w.kv_dtype == "fp8_e4m3" else f"{batches[0].w.kv_dtype} KV / f32 accumulate",
+        "data": "synthetic (seeded N(0,1) q/k/v, random block tables)",
+        "config": {"workload": DESCRIPTION[args.workload],
+                   "l2": "inputs larger than L2 (KV pool "
+                         f"{sum(b.pool.k_cache.numel() * 2 for b in batches) / 2**30:.2f} GiB)",
+                   "parallelism": f"replicas x{world}" if world > 1 else "1 GPU"},
+        "tokens_per_s": round(world * sum(b.S for b in batches) * K / t_max, 1),
+        "frac_of_spec_8tbs": round(value / SPEC_HBM_GBS, 4),
+        "frac_of_measured_peak": round(value / peak, 4),
+        "batches": per_batch,
+        "roofline": {"kernel": "pa_decode (decode kernel + split merge when splits > 1)",
+                     "bound": "hbm", "achieved": round(achieved, 1), "peak": peak,
+                     "peak_kind": f"{peak_kind} (hbm_gbs)", "unit": "GB/s",
+                     "frac": round(achieved / peak, 4), "traffic": traffic,
+                     "algorithmic_bytes_per_step": kv},
+        "cpu_baseline": cpu,
+        "e2e": e2e,
+        "gpu_launches": launches,
+        "clocks": sampler.summary(),
+    }
+    print(json.dumps(line), flush=True)
+
+
+def run_reference(args, rank, world):
+    """The fp64 oracle on the host cores, a bounded sample of the workload per step."""
+    if rank != 0:
+        return
+    names = WORKLOADS[args.workload]
+    from paged_kv_cache_270_gb300 import workloads as W
+    procs = max(1, min(os.cpu_count() or 1, 16))
+    ctx_mp = mp.get_context("spawn")
+    scales = {}
+    with ctx_mp.Pool(procs) as pool:
+        for name in names:
+            w = W.make(name)
+            if w.kv_dtype == "fp8_e4m3":
+                chunks = [(name, s, lo, min(int(w.ctx_lens[s]), lo + 16384))
+                          for s in range(w.S) for lo in range(0, int(w.ctx_lens[s]), 16384)]
+                ka = va = 0.0
+                for a, b in pool.imap_unordered(_gen_amax, chunks, chunksize=4):
+                    ka, va = max(ka, a), max(va, b)
+                scales[name] = (float(np.float32(ka) / np.float32(448.0)),
+                                float(np.float32(va) / np.float32(448.0)))
+            else:
+                scales[name] = (1.0, 1.0)
+        per_step = max(2.0, min(20.0, 150.0 / max(1, args.steps + args.warmup)))
+        for _ in range(args.warmup):
+            cpu_baseline(names, scales, per_step / 4, procs, pool)
+        vals, t_total = [], 0.0
+        last = None
+        for _ in range(args.steps):
+            t0 = time.time()
+            last = cpu_baseline(names, scales, per_step, procs, pool)
+            t_total += time.time() - t0
+            vals.append(last["value"])
+    value = statistics.fmean(vals)
+    line = {"impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "GB/s",
+            "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(t_total / args.steps * 1e3, 1), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic (seeded N(0,1) q/k/v, random block tables)",
+            "config": {"workload": DESCRIPTION[args.workload],
+                       "sample_per_step": last["sample"] if last else None},
+            "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": procs,
+                             "kind": "oracle", "sample": last["sample"] if last else None},
+            "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0},
+            "gpu_launches": 0}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__.splitlines()[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=100)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["gb300", "reference"], default="gb300")
+    ap.add_argument("--workload", choices=sorted(WORKLOADS), default="llama3_70b_fp8")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--no-cpu", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    rank, world, local_rank = _env_rank()
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl" if args.impl == "gb300" else "gloo")
+    try:
+        if args.impl == "reference":
+            run_reference(args, rank, world)
+        else:
+            run_gb300(args, rank, world, local_rank)
+    finally:
+        if world > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,241 @@
+/*
+ * pa.h -- C ABI of the paged KV-cache decode library (GB300, sm_103a).
+ *
+ * The KV cache lives in a flat physical pool of fixed-size blocks of 16 tokens;
+ * each sequence addresses it through a block table mapping logical block j to
+ * a physical block id, and the attention kernel gathers keys and values by
+ * that indirection instead of slicing a contiguous slab ("Capítulo 8 --
+ * Gestión de caché KV de nueva generación", section 8.1; "PagedAttention y
+ * Gestión de KV-Cache", section 2 figure).  The cache may hold FP8 E4M3 codes
+ * with a static per-tensor scale ("Optimización de KV Cache con
+ * PagedAttention y Cuantización FP8 para Contextos Largos (128K)", sections 4
+ * and 8).  Blocks are reference counted so sequences can share a prefix, with
+ * copy-on-write before a sequence appends into a shared block ("PagedAttention
+ * y Gestión de KV-Cache", sections 3.01 and 3.02; "KV Cache y PagedAttention",
+ * "Cómo PagedAttention soluciona esto").
+ *
+ * Conventions, for every function below:
+ *  - Returns a status: PA_OK (0) or one of the PA_ERR_* codes.  Nothing
+ *    throws across the ABI.  pa_last_error() gives the calling thread's last
+ *    message.
+ *  - Device pointers are owned by the caller.  The library never allocates or
+ *    frees device memory.  Host arrays passed in are read (or written, where
+ *    stated) during the call only.
+ *  - Functions taking a `stream` (a cudaStream_t passed as void*; NULL is the
+ *    legacy default stream) only enqueue work: they are asynchronous and do
+ *    not synchronise.  Problems found by a kernel (an out-of-range block id or
+ *    slot, a context longer than its table, a pipeline wait that timed out)
+ *    are recorded in a per-device error word; read it with
+ *    pa_get_device_error().  Kernels never trap: they skip the bad access.
+ *  - A pool handle is not thread-safe: use it from one thread at a time.
+ *  - Every device buffer must be 16-byte aligned.
+ *
+ * Pool layout in device memory (per layer l, for K and for V separately):
+ *   [num_blocks][n_kv_heads][block_size][head_dim] elements, layer l at byte
+ *   offset l * num_blocks * n_kv_heads * block_size * head_dim * elem_bytes.
+ *   One (block, kv head) tile of block_size * head_dim elements is contiguous.
+ */
+#ifndef PAGED_KV_PA_H
+#define PAGED_KV_PA_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define PA_API __attribute__((visibility("default")))
+#else
+#define PA_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* ---- status codes ---- */
+#define PA_OK 0
+#define PA_ERR_INVALID 1       /* bad argument or request (nothing changed) */
+#define PA_ERR_UNSUPPORTED 2   /* valid but not implemented (e.g. head_dim 96) */
+#define PA_ERR_OUT_OF_BLOCKS 3 /* the free list cannot satisfy an allocation */
+#define PA_ERR_NO_MEMORY 4     /* a budget that holds no block at all */
+#define PA_ERR_CUDA 5          /* a CUDA runtime call failed */
+#define PA_ERR_BOUNDS 6        /* a kernel met an out-of-range id, slot or length */
+#define PA_ERR_TIMEOUT 7       /* a kernel pipeline wait gave up (bounded spin) */
+
+/* ---- element types ---- */
+#define PA_FP16 0     /* IEEE binary16 */
+#define PA_BF16 1     /* bfloat16 */
+#define PA_FP8_E4M3 2 /* OCP FP8 E4M3FN codes, value = decode(code) * scale */
+#define PA_FP32 3     /* IEEE binary32 (decode output only: the fp32 check mode) */
+
+#define PA_BLOCK_SIZE 16
+
+/* Description of a KV pool.
+ *   n_layers    layers held by the pool (each layer has its own K and V region)
+ *   num_blocks  physical blocks per layer (>= 1)
+ *   block_size  tokens per block; must be 16
+ *   n_kv_heads  KV heads (>= 1)
+ *   head_dim    64 or 128
+ *   kv_dtype    PA_FP16, PA_BF16 or PA_FP8_E4M3.  FP16 pools take binary16
+ *               q/k/v; BF16 and FP8 pools take bfloat16 q/k/v.
+ *   k_scale, v_scale  FP8 only: static per-tensor scales (> 0, finite); a code
+ *               c stands for decode(c) * scale.  Ignored for 16-bit pools. */
+typedef struct pa_pool_desc {
+  int n_layers;
+  int num_blocks;
+  int block_size;
+  int n_kv_heads;
+  int head_dim;
+  int kv_dtype;
+  float k_scale;
+  float v_scale;
+} pa_pool_desc;
+
+typedef struct pa_pool pa_pool;
+
+/* Copies the calling thread's last error message into buf (NUL-terminated,
+ * truncated to n bytes).  Returns PA_OK. */
+PA_API int pa_last_error(char* buf, size_t n);
+
+/* KV bytes per token of a model: 2 * n_layers * n_kv_heads * head_dim *
+ * bytes(kv_dtype) -- one K and one V vector per KV head per layer
+ * ("Optimización de KV Cache ...", section 2, worked example 327,680 bytes for
+ * 80 layers, 8 KV heads, head dim 128, FP16; FP8 halves it, section 4). */
+PA_API int pa_kv_bytes_per_token(int n_layers, int n_kv_heads, int head_dim, int kv_dtype,
+                          size_t* bytes);
+
+/* Bytes of device memory the caller must provide for the K region and for the
+ * V region of a pool described by *desc (all layers). */
+PA_API int pa_pool_bytes(const pa_pool_desc* desc, size_t* k_bytes, size_t* v_bytes);
+
+/* Largest num_blocks whose K + V regions fit in budget_bytes (desc->num_blocks
+ * is ignored).  PA_ERR_NO_MEMORY if not even one block fits -- the "no
+ * available memory for the cache blocks" start-up failure ("Optimización de KV
+ * Cache ...", section 6.1). */
+PA_API int pa_pool_blocks_for_budget(const pa_pool_desc* desc, size_t budget_bytes, int* num_blocks);
+
+/* Creates a pool over caller-owned device regions k_cache and v_cache (each at
+ * least the pa_pool_bytes size, 16-byte aligned).  The host allocator starts
+ * with every block free; its LIFO free list hands out 0, 1, 2, ... first.
+ * The pool does not own the device memory. */
+PA_API int pa_pool_create(const pa_pool_desc* desc, void* k_cache, void* v_cache, pa_pool** out);
+
+/* Destroys the host state of a pool (device memory is untouched). NULL is OK. */
+PA_API int pa_pool_destroy(pa_pool* pool);
+
+/* Copies the pool's description into *desc. */
+PA_API int pa_pool_get_desc(const pa_pool* pool, pa_pool_desc* desc);
+
+/* ---- host block allocator ("Capítulo 8 ...", section 8.1: free list and
+ * reference-counted sharing; "PagedAttention y Gestión de KV-Cache",
+ * section 4.02: pages return to the free pool when a request ends) ---- */
+
+/* Allocates n blocks (refcount 1 each) into ids[0..n).  All or nothing:
+ * PA_ERR_OUT_OF_BLOCKS leaves the pool unchanged.  Freed blocks are reused
+ * first (LIFO). */
+PA_API int pa_block_alloc(pa_pool* pool, int n, int32_t* ids);
+
+/* Drops one reference from each of ids[0..n) (an id may repeat); a block whose
+ * count reaches 0 goes back on the free list, in argument order.
+ * PA_ERR_INVALID (and no change at all) if any id is out of range or would go
+ * below zero -- a double free. */
+PA_API int pa_block_free(pa_pool* pool, int n, const int32_t* ids);
+
+/* Adds one reference to each of ids[0..n) (sharing a block with another
+ * sequence).  PA_ERR_INVALID (no change) if any id is free or out of range. */
+PA_API int pa_block_incref(pa_pool* pool, int n, const int32_t* ids);
+
+/* Current reference count of block id (0 = free). */
+PA_API int pa_block_refcount(const pa_pool* pool, int32_t id, int* refcount);
+
+/* Blocks in use (refcount > 0), free, and shared (refcount > 1); any output
+ * pointer may be NULL.  used / num_blocks is the cache usage factor a serving
+ * monitor watches ("Optimización de KV Cache ...", section 7). */
+PA_API int pa_pool_stats(const pa_pool* pool, int* used, int* free_blocks, int* shared);
+
+/* Copy-on-write preparation for appending token number ctx_len (0-based) to a
+ * sequence whose block table is table_row (host array, at least
+ * ctx_len / 16 + 1 entries).  If the token falls inside an existing block
+ * (ctx_len % 16 != 0) whose refcount is above 1, a new block is allocated, the
+ * shared one loses a reference, table_row[ctx_len / 16] is rewritten to the
+ * new id, and (*src, *dst) = (old, new) with *n_pairs = 1: the caller then
+ * copies the block contents with pa_copy_blocks before writing the token.
+ * Otherwise *n_pairs = 0 and nothing changes (a token that opens a new block
+ * needs pa_block_alloc, not a copy).  PA_ERR_OUT_OF_BLOCKS if no block is
+ * free (no change). */
+PA_API int pa_cow_prepare(pa_pool* pool, int32_t* table_row, int ctx_len, int32_t* src, int32_t* dst,
+                   int* n_pairs);
+
+/* ---- device operations ---- */
+
+/* For each pair p < n_pairs of pairs_dev (device int32 [n_pairs][2] =
+ * (src, dst)), copies the K and V tiles of every KV head of block src into
+ * block dst, in layer `layer` (the device half of copy-on-write).  Pairs with
+ * an id outside [0, num_blocks) are skipped and set PA_ERR_BOUNDS in the device
+ * error word.  Destinations must be distinct and no destination may also be a
+ * source in the same call. */
+PA_API int pa_copy_blocks(pa_pool* pool, int layer, const int32_t* pairs_dev, int n_pairs, void* stream);
+
+/* Writes T new tokens into their slots of layer `layer` (scatter through the
+ * slot mapping; pages are filled on demand, "Optimización de KV Cache ...",
+ * section 3).
+ *   k, v              device [T][n_kv_heads][head_dim], binary16 for FP16
+ *                     pools, bfloat16 for BF16 and FP8 pools
+ *   slot_mapping_dev  device int64 [T]: slot = block * 16 + offset, or negative
+ *                     to skip the token; a slot >= num_blocks * 16 is skipped
+ *                     and sets PA_ERR_BOUNDS in the device error word
+ * FP8 pools store code = E4M3(round-to-nearest-even, saturating to +-448) of
+ * the IEEE fp32 quotient x / scale ("Optimización de KV Cache ...", sections 4
+ * and 8, static calibration).  16-bit pools store x unchanged.  Two tokens with
+ * the same slot in one call race. */
+PA_API int pa_reshape_and_cache(pa_pool* pool, int layer, const void* k, const void* v,
+                         const int64_t* slot_mapping_dev, int T, void* stream);
+
+/* Number of splits pa_decode uses along each sequence's pages for this batch
+ * shape when num_splits = 0 (auto): enough (sequence, KV head, split) work
+ * units to fill the GPU, each split still covering several pages.
+ * Uses the current CUDA device. */
+PA_API int pa_decode_num_splits(const pa_pool* pool, int S, int n_q_heads, int max_blocks_per_seq,
+                         int* num_splits);
+
+/* Device scratch bytes pa_decode needs for this shape and split count
+ * (num_splits = 0: the automatic choice).  0 when one split is used. */
+PA_API int pa_decode_workspace_bytes(const pa_pool* pool, int S, int n_q_heads, int max_blocks_per_seq,
+                              int num_splits, size_t* bytes);
+
+/* Paged decode attention, one query token per sequence, for layer `layer`.
+ *   out               device [S][n_q_heads][head_dim] of out_dtype: the query
+ *                     dtype (PA_FP16 for FP16 pools, PA_BF16 otherwise), or
+ *                     PA_FP32 (the fp32 check mode)
+ *   q                 device [S][n_q_heads][head_dim], same dtype as the
+ *                     pool's inputs
+ *   block_tables_dev  device int32 [S][max_blocks_per_seq]
+ *   ctx_lens_dev      device int32 [S]: tokens of context of each sequence,
+ *                     including the token written this step; 0 gives a zero
+ *                     output row
+ *   softmax_scale     multiplies q.k (usually 1/sqrt(head_dim))
+ *   num_splits        0 = automatic; else the number of splits along the pages
+ *                     (a second kernel merges the partial results)
+ *   workspace         device scratch of at least pa_decode_workspace_bytes
+ *                     (may be NULL when that size is 0)
+ * Query head g reads KV head g / (n_q_heads / n_kv_heads) (grouped-query
+ * attention); n_q_heads / n_kv_heads must be between 1 and 8.  For each
+ * sequence the result is softmax(softmax_scale * q K^T) V over its first
+ * ctx_len tokens, gathered page by page through its block table ("Capítulo 8
+ * ...", section 8.1).  Table entries beyond ceil(ctx_len / 16) are not read.
+ * An id outside [0, num_blocks) or ctx_len > 16 * max_blocks_per_seq sets
+ * PA_ERR_BOUNDS in the device error word (the output is then undefined). */
+PA_API int pa_decode(pa_pool* pool, int layer, void* out, int out_dtype, const void* q,
+              const int32_t* block_tables_dev, int max_blocks_per_seq, const int32_t* ctx_lens_dev,
+              int S, int n_q_heads, float softmax_scale, int num_splits, void* workspace,
+              size_t workspace_bytes, void* stream);
+
+/* Synchronises `stream`, then reads and clears the current device's error word.
+ * *code = PA_OK or the first PA_ERR_* a kernel recorded since the last read.
+ * The word is shared by every pool on the device. */
+PA_API int pa_get_device_error(pa_pool* pool, int* code, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PAGED_KV_PA_H */

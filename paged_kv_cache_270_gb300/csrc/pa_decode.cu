@@ -1,0 +1,692 @@
+// pa_decode.cu -- paged decode attention for sm_103a.
+//
+// One query token per sequence attends to its whole paged history: the
+// kernel takes the block table as an extra input and gathers each 16-token
+// page of keys and values by indirection instead of slicing a contiguous slab
+// ("Capítulo 8 -- Gestión de caché KV de nueva generación", section 8.1).
+// Pages may hold FP8 E4M3 codes with a static per-tensor scale, dequantised as
+// they are used ("Optimización de KV Cache con PagedAttention y Cuantización
+// FP8 para Contextos Largos (128K)", sections 4 and 8).  Long contexts (up to
+// the 128K of that page's title) are split along their pages; a second kernel
+// merges the partial softmax states.
+//
+// Kernel design (not from the pages; they give none):
+//  * grid = (split, kv head, sequence); 5 warps per CTA.
+//  * Warp 4 is the producer: it reads the sequence's block-table entries 32 at a
+//    time (one coalesced load) and issues, per page, two 1-D TMA bulk copies
+//    (the contiguous K tile and V tile of this kv head, 16 x head_dim
+//    elements each) into an 8-stage shared-memory ring, completing on an
+//    mbarrier.  The tiles are streamed once, so they carry an L2 evict-first
+//    hint.
+//  * Warps 0..3 consume whole pages round-robin in logical order.  The whole
+//    grouped-query group (G <= 8 query heads sharing this kv head) is resident,
+//    so every KV byte is read from HBM exactly once per decode.
+//  * S^T = K_page * Q^T is one m16n8k16 tensor-core MMA per 16 dims
+//    (M = 16 tokens of the page, N = 8 query heads, fp32 accumulate); the
+//    online softmax runs in the log2 domain on the accumulator fragment; P is
+//    transposed in registers (movmatrix) into the B operand of
+//    O^T += V_page^T * P^T (M = 16 dims per MMA, K = the 16 tokens).
+//    Any permutation of the head dimension that Q and K share leaves q.k
+//    unchanged, so each thread loads a contiguous 16-byte run of a K row and
+//    the matching Q run; for V each thread owns a contiguous run of output
+//    dims and byte-permutes token pairs into the A operand.
+//  * FP8 codes convert exactly to binary16; q (bfloat16) is rescaled by a power
+//    of two so the group's largest |q| lands in [2^14, 2^15) before rounding to
+//    binary16, and the scale is folded back into the softmax exponent.  For
+//    bfloat16 pools (and in fp32-output mode) P is split into a high and a low
+//    16-bit part, two MMAs, so P carries ~16 significant bits.
+//  * Accumulation follows logical page order within each warp and a fixed warp
+//    order in the merge, so the result is bit-identical under any relabelling
+//    of physical blocks.
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cmath>
+#include <mutex>
+
+#include "pa_device.cuh"
+
+namespace pa {
+
+enum KvKind { KV_F16 = 0, KV_BF16 = 1, KV_E4M3 = 2 };
+enum OutKind { OUT_F16 = 0, OUT_BF16 = 1, OUT_F32 = 3 };
+
+constexpr int kConsumerWarps = 4;
+constexpr int kThreads = (kConsumerWarps + 1) * 32;
+constexpr unsigned kFull = 0xffffffffu;
+
+template <int KV, int D>
+struct Cfg {
+  static constexpr int kElem = (KV == KV_E4M3) ? 1 : 2;
+  static constexpr int kTile = 16 * D * kElem;  // bytes of one (block, kv head) tile
+  static constexpr int kStages = 8;
+  static constexpr int kStageBytes = 2 * kTile;  // K tile + V tile
+  static constexpr int kRingBytes = kStages * kStageBytes;
+  static constexpr int kMergeBytes = kConsumerWarps * 8 * (D + 2) * 4;
+  static constexpr int kDataBytes = kRingBytes > kMergeBytes ? kRingBytes : kMergeBytes;
+  static constexpr int kSmem = kDataBytes + 2 * kStages * 8;
+  static constexpr bool kMmaBf16 = (KV == KV_BF16);
+};
+
+struct DecodeArgs {
+  const uint8_t* kpool;  // this layer's K region
+  const uint8_t* vpool;  // this layer's V region
+  const uint16_t* q;     // [S][Hq][D]
+  void* out;             // [S][Hq][D]
+  float* ws_o;           // [S][Hq][splits][D]      (splits > 1)
+  float* ws_ml;          // [S][Hq][splits][2]      (m in log2 units, l)
+  const int32_t* tables;
+  const int32_t* ctx;
+  int max_blocks;
+  int Hq, Hkv, G, num_blocks;
+  int splits, pages_per_split;
+  float qk_scale_log2;  // softmax_scale * log2(e) (* k_scale for FP8)
+  float v_scale;        // 1 for 16-bit pools
+  unsigned int* err;
+};
+
+template <int OUT>
+__device__ __forceinline__ void store_out(void* out, size_t idx, float v) {
+  if constexpr (OUT == OUT_F32) {
+    static_cast<float*>(out)[idx] = v;
+  } else if constexpr (OUT == OUT_BF16) {
+    static_cast<__nv_bfloat16*>(out)[idx] = __float2bfloat16_rn(v);
+  } else {
+    static_cast<__half*>(out)[idx] = __float2half_rn(v);
+  }
+}
+
+template <int KV, int D, int OUT, bool PSPLIT>
+__global__ void __launch_bounds__(kThreads) decode_kernel(const DecodeArgs a) {
+  using C = Cfg<KV, D>;
+  constexpr bool BF = C::kMmaBf16;
+  constexpr int NT = D / 16;  // MMA steps along the head dim (QK) / m-tiles (PV)
+  extern __shared__ __align__(128) uint8_t smem[];
+  uint8_t* ring = smem;
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::kDataBytes);
+  uint64_t* empty = full + C::kStages;
+
+  const int split = blockIdx.x, h = blockIdx.y, seq = blockIdx.z;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  int ctx = a.ctx[seq];
+  if (ctx < 0 || ctx > a.max_blocks * 16) {
+    if (threadIdx.x == 0) record_error(a.err, PA_ERR_BOUNDS);
+    ctx = ctx < 0 ? 0 : a.max_blocks * 16;
+  }
+  const int npages = (ctx + 15) >> 4;
+  const int p_begin = split * a.pages_per_split;
+  const int n_local = max(0, min(npages, p_begin + a.pages_per_split) - p_begin);
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < C::kStages; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    fence_barrier_init();
+  }
+  __syncthreads();
+
+  // per-thread softmax state of query heads 2t and 2t+1 (log2 domain)
+  float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
+  float o[NT][4];
+#pragma unroll
+  for (int i = 0; i < NT; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
+
+  if (warp == kConsumerWarps) {
+    // ------------------------------------------------------------ producer
+    const int32_t* trow = a.tables + (size_t)seq * a.max_blocks + p_begin;
+    const uint64_t policy = l2_evict_first_policy();
+    const size_t blk_stride = (size_t)a.Hkv * C::kTile;
+    const uint8_t* kbase = a.kpool + (size_t)h * C::kTile;
+    const uint8_t* vbase = a.vpool + (size_t)h * C::kTile;
+    int issued = 0;
+    bool abort = false;
+    for (int base = 0; base < n_local && !abort; base += 32) {
+      int phys = 0;
+      if (base + lane < n_local) {
+        phys = trow[base + lane];
+        if (phys < 0 || phys >= a.num_blocks) {
+          record_error(a.err, PA_ERR_BOUNDS);
+          phys = 0;
+        }
+      }
+      const int cnt = min(32, n_local - base);
+      for (int j = 0; j < cnt; ++j) {
+        const int ph = __shfl_sync(kFull, phys, j);
+        int stop = 0;
+        if (lane == 0) {
+          const int k = base + j, stage = k % C::kStages;
+          if (k >= C::kStages && !mbar_wait(&empty[stage], ((k / C::kStages) - 1) & 1)) {
+            record_error(a.err, PA_ERR_TIMEOUT);
+            stop = 1;
+          } else {
+            uint8_t* dst = ring + stage * C::kStageBytes;
+            mbar_arrive_expect_tx(&full[stage], 2 * C::kTile);
+            bulk_g2s(dst, kbase + (size_t)ph * blk_stride, C::kTile, &full[stage], policy);
+            bulk_g2s(dst + C::kTile, vbase + (size_t)ph * blk_stride, C::kTile, &full[stage],
+                     policy);
+            ++issued;
+          }
+        }
+        if (__shfl_sync(kFull, stop, 0)) {
+          abort = true;
+          break;
+        }
+      }
+    }
+    // Wait (bounded) until every copy this CTA issued has landed, so no bulk
+    // write can still target the ring when it is reused or the CTA exits.
+    if (lane == 0) {
+      for (int s = 0; s < C::kStages && s < issued; ++s) {
+        const int uses = (issued - 1 - s) / C::kStages + 1;
+        if (!mbar_wait(&full[s], (uses - 1) & 1)) record_error(a.err, PA_ERR_TIMEOUT);
+      }
+    }
+  } else {
+    // ------------------------------------------------------------ consumers
+    const int g = lane >> 2, t = lane & 3;
+    // Q fragment: query head h*G + g (zero when g >= G), dims [t*D/4, (t+1)*D/4)
+    constexpr int QW = D / 8;  // 32-bit words per thread
+    uint32_t qf[QW];
+    float qk_scale = a.qk_scale_log2;
+    {
+      const uint4* qsrc = reinterpret_cast<const uint4*>(
+          a.q + ((size_t)seq * a.Hq + (size_t)h * a.G + g) * D + t * (D / 4));
+      uint32_t raw[QW];
+#pragma unroll
+      for (int c = 0; c < QW / 4; ++c) {
+        uint4 u = make_uint4(0, 0, 0, 0);
+        if (g < a.G) u = qsrc[c];
+        raw[4 * c] = u.x;
+        raw[4 * c + 1] = u.y;
+        raw[4 * c + 2] = u.z;
+        raw[4 * c + 3] = u.w;
+      }
+      if constexpr (KV == KV_E4M3) {
+        // bfloat16 q -> binary16 with a power-of-two prescale shared by the group
+        float amax = 0.f;
+#pragma unroll
+        for (int w = 0; w < QW; ++w) {
+          amax = fmaxf(amax, fabsf(bf16_bits_to_float(raw[w] & 0xFFFFu)));
+          amax = fmaxf(amax, fabsf(bf16_bits_to_float(raw[w] >> 16)));
+        }
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) amax = fmaxf(amax, __shfl_xor_sync(kFull, amax, off));
+        int ex = 0;
+        if (amax > 0.f) frexpf(amax, &ex);
+        const float qs = amax > 0.f ? ldexpf(1.f, 15 - ex) : 1.f;
+        qk_scale = amax > 0.f ? qk_scale * ldexpf(1.f, ex - 15) : qk_scale;
+#pragma unroll
+        for (int w = 0; w < QW; ++w)
+          qf[w] = pack2<false>(bf16_bits_to_float(raw[w] & 0xFFFFu) * qs,
+                               bf16_bits_to_float(raw[w] >> 16) * qs);
+      } else {
+#pragma unroll
+        for (int w = 0; w < QW; ++w) qf[w] = raw[w];
+      }
+    }
+
+    constexpr int KB = D / 4 * C::kElem;  // K bytes per row per thread
+    constexpr int VB = D / 8 * C::kElem;  // V bytes per row per thread
+    constexpr int RB = D * C::kElem;      // bytes per token row of a tile
+
+    for (int k = warp; k < n_local; k += kConsumerWarps) {
+      const int stage = k % C::kStages;
+      // every lane waits (acquiring the TMA writes); the verdict is made warp-uniform
+      if (!__all_sync(kFull, mbar_wait(&full[stage], (k / C::kStages) & 1))) {
+        if (lane == 0) record_error(a.err, PA_ERR_TIMEOUT);
+        break;
+      }
+      const uint8_t* Ks = ring + stage * C::kStageBytes;
+      const uint8_t* Vs = Ks + C::kTile;
+      const int tok0 = (p_begin + k) * 16;
+
+      // ---- S^T[token][head] = K_page . Q^T
+      float s[4] = {0.f, 0.f, 0.f, 0.f};
+      {
+        const uint8_t* kr0 = Ks + g * RB + t * KB;
+        const uint8_t* kr1 = kr0 + 8 * RB;
+#pragma unroll
+        for (int c = 0; c < KB / 16; ++c) {
+          const uint4 r0 = lds128(kr0 + 16 * c), r1 = lds128(kr1 + 16 * c);
+          if constexpr (KV == KV_E4M3) {
+            const uint32_t w0[4] = {r0.x, r0.y, r0.z, r0.w};
+            const uint32_t w1[4] = {r1.x, r1.y, r1.z, r1.w};
+#pragma unroll
+            for (int jj = 0; jj < 4; ++jj) {
+              const int j = 4 * c + jj;
+              const uint32_t af[4] = {e4m3x2_to_f16x2(w0[jj]), e4m3x2_to_f16x2(w1[jj]),
+                                      e4m3x2_to_f16x2(w0[jj] >> 16),
+                                      e4m3x2_to_f16x2(w1[jj] >> 16)};
+              mma16816<false>(s, af, qf[2 * j], qf[2 * j + 1]);
+            }
+          } else {
+            const uint32_t a0[4] = {r0.x, r1.x, r0.y, r1.y};
+            mma16816<BF>(s, a0, qf[4 * c], qf[4 * c + 1]);
+            const uint32_t a1[4] = {r0.z, r1.z, r0.w, r1.w};
+            mma16816<BF>(s, a1, qf[4 * c + 2], qf[4 * c + 3]);
+          }
+        }
+      }
+
+      // ---- online softmax over this page (tokens g and g+8; heads 2t, 2t+1)
+      const bool ok0 = tok0 + g < ctx, ok1 = tok0 + g + 8 < ctx;
+      const float x0 = ok0 ? s[0] * qk_scale : -INFINITY;
+      const float x1 = ok0 ? s[1] * qk_scale : -INFINITY;
+      const float x2 = ok1 ? s[2] * qk_scale : -INFINITY;
+      const float x3 = ok1 ? s[3] * qk_scale : -INFINITY;
+      float pm0 = fmaxf(x0, x2), pm1 = fmaxf(x1, x3);
+#pragma unroll
+      for (int off = 4; off < 32; off <<= 1) {
+        pm0 = fmaxf(pm0, __shfl_xor_sync(kFull, pm0, off));
+        pm1 = fmaxf(pm1, __shfl_xor_sync(kFull, pm1, off));
+      }
+      // token 0 of every page is valid, so the new maxima are finite
+      const float mn0 = fmaxf(m0, pm0), mn1 = fmaxf(m1, pm1);
+      const float al0 = exp2f(m0 - mn0), al1 = exp2f(m1 - mn1);
+      const float p0 = exp2f(x0 - mn0), p1 = exp2f(x1 - mn1);
+      const float p2 = exp2f(x2 - mn0), p3 = exp2f(x3 - mn1);
+      m0 = mn0;
+      m1 = mn1;
+      l0 = l0 * al0 + (p0 + p2);
+      l1 = l1 * al1 + (p1 + p3);
+#pragma unroll
+      for (int i = 0; i < NT; ++i) {
+        o[i][0] *= al0;
+        o[i][1] *= al1;
+        o[i][2] *= al0;
+        o[i][3] *= al1;
+      }
+
+      // ---- P^T as the B operand: rows (tokens 2t, 2t+1 | 2t+8, 2t+9), column head g
+      const uint32_t plo = pack2<BF>(p0, p1), phi = pack2<BF>(p2, p3);
+      const uint32_t pb0 = movmatrix_trans(plo), pb1 = movmatrix_trans(phi);
+      uint32_t rb0 = 0, rb1 = 0;
+      if constexpr (PSPLIT) {
+        const float2 u0 = unpack2<BF>(plo), u1 = unpack2<BF>(phi);
+        rb0 = movmatrix_trans(pack2<BF>(p0 - u0.x, p1 - u0.y));
+        rb1 = movmatrix_trans(pack2<BF>(p2 - u1.x, p3 - u1.y));
+      }
+
+      // ---- O^T[dim][head] += V_page^T . P^T
+      {
+        const uint8_t* vr = Vs + g * VB;
+        const int rows[4] = {2 * t, 2 * t + 1, 2 * t + 8, 2 * t + 9};
+        constexpr int VW = VB / 4;  // words per row per thread
+        uint32_t vw[4][VW];
+#pragma unroll
+        for (int r = 0; r < 4; ++r) {
+          if constexpr (VB == 8) {
+            const uint2 u = lds64(vr + rows[r] * RB);
+            vw[r][0] = u.x;
+            vw[r][1] = u.y;
+          } else {
+#pragma unroll
+            for (int c = 0; c < VB / 16; ++c) {
+              const uint4 u = lds128(vr + rows[r] * RB + 16 * c);
+              vw[r][4 * c] = u.x;
+              vw[r][4 * c + 1] = u.y;
+              vw[r][4 * c + 2] = u.z;
+              vw[r][4 * c + 3] = u.w;
+            }
+          }
+        }
+        if (tok0 + 16 > ctx) {  // last, partial page: slots past ctx may hold anything
+#pragma unroll
+          for (int r = 0; r < 4; ++r)
+            if (tok0 + rows[r] >= ctx) {
+#pragma unroll
+              for (int w = 0; w < VW; ++w) vw[r][w] = 0u;
+            }
+        }
+#pragma unroll
+        for (int i = 0; i < NT; ++i) {
+          uint32_t af[4];
+          if constexpr (KV == KV_E4M3) {
+            const uint32_t sel = (i & 1) ? 0x7362u : 0x5140u;
+            const uint32_t x01 = __byte_perm(vw[0][i >> 1], vw[1][i >> 1], sel);
+            const uint32_t x23 = __byte_perm(vw[2][i >> 1], vw[3][i >> 1], sel);
+            af[0] = e4m3x2_to_f16x2(x01);
+            af[1] = e4m3x2_to_f16x2(x01 >> 16);
+            af[2] = e4m3x2_to_f16x2(x23);
+            af[3] = e4m3x2_to_f16x2(x23 >> 16);
+          } else {
+            af[0] = __byte_perm(vw[0][i], vw[1][i], 0x5410u);
+            af[1] = __byte_perm(vw[0][i], vw[1][i], 0x7632u);
+            af[2] = __byte_perm(vw[2][i], vw[3][i], 0x5410u);
+            af[3] = __byte_perm(vw[2][i], vw[3][i], 0x7632u);
+          }
+          mma16816<BF>(o[i], af, pb0, pb1);
+          if constexpr (PSPLIT) mma16816<BF>(o[i], af, rb0, rb1);
+        }
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&empty[stage]);
+    }
+#pragma unroll
+    for (int off = 4; off < 32; off <<= 1) {
+      l0 += __shfl_xor_sync(kFull, l0, off);
+      l1 += __shfl_xor_sync(kFull, l1, off);
+    }
+  }
+
+  __syncthreads();  // the ring is idle from here on: reuse it for the merge
+
+  float* mo = reinterpret_cast<float*>(smem);          // [warp][8 heads][D]
+  float* mml = mo + kConsumerWarps * 8 * D;            // [warp][8 heads][2]
+  if (warp < kConsumerWarps) {
+    const int g = lane >> 2, t = lane & 3;
+    float* mw = mo + warp * 8 * D;
+#pragma unroll
+    for (int i = 0; i < NT; ++i) {
+      const int d0 = g * (D / 8) + 2 * i;  // output dims held by this thread
+      mw[(2 * t) * D + d0] = o[i][0];
+      mw[(2 * t + 1) * D + d0] = o[i][1];
+      mw[(2 * t) * D + d0 + 1] = o[i][2];
+      mw[(2 * t + 1) * D + d0 + 1] = o[i][3];
+    }
+    if (g == 0) {
+      float* ml = mml + warp * 16;
+      ml[4 * t + 0] = m0;
+      ml[4 * t + 1] = l0;
+      ml[4 * t + 2] = m1;
+      ml[4 * t + 3] = l1;
+    }
+  }
+  __syncthreads();
+
+  const size_t row0 = (size_t)seq * a.Hq + (size_t)h * a.G;
+  for (int idx = threadIdx.x; idx < a.G * D; idx += kThreads) {
+    const int head = idx / D, dim = idx - head * D;
+    float M = -INFINITY;
+#pragma unroll
+    for (int w = 0; w < kConsumerWarps; ++w) M = fmaxf(M, mml[w * 16 + 2 * head]);
+    float L = 0.f, O = 0.f;
+    if (M != -INFINITY) {
+#pragma unroll
+      for (int w = 0; w < kConsumerWarps; ++w) {
+        const float mw = mml[w * 16 + 2 * head];
+        const float f = (mw == -INFINITY) ? 0.f : exp2f(mw - M);
+        L += f * mml[w * 16 + 2 * head + 1];
+        O += f * mo[(w * 8 + head) * D + dim];
+      }
+    }
+    if (a.splits == 1) {
+      store_out<OUT>(a.out, (row0 + head) * D + dim, L > 0.f ? O / L * a.v_scale : 0.f);
+    } else {
+      const size_t prow = (row0 + head) * a.splits + split;
+      a.ws_o[prow * D + dim] = O;
+      if (dim == 0) {
+        a.ws_ml[2 * prow] = M;
+        a.ws_ml[2 * prow + 1] = L;
+      }
+    }
+  }
+}
+
+// Merge of the per-split partial states: one warp per (sequence, query head).
+template <int D, int OUT>
+__global__ void __launch_bounds__(128) reduce_kernel(const float* __restrict__ ws_o,
+                                                     const float* __restrict__ ws_ml, void* out,
+                                                     int rows, int splits, float v_scale) {
+  const int row = blockIdx.x * 4 + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  if (row >= rows) return;
+  constexpr int PER = D / 32;
+  const float* ml = ws_ml + (size_t)row * splits * 2;
+  float M = -INFINITY;
+  for (int s = 0; s < splits; ++s) M = fmaxf(M, ml[2 * s]);
+  float L = 0.f, O[PER];
+#pragma unroll
+  for (int j = 0; j < PER; ++j) O[j] = 0.f;
+  if (M != -INFINITY) {
+    const float* po = ws_o + (size_t)row * splits * D + lane * PER;
+    for (int s = 0; s < splits; ++s) {
+      const float ms = ml[2 * s];
+      const float f = (ms == -INFINITY) ? 0.f : exp2f(ms - M);
+      L += f * ml[2 * s + 1];
+      if constexpr (PER == 4) {
+        const float4 v = *reinterpret_cast<const float4*>(po + (size_t)s * D);
+        O[0] += f * v.x;
+        O[1] += f * v.y;
+        O[2] += f * v.z;
+        O[3] += f * v.w;
+      } else {
+        const float2 v = *reinterpret_cast<const float2*>(po + (size_t)s * D);
+        O[0] += f * v.x;
+        O[1] += f * v.y;
+      }
+    }
+  }
+  const float inv = L > 0.f ? v_scale / L : 0.f;
+#pragma unroll
+  for (int j = 0; j < PER; ++j) store_out<OUT>(out, (size_t)row * D + lane * PER + j, O[j] * inv);
+}
+
+// ---------------------------------------------------------------- host side
+struct KernelInfo {
+  const void* fn;
+  int smem;
+  int occupancy[128];  // per device, 0 = not yet configured
+};
+
+template <int KV, int D, int OUT>
+struct Launcher {
+  static constexpr bool kPsplit = (KV == KV_BF16) || (OUT == OUT_F32);
+  static KernelInfo& info() {
+    static KernelInfo ki = {reinterpret_cast<const void*>(&decode_kernel<KV, D, OUT, kPsplit>),
+                            Cfg<KV, D>::kSmem,
+                            {}};
+    return ki;
+  }
+  static cudaError_t launch(const DecodeArgs& a, int S, cudaStream_t st) {
+    dim3 grid(a.splits, a.Hkv, S);
+    decode_kernel<KV, D, OUT, kPsplit><<<grid, kThreads, Cfg<KV, D>::kSmem, st>>>(a);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess || a.splits == 1) return e;
+    const int rows = S * a.Hq;
+    reduce_kernel<D, OUT><<<(rows + 3) / 4, 128, 0, st>>>(a.ws_o, a.ws_ml, a.out, rows, a.splits,
+                                                         a.v_scale);
+    return cudaGetLastError();
+  }
+};
+
+struct Dispatch {
+  KernelInfo* info;
+  cudaError_t (*launch)(const DecodeArgs&, int, cudaStream_t);
+};
+
+template <int KV, int D, int OUT>
+Dispatch make_dispatch() {
+  return {&Launcher<KV, D, OUT>::info(), &Launcher<KV, D, OUT>::launch};
+}
+
+template <int KV, int D>
+Dispatch pick_out(int out_dtype) {
+  if (out_dtype == PA_FP32) return make_dispatch<KV, D, OUT_F32>();
+  if constexpr (KV == KV_F16) return make_dispatch<KV, D, OUT_F16>();
+  else return make_dispatch<KV, D, OUT_BF16>();
+}
+
+template <int KV>
+Dispatch pick_d(int head_dim, int out_dtype) {
+  return head_dim == 64 ? pick_out<KV, 64>(out_dtype) : pick_out<KV, 128>(out_dtype);
+}
+
+Dispatch pick(int kv_dtype, int head_dim, int out_dtype) {
+  switch (kv_dtype) {
+    case PA_FP16:
+      return pick_d<KV_F16>(head_dim, out_dtype);
+    case PA_BF16:
+      return pick_d<KV_BF16>(head_dim, out_dtype);
+    default:
+      return pick_d<KV_E4M3>(head_dim, out_dtype);
+  }
+}
+
+// Sets the shared-memory opt-in once per device and returns resident CTAs per SM.
+int configure(KernelInfo& ki, int dev) {
+  static std::mutex mu;
+  std::lock_guard<std::mutex> lock(mu);
+  if (dev < 0 || dev >= 128) return 0;
+  if (ki.occupancy[dev] > 0) return ki.occupancy[dev];
+  if (cudaFuncSetAttribute(ki.fn, cudaFuncAttributeMaxDynamicSharedMemorySize, ki.smem) !=
+      cudaSuccess)
+    return 0;
+  int occ = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, ki.fn, kThreads, ki.smem) != cudaSuccess)
+    return 0;
+  ki.occupancy[dev] = occ > 0 ? occ : 1;
+  return ki.occupancy[dev];
+}
+
+int in_dtype_of(int kv_dtype) { return kv_dtype == PA_FP16 ? PA_FP16 : PA_BF16; }
+
+int check_shape(const pa_pool* pool, int S, int n_q_heads, int max_blocks) {
+  if (!pool) return fail(PA_ERR_INVALID, "null pool");
+  if (S < 0 || max_blocks < 1 || n_q_heads < 1)
+    return fail(PA_ERR_INVALID, "need S >= 0, max_blocks_per_seq >= 1, n_q_heads >= 1");
+  const int hkv = pool->desc.n_kv_heads;
+  if (n_q_heads % hkv != 0)
+    return fail(PA_ERR_INVALID, "n_q_heads %d is not a multiple of n_kv_heads %d", n_q_heads, hkv);
+  if (n_q_heads / hkv > 8)
+    return fail(PA_ERR_UNSUPPORTED, "query heads per kv head must be <= 8 (got %d)",
+                n_q_heads / hkv);
+  if (S > 65535) return fail(PA_ERR_UNSUPPORTED, "at most 65535 sequences per call");
+  if (hkv > 65535) return fail(PA_ERR_UNSUPPORTED, "at most 65535 kv heads");
+  return PA_OK;
+}
+
+// Splits along the pages: choose s minimising waves(s) * (pages per split +
+// fixed per-CTA cost), where waves(s) = ceil(S * Hkv * s / resident CTAs).
+int auto_splits(const pa_pool* pool, int S, int max_blocks, int* out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return fail(PA_ERR_CUDA, "cudaGetDevice: %s", cudaGetErrorString(e));
+  int sms = 0;
+  e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (e != cudaSuccess) return fail(PA_ERR_CUDA, "SM count: %s", cudaGetErrorString(e));
+  Dispatch d = pick(pool->desc.kv_dtype, pool->desc.head_dim, in_dtype_of(pool->desc.kv_dtype));
+  int occ = configure(*d.info, dev);
+  if (occ <= 0) return fail(PA_ERR_CUDA, "decode kernel occupancy query failed");
+  const long long slots = (long long)sms * occ;
+  const long long units = (long long)std::max(S, 1) * pool->desc.n_kv_heads;
+  const int max_s = std::min(max_blocks, 256);
+  int best = 1;
+  double best_cost = 1e300;
+  for (int s = 1; s <= max_s; ++s) {
+    const int pps = (max_blocks + s - 1) / s;
+    if (s > 1 && (max_blocks + pps - 1) / pps != s) continue;  // same as a smaller s
+    const long long waves = (units * s + slots - 1) / slots;
+    const double cost = (double)waves * (pps + 4.0 + (s > 1 ? 2.0 : 0.0));
+    if (cost < best_cost * 0.98) {
+      best_cost = cost;
+      best = s;
+    }
+  }
+  *out = best;
+  return PA_OK;
+}
+
+int resolve_splits(const pa_pool* pool, int S, int max_blocks, int num_splits, int* splits,
+                   int* pps) {
+  int s = num_splits;
+  if (s < 0) return fail(PA_ERR_INVALID, "num_splits must be >= 0");
+  if (s == 0) {
+    int st = auto_splits(pool, S, max_blocks, &s);
+    if (st) return st;
+  }
+  s = std::max(1, std::min(s, max_blocks));
+  if (s > 65535) s = 65535;
+  const int p = (max_blocks + s - 1) / s;
+  *pps = p;
+  *splits = (max_blocks + p - 1) / p;
+  return PA_OK;
+}
+
+}  // namespace pa
+
+using namespace pa;
+
+extern "C" {
+
+int pa_decode_num_splits(const pa_pool* pool, int S, int n_q_heads, int max_blocks_per_seq,
+                         int* num_splits) {
+  int st = check_shape(pool, S, n_q_heads, max_blocks_per_seq);
+  if (st) return st;
+  if (!num_splits) return fail(PA_ERR_INVALID, "null output");
+  int pps;
+  return resolve_splits(pool, S, max_blocks_per_seq, 0, num_splits, &pps);
+}
+
+int pa_decode_workspace_bytes(const pa_pool* pool, int S, int n_q_heads, int max_blocks_per_seq,
+                              int num_splits, size_t* bytes) {
+  int st = check_shape(pool, S, n_q_heads, max_blocks_per_seq);
+  if (st) return st;
+  if (!bytes) return fail(PA_ERR_INVALID, "null output");
+  int splits, pps;
+  st = resolve_splits(pool, S, max_blocks_per_seq, num_splits, &splits, &pps);
+  if (st) return st;
+  *bytes = splits > 1 ? (size_t)S * n_q_heads * splits * (pool->desc.head_dim + 2) * sizeof(float)
+                      : 0;
+  return PA_OK;
+}
+
+int pa_decode(pa_pool* pool, int layer, void* out, int out_dtype, const void* q,
+              const int32_t* block_tables_dev, int max_blocks_per_seq, const int32_t* ctx_lens_dev,
+              int S, int n_q_heads, float softmax_scale, int num_splits, void* workspace,
+              size_t workspace_bytes, void* stream) {
+  int st = check_pool_layer(pool, layer);
+  if (st) return st;
+  st = check_shape(pool, S, n_q_heads, max_blocks_per_seq);
+  if (st) return st;
+  const pa_pool_desc& d = pool->desc;
+  if (out_dtype != PA_FP32 && out_dtype != in_dtype_of(d.kv_dtype))
+    return fail(PA_ERR_INVALID, "out_dtype must be the query dtype or PA_FP32");
+  if (!std::isfinite(softmax_scale)) return fail(PA_ERR_INVALID, "softmax_scale must be finite");
+  if (S == 0) return PA_OK;
+  if (!out || !q || !block_tables_dev || !ctx_lens_dev) return fail(PA_ERR_INVALID, "null argument");
+  if (((uintptr_t)out | (uintptr_t)q) & 15u) return fail(PA_ERR_INVALID, "q and out must be 16-byte aligned");
+  int splits, pps;
+  st = resolve_splits(pool, S, max_blocks_per_seq, num_splits, &splits, &pps);
+  if (st) return st;
+  const size_t need =
+      splits > 1 ? (size_t)S * n_q_heads * splits * (d.head_dim + 2) * sizeof(float) : 0;
+  if (need > 0 && (!workspace || workspace_bytes < need))
+    return fail(PA_ERR_INVALID, "workspace of %zu bytes needed (%d splits), %zu given", need,
+                splits, workspace_bytes);
+  if (need > 0 && ((uintptr_t)workspace & 15u)) return fail(PA_ERR_INVALID, "workspace must be 16-byte aligned");
+  unsigned int* err = device_error_word();
+  if (!err) return PA_ERR_CUDA;
+  int dev = 0;
+  cudaGetDevice(&dev);
+  Dispatch disp = pick(d.kv_dtype, d.head_dim, out_dtype);
+  if (configure(*disp.info, dev) <= 0) return fail(PA_ERR_CUDA, "decode kernel configuration failed");
+
+  DecodeArgs a;
+  a.kpool = pool->k + (size_t)layer * pool->layer_bytes;
+  a.vpool = pool->v + (size_t)layer * pool->layer_bytes;
+  a.q = static_cast<const uint16_t*>(q);
+  a.out = out;
+  a.ws_o = static_cast<float*>(workspace);
+  a.ws_ml = a.ws_o ? a.ws_o + (size_t)S * n_q_heads * splits * d.head_dim : nullptr;
+  a.tables = block_tables_dev;
+  a.ctx = ctx_lens_dev;
+  a.max_blocks = max_blocks_per_seq;
+  a.Hq = n_q_heads;
+  a.Hkv = d.n_kv_heads;
+  a.G = n_q_heads / d.n_kv_heads;
+  a.num_blocks = d.num_blocks;
+  a.splits = splits;
+  a.pages_per_split = pps;
+  const float log2e = 1.4426950408889634f;
+  a.qk_scale_log2 = softmax_scale * log2e * (d.kv_dtype == PA_FP8_E4M3 ? d.k_scale : 1.f);
+  a.v_scale = d.kv_dtype == PA_FP8_E4M3 ? d.v_scale : 1.f;
+  a.err = err;
+  cudaError_t e = disp.launch(a, S, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return fail(PA_ERR_CUDA, "decode launch: %s", cudaGetErrorString(e));
+  return PA_OK;
+}
+
+}  // extern "C"

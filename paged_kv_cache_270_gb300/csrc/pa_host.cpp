@@ -1,0 +1,254 @@
+// pa_host.cpp -- host side of the library: pool descriptions and sizing, the
+// block allocator (free list + reference counts), copy-on-write preparation
+// and error reporting.
+//
+// The block manager follows the pages' description of PagedAttention as
+// virtual memory for the KV cache: a flat pool of fixed 16-token blocks, a
+// per-sequence block table, reference-counted sharing of blocks between
+// sequences ("Capítulo 8 -- Gestión de caché KV de nueva generación", section
+// 8.1), copy-on-write when a sequence starts writing its own tokens into a
+// shared block ("PagedAttention y Gestión de KV-Cache", section 3.01), and
+// return of every page to the free pool when a request ends or is cancelled
+// (same page, section 4.02).
+#include <stdarg.h>
+#include <stdio.h>
+#include <string.h>
+
+#include <cmath>
+#include <new>
+#include <string>
+#include <unordered_map>
+
+#include "pa_internal.h"
+
+namespace {
+thread_local std::string g_last_error;
+
+int elem_bytes_of(int dtype) {
+  switch (dtype) {
+    case PA_FP16:
+    case PA_BF16:
+      return 2;
+    case PA_FP8_E4M3:
+      return 1;
+    default:
+      return 0;
+  }
+}
+
+// Validates everything in a description except num_blocks.
+int check_desc_shape(const pa_pool_desc* d) {
+  if (!d) return pa::fail(PA_ERR_INVALID, "null pool description");
+  if (d->n_layers < 1) return pa::fail(PA_ERR_INVALID, "n_layers must be >= 1 (got %d)", d->n_layers);
+  if (d->block_size != PA_BLOCK_SIZE)
+    return pa::fail(PA_ERR_UNSUPPORTED, "block_size must be 16 (got %d)", d->block_size);
+  if (d->n_kv_heads < 1)
+    return pa::fail(PA_ERR_INVALID, "n_kv_heads must be >= 1 (got %d)", d->n_kv_heads);
+  if (d->head_dim != 64 && d->head_dim != 128)
+    return pa::fail(PA_ERR_UNSUPPORTED, "head_dim must be 64 or 128 (got %d)", d->head_dim);
+  if (elem_bytes_of(d->kv_dtype) == 0)
+    return pa::fail(PA_ERR_UNSUPPORTED, "kv_dtype %d is not a cache type", d->kv_dtype);
+  if (d->kv_dtype == PA_FP8_E4M3) {
+    if (!(d->k_scale > 0.f) || !std::isfinite(d->k_scale) || !(d->v_scale > 0.f) ||
+        !std::isfinite(d->v_scale))
+      return pa::fail(PA_ERR_INVALID, "FP8 pools need finite positive k_scale and v_scale");
+  }
+  return PA_OK;
+}
+
+size_t block_bytes_all_layers(const pa_pool_desc* d) {
+  // K + V, every layer, one block
+  return 2ull * (size_t)d->n_layers * (size_t)d->n_kv_heads * (size_t)d->block_size *
+         (size_t)d->head_dim * (size_t)elem_bytes_of(d->kv_dtype);
+}
+}  // namespace
+
+namespace pa {
+int fail(int code, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof buf, fmt, ap);
+  va_end(ap);
+  g_last_error = buf;
+  return code;
+}
+
+int check_pool_layer(const pa_pool* pool, int layer) {
+  if (!pool) return fail(PA_ERR_INVALID, "null pool");
+  if (layer < 0 || layer >= pool->desc.n_layers)
+    return fail(PA_ERR_INVALID, "layer %d outside [0, %d)", layer, pool->desc.n_layers);
+  return PA_OK;
+}
+}  // namespace pa
+
+extern "C" {
+
+int pa_last_error(char* buf, size_t n) {
+  if (buf && n) {
+    size_t m = g_last_error.size() < n - 1 ? g_last_error.size() : n - 1;
+    memcpy(buf, g_last_error.data(), m);
+    buf[m] = '\0';
+  }
+  return PA_OK;
+}
+
+int pa_kv_bytes_per_token(int n_layers, int n_kv_heads, int head_dim, int kv_dtype, size_t* bytes) {
+  int b = elem_bytes_of(kv_dtype);
+  if (!bytes || n_layers < 1 || n_kv_heads < 1 || head_dim < 1 || b == 0)
+    return pa::fail(PA_ERR_INVALID, "pa_kv_bytes_per_token: bad argument");
+  *bytes = 2ull * (size_t)n_layers * (size_t)n_kv_heads * (size_t)head_dim * (size_t)b;
+  return PA_OK;
+}
+
+int pa_pool_bytes(const pa_pool_desc* desc, size_t* k_bytes, size_t* v_bytes) {
+  int st = check_desc_shape(desc);
+  if (st) return st;
+  if (desc->num_blocks < 1) return pa::fail(PA_ERR_INVALID, "num_blocks must be >= 1");
+  size_t half = block_bytes_all_layers(desc) / 2 * (size_t)desc->num_blocks;
+  if (k_bytes) *k_bytes = half;
+  if (v_bytes) *v_bytes = half;
+  return PA_OK;
+}
+
+int pa_pool_blocks_for_budget(const pa_pool_desc* desc, size_t budget_bytes, int* num_blocks) {
+  int st = check_desc_shape(desc);
+  if (st) return st;
+  if (!num_blocks) return pa::fail(PA_ERR_INVALID, "null output");
+  size_t per = block_bytes_all_layers(desc);
+  size_t n = budget_bytes / per;
+  if (n == 0)
+    return pa::fail(PA_ERR_NO_MEMORY,
+                    "no available memory for the cache blocks: budget %zu B < one block %zu B",
+                    budget_bytes, per);
+  *num_blocks = n > 0x7FFFFFFF ? 0x7FFFFFFF : (int)n;
+  return PA_OK;
+}
+
+int pa_pool_create(const pa_pool_desc* desc, void* k_cache, void* v_cache, pa_pool** out) {
+  int st = check_desc_shape(desc);
+  if (st) return st;
+  if (!out) return pa::fail(PA_ERR_INVALID, "null output handle");
+  *out = nullptr;
+  if (desc->num_blocks < 1) return pa::fail(PA_ERR_NO_MEMORY, "num_blocks must be >= 1");
+  if (!k_cache || !v_cache) return pa::fail(PA_ERR_INVALID, "null cache region");
+  if (((uintptr_t)k_cache | (uintptr_t)v_cache) & 15u)
+    return pa::fail(PA_ERR_INVALID, "cache regions must be 16-byte aligned");
+  pa_pool* p = new (std::nothrow) pa_pool;
+  if (!p) return pa::fail(PA_ERR_NO_MEMORY, "host allocation failed");
+  p->desc = *desc;
+  p->k = static_cast<uint8_t*>(k_cache);
+  p->v = static_cast<uint8_t*>(v_cache);
+  p->elem_bytes = elem_bytes_of(desc->kv_dtype);
+  p->tile_bytes = (size_t)desc->block_size * desc->head_dim * p->elem_bytes;
+  p->layer_bytes = (size_t)desc->num_blocks * desc->n_kv_heads * p->tile_bytes;
+  try {
+    p->refcount.assign(desc->num_blocks, 0);
+    p->free_stack.resize(desc->num_blocks);
+  } catch (...) {
+    delete p;
+    return pa::fail(PA_ERR_NO_MEMORY, "host allocation failed");
+  }
+  // top of the stack is the back: the first pops return 0, 1, 2, ...
+  for (int i = 0; i < desc->num_blocks; ++i) p->free_stack[i] = desc->num_blocks - 1 - i;
+  *out = p;
+  return PA_OK;
+}
+
+int pa_pool_destroy(pa_pool* pool) {
+  delete pool;
+  return PA_OK;
+}
+
+int pa_pool_get_desc(const pa_pool* pool, pa_pool_desc* desc) {
+  if (!pool || !desc) return pa::fail(PA_ERR_INVALID, "null argument");
+  *desc = pool->desc;
+  return PA_OK;
+}
+
+int pa_block_alloc(pa_pool* pool, int n, int32_t* ids) {
+  if (!pool || n < 0 || (n > 0 && !ids)) return pa::fail(PA_ERR_INVALID, "pa_block_alloc: bad argument");
+  if ((size_t)n > pool->free_stack.size())
+    return pa::fail(PA_ERR_OUT_OF_BLOCKS, "out of cache blocks: need %d, %zu free", n,
+                    pool->free_stack.size());
+  for (int i = 0; i < n; ++i) {
+    int32_t b = pool->free_stack.back();
+    pool->free_stack.pop_back();
+    pool->refcount[b] = 1;
+    ids[i] = b;
+  }
+  return PA_OK;
+}
+
+int pa_block_free(pa_pool* pool, int n, const int32_t* ids) {
+  if (!pool || n < 0 || (n > 0 && !ids)) return pa::fail(PA_ERR_INVALID, "pa_block_free: bad argument");
+  // validate the whole request first: no change unless every decrement is legal
+  std::unordered_map<int32_t, int> count;
+  for (int i = 0; i < n; ++i) {
+    int32_t b = ids[i];
+    if (b < 0 || b >= pool->desc.num_blocks)
+      return pa::fail(PA_ERR_INVALID, "free of block %d outside [0, %d)", b, pool->desc.num_blocks);
+    if (++count[b] > pool->refcount[b])
+      return pa::fail(PA_ERR_INVALID, "free of block %d below refcount 0 (double free)", b);
+  }
+  for (int i = 0; i < n; ++i) {
+    int32_t b = ids[i];
+    if (--pool->refcount[b] == 0) pool->free_stack.push_back(b);
+  }
+  return PA_OK;
+}
+
+int pa_block_incref(pa_pool* pool, int n, const int32_t* ids) {
+  if (!pool || n < 0 || (n > 0 && !ids)) return pa::fail(PA_ERR_INVALID, "pa_block_incref: bad argument");
+  for (int i = 0; i < n; ++i) {
+    int32_t b = ids[i];
+    if (b < 0 || b >= pool->desc.num_blocks || pool->refcount[b] == 0)
+      return pa::fail(PA_ERR_INVALID, "incref of block %d, which is not allocated", b);
+  }
+  for (int i = 0; i < n; ++i) ++pool->refcount[ids[i]];
+  return PA_OK;
+}
+
+int pa_block_refcount(const pa_pool* pool, int32_t id, int* refcount) {
+  if (!pool || !refcount || id < 0 || id >= pool->desc.num_blocks)
+    return pa::fail(PA_ERR_INVALID, "pa_block_refcount: bad argument");
+  *refcount = pool->refcount[id];
+  return PA_OK;
+}
+
+int pa_pool_stats(const pa_pool* pool, int* used, int* free_blocks, int* shared) {
+  if (!pool) return pa::fail(PA_ERR_INVALID, "null pool");
+  int u = 0, s = 0;
+  for (int32_t r : pool->refcount) {
+    u += r > 0;
+    s += r > 1;
+  }
+  if (used) *used = u;
+  if (free_blocks) *free_blocks = pool->desc.num_blocks - u;
+  if (shared) *shared = s;
+  return PA_OK;
+}
+
+int pa_cow_prepare(pa_pool* pool, int32_t* table_row, int ctx_len, int32_t* src, int32_t* dst,
+                   int* n_pairs) {
+  if (!pool || !table_row || !src || !dst || !n_pairs || ctx_len < 0)
+    return pa::fail(PA_ERR_INVALID, "pa_cow_prepare: bad argument");
+  *n_pairs = 0;
+  const int B = pool->desc.block_size;
+  if (ctx_len % B == 0) return PA_OK;  // the token opens a fresh block
+  int32_t old = table_row[ctx_len / B];
+  if (old < 0 || old >= pool->desc.num_blocks || pool->refcount[old] == 0)
+    return pa::fail(PA_ERR_INVALID, "table entry %d is not an allocated block", old);
+  if (pool->refcount[old] <= 1) return PA_OK;  // sole owner writes in place
+  int32_t fresh;
+  int st = pa_block_alloc(pool, 1, &fresh);
+  if (st) return st;
+  --pool->refcount[old];  // stays >= 1: still held by the other sharers
+  table_row[ctx_len / B] = fresh;
+  *src = old;
+  *dst = fresh;
+  *n_pairs = 1;
+  return PA_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,34 @@
+// pa_internal.h -- library-internal declarations shared by the host and CUDA
+// translation units (not part of the public ABI).
+#pragma once
+
+#include <stddef.h>
+#include <stdint.h>
+
+#include <vector>
+
+#include "../../include/pa.h"
+
+struct pa_pool {
+  pa_pool_desc desc;
+  uint8_t* k;                     // device, all layers
+  uint8_t* v;                     // device, all layers
+  int elem_bytes;                 // 1 (FP8) or 2
+  size_t tile_bytes;              // one (block, kv head) tile: block_size * head_dim * elem_bytes
+  size_t layer_bytes;             // one layer of K (or V): num_blocks * n_kv_heads * tile_bytes
+  std::vector<int32_t> refcount;  // per block
+  std::vector<int32_t> free_stack;  // top = back()
+};
+
+namespace pa {
+
+// Records `msg` as the calling thread's last error and returns `code`.
+int fail(int code, const char* fmt, ...);
+
+// Address of the per-device error word (current device); nullptr on failure
+// (the error is then recorded and PA_ERR_CUDA should be returned).
+unsigned int* device_error_word();
+
+int check_pool_layer(const pa_pool* pool, int layer);
+
+}  // namespace pa
