@@ -229,6 +229,38 @@ PA_API int pa_decode(pa_pool* pool, int layer, void* out, int out_dtype, const v
               int S, int n_q_heads, float softmax_scale, int num_splits, void* workspace,
               size_t workspace_bytes, void* stream);
 
+/* Size of the device scratch that pa_decode_no_alloc keeps in the library
+ * itself: 8 MiB per GPU that loads the library, held until the process exits. */
+#define PA_NOALLOC_SCRATCH_BYTES (8u << 20)
+
+/* pa_decode for callers that cannot allocate device memory.  (The pages have
+ * no counterpart: this is an integration entry point of this library.)
+ *
+ * Some callers cannot call cudaMalloc or any allocating routine: a plugin run
+ * by a host framework that owns every device allocation and hands the plugin
+ * only its input and output pointers, or a serving loop that must not allocate
+ * once it is running, because an allocation can synchronise the device and
+ * stall the other streams.  Such a caller cannot provide pa_decode's
+ * workspace.  This variant takes the same arguments minus the workspace and
+ * keeps the split partials in a fixed array inside the library instead, of
+ * PA_NOALLOC_SCRATCH_BYTES.  It allocates nothing and frees nothing.
+ *
+ *  - num_splits = 0: the automatic split count, lowered if needed until the
+ *    partials fit the array (one split needs no scratch at all).  An explicit
+ *    num_splits whose partials, S * n_q_heads * num_splits * (head_dim + 2) * 4
+ *    bytes, exceed PA_NOALLOC_SCRATCH_BYTES is rejected with PA_ERR_INVALID.
+ *  - The first call on a device looks up the array's device address with that
+ *    device current; make that first call before any stream capture.
+ *  - Every call on a device shares the one array and overwrites it.  Each call
+ *    writes every partial its merge reads before reading it, so nothing needs
+ *    clearing between calls, but calls whose kernels overlap on the GPU (on
+ *    different streams, or from different threads) race on it: serialise them.
+ * Results equal pa_decode's for the same split count. */
+PA_API int pa_decode_no_alloc(pa_pool* pool, int layer, void* out, int out_dtype, const void* q,
+                              const int32_t* block_tables_dev, int max_blocks_per_seq,
+                              const int32_t* ctx_lens_dev, int S, int n_q_heads,
+                              float softmax_scale, int num_splits, void* stream);
+
 /* Synchronises `stream`, then reads and clears the current device's error word.
  * *code = PA_OK or the first PA_ERR_* a kernel recorded since the last read.
  * The word is shared by every pool on the device. */

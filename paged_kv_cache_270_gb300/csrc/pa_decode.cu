@@ -689,4 +689,68 @@ int pa_decode(pa_pool* pool, int layer, void* out, int out_dtype, const void* q,
   return PA_OK;
 }
 
+// ---------------------------------------------------------------------------
+// Fixed scratch for pa_decode_no_alloc: the split partials of one call, for
+// callers that cannot allocate device memory.  One copy per device that loads
+// the library; its device address is looked up once per device.
+static __device__ __align__(256) float g_noalloc_scratch[PA_NOALLOC_SCRATCH_BYTES / sizeof(float)];
+
+static int noalloc_scratch(void** ptr) {
+  static std::mutex mu;
+  static void* cached[128] = {};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return fail(PA_ERR_CUDA, "cudaGetDevice: %s", cudaGetErrorString(e));
+  if (dev < 0 || dev >= 128) return fail(PA_ERR_UNSUPPORTED, "device index %d", dev);
+  std::lock_guard<std::mutex> lock(mu);
+  if (!cached[dev]) {
+    void* p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+    if (e != cudaSuccess || !p)
+      return fail(PA_ERR_CUDA, "cudaGetSymbolAddress(no-alloc scratch): %s", cudaGetErrorString(e));
+    cached[dev] = p;
+  }
+  *ptr = cached[dev];
+  return PA_OK;
+}
+
+int pa_decode_no_alloc(pa_pool* pool, int layer, void* out, int out_dtype, const void* q,
+                       const int32_t* block_tables_dev, int max_blocks_per_seq,
+                       const int32_t* ctx_lens_dev, int S, int n_q_heads, float softmax_scale,
+                       int num_splits, void* stream) {
+  int st = check_pool_layer(pool, layer);
+  if (st) return st;
+  st = check_shape(pool, S, n_q_heads, max_blocks_per_seq);
+  if (st) return st;
+  if (S == 0) return PA_OK;
+  const size_t row_bytes = (size_t)S * n_q_heads * (pool->desc.head_dim + 2) * sizeof(float);
+  int splits, pps;
+  st = resolve_splits(pool, S, max_blocks_per_seq, num_splits, &splits, &pps);
+  if (st) return st;
+  if (splits > 1 && row_bytes * splits > PA_NOALLOC_SCRATCH_BYTES) {
+    if (num_splits != 0)
+      return fail(PA_ERR_INVALID,
+                  "pa_decode_no_alloc: %d splits need %zu bytes of scratch, above the static "
+                  "maximum of %u bytes (use fewer splits, or pa_decode with a workspace)",
+                  splits, row_bytes * splits, (unsigned)PA_NOALLOC_SCRATCH_BYTES);
+    // automatic choice: the largest split count whose partials fit
+    int s = (int)std::min<size_t>((size_t)splits, PA_NOALLOC_SCRATCH_BYTES / row_bytes);
+    for (;; --s) {
+      if (s <= 1) {
+        splits = 1;
+        break;
+      }
+      st = resolve_splits(pool, S, max_blocks_per_seq, s, &splits, &pps);
+      if (st) return st;
+      if (row_bytes * splits <= PA_NOALLOC_SCRATCH_BYTES) break;
+    }
+  }
+  void* scratch = nullptr;
+  st = noalloc_scratch(&scratch);
+  if (st) return st;
+  return pa_decode(pool, layer, out, out_dtype, q, block_tables_dev, max_blocks_per_seq,
+                   ctx_lens_dev, S, n_q_heads, softmax_scale, splits, scratch,
+                   PA_NOALLOC_SCRATCH_BYTES, stream);
+}
+
 }  // extern "C"
