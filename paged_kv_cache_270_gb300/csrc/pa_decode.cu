@@ -13,11 +13,12 @@
 // Kernel design (not from the pages; they give none):
 //  * grid = (split, kv head, sequence); 5 warps per CTA.
 //  * Warp 4 is the producer: it reads the sequence's block-table entries 32 at a
-//    time (one coalesced load) and issues, per page, two 1-D TMA bulk copies
-//    (the contiguous K tile and V tile of this kv head, 16 x head_dim
-//    elements each) into an 8-stage shared-memory ring, completing on an
-//    mbarrier.  The tiles are streamed once, so they carry an L2 evict-first
-//    hint.
+//    time (one coalesced load) and issues, per page, two TMA tensor copies (the
+//    contiguous K tile and V tile of this kv head, 16 rows of head_dim
+//    elements) into an 8-stage shared-memory ring, completing on an mbarrier.
+//    Rows of 128 or 256 bytes are written with the TMA's 128-byte swizzle, so
+//    the consumers' 16-byte shared-memory reads below are bank-conflict free.
+//    The tiles are streamed once, so they carry an L2 evict-first hint.
 //  * Warps 0..3 consume whole pages round-robin in logical order.  The whole
 //    grouped-query group (G <= 8 query heads sharing this kv head) is resident,
 //    so every KV byte is read from HBM exactly once per decode.
@@ -38,6 +39,7 @@
 //  * Accumulation follows logical page order within each warp and a fixed warp
 //    order in the merge, so the result is bit-identical under any relabelling
 //    of physical blocks.
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 #include <algorithm>
@@ -58,19 +60,24 @@ constexpr unsigned kFull = 0xffffffffu;
 template <int KV, int D>
 struct Cfg {
   static constexpr int kElem = (KV == KV_E4M3) ? 1 : 2;
-  static constexpr int kTile = 16 * D * kElem;  // bytes of one (block, kv head) tile
+  static constexpr int kRowBytes = D * kElem;    // one token row of a tile
+  static constexpr int kTile = 16 * kRowBytes;   // bytes of one (block, kv head) tile
+  // Rows of 128 or 256 bytes are loaded with 128-byte TMA swizzling, which
+  // makes every shared-memory read of the consumers below bank-conflict free.
+  static constexpr bool kSwizzle = (kRowBytes % 128) == 0;
+  static constexpr int kTmaRank = kRowBytes == 256 ? 3 : 2;
   static constexpr int kStages = 8;
   static constexpr int kStageBytes = 2 * kTile;  // K tile + V tile
   static constexpr int kRingBytes = kStages * kStageBytes;
   static constexpr int kMergeBytes = kConsumerWarps * 8 * (D + 2) * 4;
   static constexpr int kDataBytes = kRingBytes > kMergeBytes ? kRingBytes : kMergeBytes;
-  static constexpr int kSmem = kDataBytes + 2 * kStages * 8;
+  static constexpr int kAlign = 1024;  // a 128-byte-swizzled TMA destination is 1 KiB aligned
+  static constexpr int kSmem = kDataBytes + 2 * kStages * 8 + kAlign;
   static constexpr bool kMmaBf16 = (KV == KV_BF16);
+  static_assert(kStageBytes % kAlign == 0 || !kSwizzle, "tiles must stay 1 KiB aligned");
 };
 
 struct DecodeArgs {
-  const uint8_t* kpool;  // this layer's K region
-  const uint8_t* vpool;  // this layer's V region
   const uint16_t* q;     // [S][Hq][D]
   void* out;             // [S][Hq][D]
   float* ws_o;           // [S][Hq][splits][D]      (splits > 1)
@@ -96,12 +103,31 @@ __device__ __forceinline__ void store_out(void* out, size_t idx, float v) {
   }
 }
 
+// Loads the K or V tile of `row0` (= (block * Hkv + head) * 16) through the map.
+template <int RANK>
+__device__ __forceinline__ void load_tile(void* dst, const CUtensorMap* map, int row0,
+                                          uint64_t* bar, uint64_t policy) {
+  if constexpr (RANK == 3) tma_load_3d(dst, map, 0, 0, row0, bar, policy);
+  else tma_load_2d(dst, map, 0, row0, bar, policy);
+}
+
+template <bool SWZ>
+__device__ __forceinline__ uint32_t tile_off(uint32_t off) {
+  if constexpr (SWZ) return swizzle128(off);
+  else return off;
+}
+
 template <int KV, int D, int OUT, bool PSPLIT>
-__global__ void __launch_bounds__(kThreads) decode_kernel(const DecodeArgs a) {
+__global__ void __launch_bounds__(kThreads) decode_kernel(const DecodeArgs a,
+                                                          const __grid_constant__ CUtensorMap tmk,
+                                                          const __grid_constant__ CUtensorMap tmv) {
   using C = Cfg<KV, D>;
   constexpr bool BF = C::kMmaBf16;
+  constexpr bool SWZ = C::kSwizzle;
   constexpr int NT = D / 16;  // MMA steps along the head dim (QK) / m-tiles (PV)
-  extern __shared__ __align__(128) uint8_t smem[];
+  extern __shared__ __align__(16) uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + C::kAlign - 1) & ~uintptr_t(C::kAlign - 1));
   uint8_t* ring = smem;
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::kDataBytes);
   uint64_t* empty = full + C::kStages;
@@ -117,6 +143,12 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(const DecodeArgs a) {
   const int npages = (ctx + 15) >> 4;
   const int p_begin = split * a.pages_per_split;
   const int n_local = max(0, min(npages, p_begin + a.pages_per_split) - p_begin);
+  // A split past the end of this sequence's pages has nothing to do: no partial
+  // is written for it and the merge never reads one.  Split 0 always runs (it
+  // writes the zero row of an empty context).
+  if (split > 0 && n_local == 0) return;
+  // Sequences that fit in one split are finished here, without a merge.
+  const bool direct = a.splits == 1 || npages <= a.pages_per_split;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < C::kStages; ++s) {
@@ -124,6 +156,10 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(const DecodeArgs a) {
       mbar_init(&empty[s], 1);
     }
     fence_barrier_init();
+  }
+  if (threadIdx.x == kConsumerWarps * 32) {
+    prefetch_tensormap(&tmk);
+    prefetch_tensormap(&tmv);
   }
   __syncthreads();
 
@@ -137,9 +173,6 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(const DecodeArgs a) {
     // ------------------------------------------------------------ producer
     const int32_t* trow = a.tables + (size_t)seq * a.max_blocks + p_begin;
     const uint64_t policy = l2_evict_first_policy();
-    const size_t blk_stride = (size_t)a.Hkv * C::kTile;
-    const uint8_t* kbase = a.kpool + (size_t)h * C::kTile;
-    const uint8_t* vbase = a.vpool + (size_t)h * C::kTile;
     int issued = 0;
     bool abort = false;
     for (int base = 0; base < n_local && !abort; base += 32) {
@@ -162,10 +195,10 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(const DecodeArgs a) {
             stop = 1;
           } else {
             uint8_t* dst = ring + stage * C::kStageBytes;
+            const int row0 = (ph * a.Hkv + h) * 16;
             mbar_arrive_expect_tx(&full[stage], 2 * C::kTile);
-            bulk_g2s(dst, kbase + (size_t)ph * blk_stride, C::kTile, &full[stage], policy);
-            bulk_g2s(dst + C::kTile, vbase + (size_t)ph * blk_stride, C::kTile, &full[stage],
-                     policy);
+            load_tile<C::kTmaRank>(dst, &tmk, row0, &full[stage], policy);
+            load_tile<C::kTmaRank>(dst + C::kTile, &tmv, row0, &full[stage], policy);
             ++issued;
           }
         }
@@ -229,7 +262,7 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(const DecodeArgs a) {
 
     constexpr int KB = D / 4 * C::kElem;  // K bytes per row per thread
     constexpr int VB = D / 8 * C::kElem;  // V bytes per row per thread
-    constexpr int RB = D * C::kElem;      // bytes per token row of a tile
+    constexpr int RB = C::kRowBytes;
 
     for (int k = warp; k < n_local; k += kConsumerWarps) {
       const int stage = k % C::kStages;
@@ -242,40 +275,74 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(const DecodeArgs a) {
       const uint8_t* Vs = Ks + C::kTile;
       const int tok0 = (p_begin + k) * 16;
 
-      // ---- S^T[token][head] = K_page . Q^T
-      float s[4] = {0.f, 0.f, 0.f, 0.f};
+      // ---- issue every shared-memory read of the page up front
+      constexpr int VW = VB / 4;  // V words per row per thread
+      const int rows[4] = {2 * t, 2 * t + 1, 2 * t + 8, 2 * t + 9};
+      uint4 kr[2][KB / 16];
+      uint32_t vw[4][VW];
       {
-        const uint8_t* kr0 = Ks + g * RB + t * KB;
-        const uint8_t* kr1 = kr0 + 8 * RB;
+        const uint32_t kr0 = g * RB + t * KB;
 #pragma unroll
         for (int c = 0; c < KB / 16; ++c) {
-          const uint4 r0 = lds128(kr0 + 16 * c), r1 = lds128(kr1 + 16 * c);
-          if constexpr (KV == KV_E4M3) {
-            const uint32_t w0[4] = {r0.x, r0.y, r0.z, r0.w};
-            const uint32_t w1[4] = {r1.x, r1.y, r1.z, r1.w};
+          kr[0][c] = lds128(Ks + tile_off<SWZ>(kr0 + 16 * c));
+          kr[1][c] = lds128(Ks + tile_off<SWZ>(kr0 + 8 * RB + 16 * c));
+        }
 #pragma unroll
-            for (int jj = 0; jj < 4; ++jj) {
-              const int j = 4 * c + jj;
-              const uint32_t af[4] = {e4m3x2_to_f16x2(w0[jj]), e4m3x2_to_f16x2(w1[jj]),
-                                      e4m3x2_to_f16x2(w0[jj] >> 16),
-                                      e4m3x2_to_f16x2(w1[jj] >> 16)};
-              mma16816<false>(s, af, qf[2 * j], qf[2 * j + 1]);
-            }
+        for (int r = 0; r < 4; ++r) {
+          const uint32_t vo = rows[r] * RB + g * VB;
+          if constexpr (VB == 8) {
+            const uint2 u = lds64(Vs + tile_off<SWZ>(vo));
+            vw[r][0] = u.x;
+            vw[r][1] = u.y;
           } else {
-            const uint32_t a0[4] = {r0.x, r1.x, r0.y, r1.y};
-            mma16816<BF>(s, a0, qf[4 * c], qf[4 * c + 1]);
-            const uint32_t a1[4] = {r0.z, r1.z, r0.w, r1.w};
-            mma16816<BF>(s, a1, qf[4 * c + 2], qf[4 * c + 3]);
+#pragma unroll
+            for (int c = 0; c < VB / 16; ++c) {
+              const uint4 u = lds128(Vs + tile_off<SWZ>(vo + 16 * c));
+              vw[r][4 * c] = u.x;
+              vw[r][4 * c + 1] = u.y;
+              vw[r][4 * c + 2] = u.z;
+              vw[r][4 * c + 3] = u.w;
+            }
           }
         }
       }
 
+      // ---- S^T[token][head] = K_page . Q^T
+      float s[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+      for (int c = 0; c < KB / 16; ++c) {
+        const uint4 r0 = kr[0][c], r1 = kr[1][c];
+        if constexpr (KV == KV_E4M3) {
+          const uint32_t w0[4] = {r0.x, r0.y, r0.z, r0.w};
+          const uint32_t w1[4] = {r1.x, r1.y, r1.z, r1.w};
+#pragma unroll
+          for (int jj = 0; jj < 4; ++jj) {
+            const int j = 4 * c + jj;
+            const uint32_t af[4] = {e4m3x2_to_f16x2(w0[jj]), e4m3x2_to_f16x2(w1[jj]),
+                                    e4m3x2_to_f16x2(w0[jj] >> 16), e4m3x2_to_f16x2(w1[jj] >> 16)};
+            mma16816<false>(s, af, qf[2 * j], qf[2 * j + 1]);
+          }
+        } else {
+          const uint32_t a0[4] = {r0.x, r1.x, r0.y, r1.y};
+          mma16816<BF>(s, a0, qf[4 * c], qf[4 * c + 1]);
+          const uint32_t a1[4] = {r0.z, r1.z, r0.w, r1.w};
+          mma16816<BF>(s, a1, qf[4 * c + 2], qf[4 * c + 3]);
+        }
+      }
+
       // ---- online softmax over this page (tokens g and g+8; heads 2t, 2t+1)
-      const bool ok0 = tok0 + g < ctx, ok1 = tok0 + g + 8 < ctx;
-      const float x0 = ok0 ? s[0] * qk_scale : -INFINITY;
-      const float x1 = ok0 ? s[1] * qk_scale : -INFINITY;
-      const float x2 = ok1 ? s[2] * qk_scale : -INFINITY;
-      const float x3 = ok1 ? s[3] * qk_scale : -INFINITY;
+      float x0 = s[0] * qk_scale, x1 = s[1] * qk_scale;
+      float x2 = s[2] * qk_scale, x3 = s[3] * qk_scale;
+      if (tok0 + 16 > ctx) {  // last, partial page (warp-uniform): slots past ctx hold anything
+        if (tok0 + g >= ctx) x0 = x1 = -INFINITY;
+        if (tok0 + g + 8 >= ctx) x2 = x3 = -INFINITY;
+#pragma unroll
+        for (int r = 0; r < 4; ++r)
+          if (tok0 + rows[r] >= ctx) {
+#pragma unroll
+            for (int w = 0; w < VW; ++w) vw[r][w] = 0u;
+          }
+      }
       float pm0 = fmaxf(x0, x2), pm1 = fmaxf(x1, x3);
 #pragma unroll
       for (int off = 4; off < 32; off <<= 1) {
@@ -284,20 +351,24 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(const DecodeArgs a) {
       }
       // token 0 of every page is valid, so the new maxima are finite
       const float mn0 = fmaxf(m0, pm0), mn1 = fmaxf(m1, pm1);
-      const float al0 = exp2f(m0 - mn0), al1 = exp2f(m1 - mn1);
-      const float p0 = exp2f(x0 - mn0), p1 = exp2f(x1 - mn1);
-      const float p2 = exp2f(x2 - mn0), p3 = exp2f(x3 - mn1);
-      m0 = mn0;
-      m1 = mn1;
-      l0 = l0 * al0 + (p0 + p2);
-      l1 = l1 * al1 + (p1 + p3);
+      if (__any_sync(kFull, (mn0 != m0) | (mn1 != m1))) {  // rescale only when a max moved
+        const float al0 = fast_exp2(m0 - mn0), al1 = fast_exp2(m1 - mn1);
+        l0 *= al0;
+        l1 *= al1;
 #pragma unroll
-      for (int i = 0; i < NT; ++i) {
-        o[i][0] *= al0;
-        o[i][1] *= al1;
-        o[i][2] *= al0;
-        o[i][3] *= al1;
+        for (int i = 0; i < NT; ++i) {
+          o[i][0] *= al0;
+          o[i][1] *= al1;
+          o[i][2] *= al0;
+          o[i][3] *= al1;
+        }
+        m0 = mn0;
+        m1 = mn1;
       }
+      const float p0 = fast_exp2(x0 - m0), p1 = fast_exp2(x1 - m1);
+      const float p2 = fast_exp2(x2 - m0), p3 = fast_exp2(x3 - m1);
+      l0 += p0 + p2;
+      l1 += p1 + p3;
 
       // ---- P^T as the B operand: rows (tokens 2t, 2t+1 | 2t+8, 2t+9), column head g
       const uint32_t plo = pack2<BF>(p0, p1), phi = pack2<BF>(p2, p3);
@@ -311,35 +382,6 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(const DecodeArgs a) {
 
       // ---- O^T[dim][head] += V_page^T . P^T
       {
-        const uint8_t* vr = Vs + g * VB;
-        const int rows[4] = {2 * t, 2 * t + 1, 2 * t + 8, 2 * t + 9};
-        constexpr int VW = VB / 4;  // words per row per thread
-        uint32_t vw[4][VW];
-#pragma unroll
-        for (int r = 0; r < 4; ++r) {
-          if constexpr (VB == 8) {
-            const uint2 u = lds64(vr + rows[r] * RB);
-            vw[r][0] = u.x;
-            vw[r][1] = u.y;
-          } else {
-#pragma unroll
-            for (int c = 0; c < VB / 16; ++c) {
-              const uint4 u = lds128(vr + rows[r] * RB + 16 * c);
-              vw[r][4 * c] = u.x;
-              vw[r][4 * c + 1] = u.y;
-              vw[r][4 * c + 2] = u.z;
-              vw[r][4 * c + 3] = u.w;
-            }
-          }
-        }
-        if (tok0 + 16 > ctx) {  // last, partial page: slots past ctx may hold anything
-#pragma unroll
-          for (int r = 0; r < 4; ++r)
-            if (tok0 + rows[r] >= ctx) {
-#pragma unroll
-              for (int w = 0; w < VW; ++w) vw[r][w] = 0u;
-            }
-        }
 #pragma unroll
         for (int i = 0; i < NT; ++i) {
           uint32_t af[4];
@@ -407,12 +449,12 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(const DecodeArgs a) {
 #pragma unroll
       for (int w = 0; w < kConsumerWarps; ++w) {
         const float mw = mml[w * 16 + 2 * head];
-        const float f = (mw == -INFINITY) ? 0.f : exp2f(mw - M);
+        const float f = (mw == -INFINITY) ? 0.f : fast_exp2(mw - M);
         L += f * mml[w * 16 + 2 * head + 1];
         O += f * mo[(w * 8 + head) * D + dim];
       }
     }
-    if (a.splits == 1) {
+    if (direct) {
       store_out<OUT>(a.out, (row0 + head) * D + dim, L > 0.f ? O / L * a.v_scale : 0.f);
     } else {
       const size_t prow = (row0 + head) * a.splits + split;
@@ -425,26 +467,40 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(const DecodeArgs a) {
   }
 }
 
-// Merge of the per-split partial states: one warp per (sequence, query head).
+// Merge of the per-split partial states, M = max m_i, L = sum l_i 2^(m_i - M),
+// O = sum o_i 2^(m_i - M) / L, over the splits the sequence used (rows of
+// sequences that fit one split were written by the decode kernel itself).
+__device__ __forceinline__ int used_splits(const int32_t* ctx, int seq, int max_blocks, int pps) {
+  int c = ctx[seq];
+  c = c < 0 ? 0 : min(c, max_blocks * 16);
+  return ((c + 15) / 16 + pps - 1) / pps;
+}
+
+// Few splits: one warp per (sequence, query head), splits walked in a loop.
 template <int D, int OUT>
-__global__ void __launch_bounds__(128) reduce_kernel(const float* __restrict__ ws_o,
-                                                     const float* __restrict__ ws_ml, void* out,
-                                                     int rows, int splits, float v_scale) {
+__global__ void __launch_bounds__(128) reduce_rows_kernel(const float* __restrict__ ws_o,
+                                                          const float* __restrict__ ws_ml,
+                                                          const int32_t* __restrict__ ctx,
+                                                          void* out, int rows, int Hq, int splits,
+                                                          int max_blocks, int pps, float v_scale) {
   const int row = blockIdx.x * 4 + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
   if (row >= rows) return;
+  const int n = min(splits, used_splits(ctx, row / Hq, max_blocks, pps));
+  if (n <= 1) return;
   constexpr int PER = D / 32;
   const float* ml = ws_ml + (size_t)row * splits * 2;
   float M = -INFINITY;
-  for (int s = 0; s < splits; ++s) M = fmaxf(M, ml[2 * s]);
+  for (int s = 0; s < n; ++s) M = fmaxf(M, ml[2 * s]);
   float L = 0.f, O[PER];
 #pragma unroll
   for (int j = 0; j < PER; ++j) O[j] = 0.f;
   if (M != -INFINITY) {
     const float* po = ws_o + (size_t)row * splits * D + lane * PER;
-    for (int s = 0; s < splits; ++s) {
+#pragma unroll 4
+    for (int s = 0; s < n; ++s) {
       const float ms = ml[2 * s];
-      const float f = (ms == -INFINITY) ? 0.f : exp2f(ms - M);
+      const float f = (ms == -INFINITY) ? 0.f : fast_exp2(ms - M);
       L += f * ml[2 * s + 1];
       if constexpr (PER == 4) {
         const float4 v = *reinterpret_cast<const float4*>(po + (size_t)s * D);
@@ -464,6 +520,56 @@ __global__ void __launch_bounds__(128) reduce_kernel(const float* __restrict__ w
   for (int j = 0; j < PER; ++j) store_out<OUT>(out, (size_t)row * D + lane * PER + j, O[j] * inv);
 }
 
+// Many splits: one 128-thread CTA per row; the split weights are computed
+// once into shared memory and every thread (one head dim each) streams its
+// column of partials with independent loads.
+template <int D, int OUT>
+__global__ void __launch_bounds__(128) reduce_wide_kernel(const float* __restrict__ ws_o,
+                                                          const float* __restrict__ ws_ml,
+                                                          const int32_t* __restrict__ ctx,
+                                                          void* out, int Hq, int splits,
+                                                          int max_blocks, int pps, float v_scale) {
+  __shared__ float wsh[128];
+  __shared__ float red[4];
+  const int row = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int n = min(splits, used_splits(ctx, row / Hq, max_blocks, pps));
+  if (n <= 1) return;
+  const float* ml = ws_ml + (size_t)row * splits * 2;
+  float m = -INFINITY;
+  for (int s = tid; s < n; s += 128) m = fmaxf(m, ml[2 * s]);
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(kFull, m, off));
+  if (lane == 0) red[warp] = m;
+  __syncthreads();
+  const float M = fmaxf(fmaxf(red[0], red[1]), fmaxf(red[2], red[3]));
+  __syncthreads();
+  float L = 0.f, O = 0.f;
+  for (int base = 0; base < n; base += 128) {
+    const int s = base + tid;
+    float w = 0.f;
+    if (s < n && M != -INFINITY) {
+      const float ms = ml[2 * s];
+      w = (ms == -INFINITY) ? 0.f : fast_exp2(ms - M);
+      L += w * ml[2 * s + 1];
+    }
+    wsh[tid] = w;
+    __syncthreads();
+    const int cnt = min(128, n - base);
+    if (tid < D) {
+      const float* po = ws_o + ((size_t)row * splits + base) * D + tid;
+#pragma unroll 8
+      for (int j = 0; j < cnt; ++j) O += wsh[j] * po[(size_t)j * D];
+    }
+    __syncthreads();
+  }
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) L += __shfl_xor_sync(kFull, L, off);
+  if (lane == 0) red[warp] = L;
+  __syncthreads();
+  L = red[0] + red[1] + red[2] + red[3];
+  if (tid < D) store_out<OUT>(out, (size_t)row * D + tid, L > 0.f ? O * (v_scale / L) : 0.f);
+}
+
 // ---------------------------------------------------------------- host side
 struct KernelInfo {
   const void* fn;
@@ -480,22 +586,106 @@ struct Launcher {
                             {}};
     return ki;
   }
-  static cudaError_t launch(const DecodeArgs& a, int S, cudaStream_t st) {
+  static cudaError_t launch(const DecodeArgs& a, const CUtensorMap* tk, const CUtensorMap* tv,
+                            int S, cudaStream_t st) {
     dim3 grid(a.splits, a.Hkv, S);
-    decode_kernel<KV, D, OUT, kPsplit><<<grid, kThreads, Cfg<KV, D>::kSmem, st>>>(a);
+    decode_kernel<KV, D, OUT, kPsplit><<<grid, kThreads, Cfg<KV, D>::kSmem, st>>>(a, *tk, *tv);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess || a.splits == 1) return e;
     const int rows = S * a.Hq;
-    reduce_kernel<D, OUT><<<(rows + 3) / 4, 128, 0, st>>>(a.ws_o, a.ws_ml, a.out, rows, a.splits,
-                                                         a.v_scale);
+    if (a.splits <= 8)
+      reduce_rows_kernel<D, OUT><<<(rows + 3) / 4, 128, 0, st>>>(
+          a.ws_o, a.ws_ml, a.ctx, a.out, rows, a.Hq, a.splits, a.max_blocks, a.pages_per_split,
+          a.v_scale);
+    else
+      reduce_wide_kernel<D, OUT><<<rows, 128, 0, st>>>(a.ws_o, a.ws_ml, a.ctx, a.out, a.Hq,
+                                                      a.splits, a.max_blocks, a.pages_per_split,
+                                                      a.v_scale);
     return cudaGetLastError();
   }
 };
 
 struct Dispatch {
   KernelInfo* info;
-  cudaError_t (*launch)(const DecodeArgs&, int, cudaStream_t);
+  cudaError_t (*launch)(const DecodeArgs&, const CUtensorMap*, const CUtensorMap*, int,
+                        cudaStream_t);
 };
+
+// ---- TMA descriptors of the pool regions
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_tiled() {
+  static std::once_flag once;
+  static EncodeTiledFn fn = nullptr;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  });
+  return fn;
+}
+
+// A map over one layer's K (or V) region seen as rows of one token of one kv
+// head (row_bytes = head_dim * elem_bytes); a box is one 16-row tile.  Rows of
+// 256 bytes are described as [rows][2][128] so every box row is 128 bytes, the
+// largest the 128-byte swizzle accepts.
+int make_tile_map(CUtensorMap* m, void* base, int row_bytes, long long rows) {
+  EncodeTiledFn f = encode_tiled();
+  if (!f) return fail(PA_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
+  const CUtensorMapSwizzle swz =
+      (row_bytes % 128 == 0) ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE;
+  CUresult r;
+  if (row_bytes == 256) {
+    const cuuint64_t dims[3] = {128, 2, (cuuint64_t)rows};
+    const cuuint64_t strides[2] = {128, 256};
+    const cuuint32_t box[3] = {128, 2, 16};
+    const cuuint32_t es[3] = {1, 1, 1};
+    r = f(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, base, dims, strides, box, es,
+          CU_TENSOR_MAP_INTERLEAVE_NONE, swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  } else {
+    const cuuint64_t dims[2] = {(cuuint64_t)row_bytes, (cuuint64_t)rows};
+    const cuuint64_t strides[1] = {(cuuint64_t)row_bytes};
+    const cuuint32_t box[2] = {(cuuint32_t)row_bytes, 16};
+    const cuuint32_t es[2] = {1, 1};
+    r = f(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, base, dims, strides, box, es,
+          CU_TENSOR_MAP_INTERLEAVE_NONE, swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  }
+  if (r != CUDA_SUCCESS) return fail(PA_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d)", (int)r);
+  return PA_OK;
+}
+
+// The K and V maps of `layer`, encoded on first use.
+int layer_maps(pa_pool* pool, int layer, const CUtensorMap** tk, const CUtensorMap** tv) {
+  static_assert(sizeof(CUtensorMap) == sizeof(pa_tmap_blob), "tensor map size");
+  const pa_pool_desc& d = pool->desc;
+  if (pool->tmaps.size() != 2u * d.n_layers) {
+    pool->tmaps.assign(2u * d.n_layers, pa_tmap_blob{});
+    pool->tmap_ready.assign(d.n_layers, 0);
+  }
+  CUtensorMap* maps = reinterpret_cast<CUtensorMap*>(pool->tmaps.data());
+  if (!pool->tmap_ready[layer]) {
+    const int row_bytes = d.head_dim * pool->elem_bytes;
+    const long long rows = (long long)d.num_blocks * d.n_kv_heads * d.block_size;
+    int st = make_tile_map(&maps[2 * layer], pool->k + (size_t)layer * pool->layer_bytes,
+                           row_bytes, rows);
+    if (st) return st;
+    st = make_tile_map(&maps[2 * layer + 1], pool->v + (size_t)layer * pool->layer_bytes,
+                       row_bytes, rows);
+    if (st) return st;
+    pool->tmap_ready[layer] = 1;
+  }
+  *tk = &maps[2 * layer];
+  *tv = &maps[2 * layer + 1];
+  return PA_OK;
+}
 
 template <int KV, int D, int OUT>
 Dispatch make_dispatch() {
@@ -558,8 +748,13 @@ int check_shape(const pa_pool* pool, int S, int n_q_heads, int max_blocks) {
   return PA_OK;
 }
 
-// Splits along the pages: choose s minimising waves(s) * (pages per split +
-// fixed per-CTA cost), where waves(s) = ceil(S * Hkv * s / resident CTAs).
+// Splits along the pages.  With r resident CTAs, u = S * Hkv units and at
+// most B pages per unit, a split count s gives CTAs of P = ceil(B / s) pages;
+// if a fraction f of the units' pages is really there, the kernel takes about
+// ceil(f * u * s / r) waves of (P + c) page-times.  The contexts live on the
+// device, so the choice averages the full (f = 1) and the half-full (f = 1/2)
+// batch: the first favours whole waves for uniform batches, the second keeps
+// the longest sequences of a ragged batch from setting the kernel time.
 int auto_splits(const pa_pool* pool, int S, int max_blocks, int* out) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
@@ -570,16 +765,18 @@ int auto_splits(const pa_pool* pool, int S, int max_blocks, int* out) {
   Dispatch d = pick(pool->desc.kv_dtype, pool->desc.head_dim, in_dtype_of(pool->desc.kv_dtype));
   int occ = configure(*d.info, dev);
   if (occ <= 0) return fail(PA_ERR_CUDA, "decode kernel occupancy query failed");
-  const long long slots = (long long)sms * occ;
-  const long long units = (long long)std::max(S, 1) * pool->desc.n_kv_heads;
+  const double slots = (double)sms * occ;
+  const double units = (double)std::max(S, 1) * pool->desc.n_kv_heads;
   const int max_s = std::min(max_blocks, 256);
   int best = 1;
   double best_cost = 1e300;
   for (int s = 1; s <= max_s; ++s) {
     const int pps = (max_blocks + s - 1) / s;
     if (s > 1 && (max_blocks + pps - 1) / pps != s) continue;  // same as a smaller s
-    const long long waves = (units * s + slots - 1) / slots;
-    const double cost = (double)waves * (pps + 4.0 + (s > 1 ? 2.0 : 0.0));
+    const double per = pps + 4.0 + (s > 1 ? 2.0 : 0.0);
+    const double full = std::ceil(units * s / slots) * per;
+    const double half = std::ceil(0.5 * units * s / slots) * per;
+    const double cost = 0.5 * (full + half);
     if (cost < best_cost * 0.98) {
       best_cost = cost;
       best = s;
@@ -664,9 +861,11 @@ int pa_decode(pa_pool* pool, int layer, void* out, int out_dtype, const void* q,
   Dispatch disp = pick(d.kv_dtype, d.head_dim, out_dtype);
   if (configure(*disp.info, dev) <= 0) return fail(PA_ERR_CUDA, "decode kernel configuration failed");
 
+  const CUtensorMap *tk = nullptr, *tv = nullptr;
+  st = layer_maps(pool, layer, &tk, &tv);
+  if (st) return st;
+
   DecodeArgs a;
-  a.kpool = pool->k + (size_t)layer * pool->layer_bytes;
-  a.vpool = pool->v + (size_t)layer * pool->layer_bytes;
   a.q = static_cast<const uint16_t*>(q);
   a.out = out;
   a.ws_o = static_cast<float*>(workspace);
@@ -684,7 +883,7 @@ int pa_decode(pa_pool* pool, int layer, void* out, int out_dtype, const void* q,
   a.qk_scale_log2 = softmax_scale * log2e * (d.kv_dtype == PA_FP8_E4M3 ? d.k_scale : 1.f);
   a.v_scale = d.kv_dtype == PA_FP8_E4M3 ? d.v_scale : 1.f;
   a.err = err;
-  cudaError_t e = disp.launch(a, S, static_cast<cudaStream_t>(stream));
+  cudaError_t e = disp.launch(a, tk, tv, S, static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return fail(PA_ERR_CUDA, "decode launch: %s", cudaGetErrorString(e));
   return PA_OK;
 }

@@ -9,6 +9,11 @@
 
 #include "../../include/pa.h"
 
+// Opaque storage for one CUtensorMap (128 bytes, 64-byte aligned).
+struct alignas(64) pa_tmap_blob {
+  unsigned char bytes[128];
+};
+
 struct pa_pool {
   pa_pool_desc desc;
   uint8_t* k;                     // device, all layers
@@ -18,6 +23,10 @@ struct pa_pool {
   size_t layer_bytes;             // one layer of K (or V): num_blocks * n_kv_heads * tile_bytes
   std::vector<int32_t> refcount;  // per block
   std::vector<int32_t> free_stack;  // top = back()
+  // TMA descriptors of each layer's K and V regions ([2 * layer + {0: K, 1: V}]),
+  // encoded on first use by pa_decode.
+  std::vector<pa_tmap_blob> tmaps;
+  std::vector<char> tmap_ready;  // per layer
 };
 
 namespace pa {
