@@ -60,7 +60,12 @@ DESCRIPTION = {
 
 # DRAM traffic per decode launch from one ncu capture, valid only while the
 # decode source is byte-identical to the one measured.
-NCU_TRAFFIC = {"source_sha256": None, "bytes_per_launch": {}}
+NCU_TRAFFIC = {
+    "source_sha256": "9667eabbeac7d0b38166dbc16e345e9c5318380efe509de57f0c437f9f696056",
+    # dram__bytes_read.sum + dram__bytes_write.sum of one decode launch
+    "bytes_per_launch": {"llama3_70b_fp8_a": 1074140000 + 5422336,
+                         "llama3_70b_fp8_b": 2152005000 + 7624448},
+}
 
 
 # --------------------------------------------------------------------- workers

@@ -72,7 +72,14 @@ struct Cfg {
   static constexpr int kMergeBytes = kConsumerWarps * 8 * (D + 2) * 4;
   static constexpr int kDataBytes = kRingBytes > kMergeBytes ? kRingBytes : kMergeBytes;
   static constexpr int kAlign = 1024;  // a 128-byte-swizzled TMA destination is 1 KiB aligned
-  static constexpr int kSmem = kDataBytes + 2 * kStages * 8 + kAlign;
+  // FP8 pools keep the query fragments in shared memory instead of 16 registers
+  // per thread ([warp][D/16 pairs][32 lanes] x 8 bytes), which lets five CTAs
+  // share an SM; 16-bit pools are limited by their ring size anyway.
+  static constexpr bool kQInSmem = (KV == KV_E4M3);
+  static constexpr int kQBytes = kQInSmem ? kConsumerWarps * (D / 16) * 32 * 8 : 0;
+  static constexpr int kSmem = kDataBytes + 2 * kStages * 8 + kQBytes + kAlign;
+  // register budget, in CTAs per SM (16-bit pools: what their ring size allows)
+  static constexpr int kMinBlocks = kQInSmem ? 5 : (D == 128 ? 3 : 4);
   static constexpr bool kMmaBf16 = (KV == KV_BF16);
   static_assert(kStageBytes % kAlign == 0 || !kSwizzle, "tiles must stay 1 KiB aligned");
 };
@@ -118,7 +125,7 @@ __device__ __forceinline__ uint32_t tile_off(uint32_t off) {
 }
 
 template <int KV, int D, int OUT, bool PSPLIT>
-__global__ void __launch_bounds__(kThreads) decode_kernel(const DecodeArgs a,
+__global__ void __launch_bounds__(kThreads, (Cfg<KV, D>::kMinBlocks)) decode_kernel(const DecodeArgs a,
                                                           const __grid_constant__ CUtensorMap tmk,
                                                           const __grid_constant__ CUtensorMap tmv) {
   using C = Cfg<KV, D>;
@@ -260,6 +267,15 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(const DecodeArgs a,
       }
     }
 
+    uint2* qsm = nullptr;
+    if constexpr (C::kQInSmem) {
+      // park the fragments in shared memory: [pair j][lane] (conflict-free 8-byte loads)
+      qsm = reinterpret_cast<uint2*>(smem + C::kDataBytes + 2 * C::kStages * 8) + warp * (QW / 2) * 32;
+#pragma unroll
+      for (int j = 0; j < QW / 2; ++j) qsm[j * 32 + lane] = make_uint2(qf[2 * j], qf[2 * j + 1]);
+      __syncwarp();
+    }
+
     constexpr int KB = D / 4 * C::kElem;  // K bytes per row per thread
     constexpr int VB = D / 8 * C::kElem;  // V bytes per row per thread
     constexpr int RB = C::kRowBytes;
@@ -320,7 +336,8 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(const DecodeArgs a,
             const int j = 4 * c + jj;
             const uint32_t af[4] = {e4m3x2_to_f16x2(w0[jj]), e4m3x2_to_f16x2(w1[jj]),
                                     e4m3x2_to_f16x2(w0[jj] >> 16), e4m3x2_to_f16x2(w1[jj] >> 16)};
-            mma16816<false>(s, af, qf[2 * j], qf[2 * j + 1]);
+            const uint2 qj = qsm[j * 32 + lane];
+            mma16816<false>(s, af, qj.x, qj.y);
           }
         } else {
           const uint32_t a0[4] = {r0.x, r1.x, r0.y, r1.y};

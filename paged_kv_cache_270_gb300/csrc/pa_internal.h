@@ -7,7 +7,7 @@
 
 #include <vector>
 
-#include "../../include/pa.h"
+#include "pa.h"  // include/ is on the include path
 
 // Opaque storage for one CUtensorMap (128 bytes, 64-byte aligned).
 struct alignas(64) pa_tmap_blob {
