@@ -73,6 +73,9 @@ def _load():
         lib.or_paged_attention.argtypes = [i32, i32, i32, i32, i32, i32, P, P, f32, f32, P, i32,
                                            P, i32, P, i32, f64, P, P]
         lib.or_paged_attention.restype = i32
+        lib.or_paged_prefill.argtypes = [i32, i32, i32, i32, i32, i32, P, P, f32, f32, P, i32, P,
+                                          P, i32, P, i32, f64, P]
+        lib.or_paged_prefill.restype = i32
         lib.or_slab_attention.argtypes = [P, P, i32, i32, i32, P, i32, P, i32, f64, P]
         lib.or_slab_attention.restype = i32
         _lib = lib
@@ -199,4 +202,28 @@ def slab_attention(K: np.ndarray, V: np.ndarray, q: np.ndarray, ctx_lens: np.nda
                                    softmax_scale, _ptr(out))
     if st != 0:
         raise ValueError(f"oracle slab_attention status {st}")
+    return out
+
+
+def paged_prefill(kv_dtype: str, q_dtype: str, num_blocks: int, block_size: int, n_kv_heads: int,
+                  head_dim: int, k_pool: np.ndarray, v_pool: np.ndarray, k_scale: float,
+                  v_scale: float, q_bits: np.ndarray, q_start: np.ndarray,
+                  block_tables: np.ndarray, ctx_lens: np.ndarray,
+                  softmax_scale: float) -> np.ndarray:
+    """fp64 causal attention of each chunk over its paged history; out [T][Hq][d]."""
+    q_bits = np.ascontiguousarray(q_bits, dtype=np.uint16)
+    T, Hq, d = q_bits.shape
+    assert d == head_dim
+    qs = np.ascontiguousarray(q_start, dtype=np.int32)
+    tables = np.ascontiguousarray(block_tables, dtype=np.int32)
+    ctx = np.ascontiguousarray(ctx_lens, dtype=np.int32)
+    S = ctx.shape[0]
+    assert qs.shape[0] == S + 1 and qs[-1] == T
+    out = np.zeros((T, Hq, d), dtype=np.float64)
+    st = _load().or_paged_prefill(
+        dtype_code(kv_dtype), dtype_code(q_dtype), num_blocks, block_size, n_kv_heads, head_dim,
+        _ptr(k_pool), _ptr(v_pool), k_scale, v_scale, _ptr(q_bits), Hq, _ptr(qs), _ptr(tables),
+        tables.shape[1], _ptr(ctx), S, softmax_scale, _ptr(out))
+    if st != 0:
+        raise ValueError(f"oracle paged_prefill status {st}")
     return out

@@ -26,6 +26,12 @@
  *    contiguous K, V, then textbook softmax attention per query head, with
  *    query head g reading kv head floor(g / G), G = n_q_heads / n_kv_heads.
  *    Everything in fp64.  A sequence of context length 0 yields a zero output.
+ *  - Chunked prefill: a chunk of C new tokens of a sequence, already written
+ *    to the cache, each attend causally to every earlier token and to
+ *    themselves (prefill split into packets interleaved with decode steps,
+ *    "Optimización de KV Cache ...", sections 5 and 6.3).  Query j of a chunk
+ *    that ends the sequence's ctx tokens sits at position ctx - C + j and sees
+ *    tokens [0, ctx - C + j].
  *  - Copy of whole blocks (K and V tiles of every kv head), the copy-on-write
  *    step of shared prefixes ("PagedAttention y Gestión de KV-Cache", section
  *    3.01; "KV Cache y PagedAttention", "Cómo PagedAttention soluciona esto").
@@ -340,4 +346,75 @@ int or_slab_attention(const double* K, const double* V, int max_ctx, int n_kv_he
     }
   }
   return 0;
+}
+
+/* ---------------------------------------------------------------------------
+ * Chunked prefill over the paged cache.
+ *   q        : [T][n_q_heads][head_dim] 16-bit bit patterns; the chunk of
+ *              sequence s is rows q_start[s] .. q_start[s+1]-1
+ *   ctx_lens : [S] tokens of sequence s in the cache, the chunk included
+ *   out      : [T][n_q_heads][head_dim] fp64
+ * Returns 0, -1 on an invalid block id / length, -2 on a bad head count.
+ * ------------------------------------------------------------------------- */
+int or_paged_prefill(int kv_dtype, int q_dtype, int num_blocks, int block_size, int n_kv_heads,
+                     int head_dim, const uint8_t* k_pool, const uint8_t* v_pool, float k_scale,
+                     float v_scale, const uint16_t* q, int n_q_heads, const int32_t* q_start,
+                     const int32_t* block_tables, int max_blocks_per_seq, const int32_t* ctx_lens,
+                     int S, double softmax_scale, double* out) {
+  if (n_kv_heads <= 0 || n_q_heads % n_kv_heads != 0) return -2;
+  int G = n_q_heads / n_kv_heads;
+  int status = 0;
+  double* qv = (double*)malloc(sizeof(double) * (size_t)head_dim);
+  for (int s = 0; s < S; ++s) {
+    int n = ctx_lens[s];
+    int C = q_start[s + 1] - q_start[s];
+    for (long long r = q_start[s]; r < q_start[s + 1]; ++r)
+      for (long long i = 0; i < (long long)n_q_heads * head_dim; ++i)
+        out[r * n_q_heads * head_dim + i] = 0.0;
+    int nblk = (n + block_size - 1) / block_size;
+    if (n < 0 || C < 0 || C > n || nblk > max_blocks_per_seq) {
+      status = -1;
+      continue;
+    }
+    int bad = 0;
+    for (int j = 0; j < nblk; ++j) {
+      int b = block_tables[(long long)s * max_blocks_per_seq + j];
+      if (b < 0 || b >= num_blocks) bad = 1;
+    }
+    if (bad) {
+      status = -1;
+      continue;
+    }
+    /* gather the sequence's pages in logical order (as for decode) */
+    long long row = (long long)n_kv_heads * head_dim;
+    double* K = (double*)malloc(sizeof(double) * (size_t)(n > 0 ? n * row : 1));
+    double* V = (double*)malloc(sizeof(double) * (size_t)(n > 0 ? n * row : 1));
+    for (int tok = 0; tok < n; ++tok) {
+      int j = tok / block_size, off = tok % block_size;
+      int b = block_tables[(long long)s * max_blocks_per_seq + j];
+      for (int h = 0; h < n_kv_heads; ++h) {
+        for (int i = 0; i < head_dim; ++i) {
+          long long idx = pool_index(b, h, off, i, n_kv_heads, block_size, head_dim);
+          K[tok * row + h * head_dim + i] = pool_value(kv_dtype, k_pool, idx, k_scale);
+          V[tok * row + h * head_dim + i] = pool_value(kv_dtype, v_pool, idx, v_scale);
+        }
+      }
+    }
+    /* query j sees tokens [0, n - C + j] */
+    for (int j = 0; j < C; ++j) {
+      long long r = q_start[s] + j;
+      int visible = n - C + j + 1;
+      for (int g = 0; g < n_q_heads; ++g) {
+        int h = g / G;
+        const uint16_t* qg = q + (r * n_q_heads + g) * head_dim;
+        for (int i = 0; i < head_dim; ++i) qv[i] = or_value16(q_dtype, qg[i]);
+        attend(qv, K + h * head_dim, V + h * head_dim, row, visible, head_dim, softmax_scale,
+               out + (r * n_q_heads + g) * head_dim, NULL);
+      }
+    }
+    free(K);
+    free(V);
+  }
+  free(qv);
+  return status;
 }
