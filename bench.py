@@ -47,7 +47,9 @@ WORKLOADS = {
     "llama3_70b_fp8_b": ["llama3_70b_fp8_b"],
     "llama3_8b_bf16": ["llama3_8b_bf16"],
     "llama3_8b_fp8": ["llama3_8b_fp8"],
+    "llama3_70b_fp8_prefill": ["llama3_70b_fp8_prefill"],
 }
+PREFILL_METRIC = "chunked prefill attention over a paged FP8 KV cache: TFLOP/s, 1 GPU"
 DESCRIPTION = {
     "llama3_70b_fp8": "Llama-3.1-70B-shaped single-layer decode, FP8 E4M3 paged KV (per-tensor "
                       "scales amax/448), Hq 64 / Hkv 8 / d 128, 16-token blocks, random block "
@@ -56,6 +58,9 @@ DESCRIPTION = {
     "llama3_70b_fp8_b": "Llama-3.1-70B-shaped FP8 decode, 256 x 4096 tokens",
     "llama3_8b_bf16": "Llama-3.1-8B-shaped bf16 decode, 64 seqs, ctx U[512,4096]",
     "llama3_8b_fp8": "Llama-3.1-8B-shaped FP8 decode, 64 seqs, ctx U[512,4096], 1% K outliers",
+    "llama3_70b_fp8_prefill": "Llama-3.1-70B-shaped chunked prefill, FP8 E4M3 paged KV, Hq 64 / "
+                              "Hkv 8 / d 128: 4 sequences each prefilling a 2048-token chunk after "
+                              "6144 cached tokens (one 8192-token packet), causal",
 }
 
 # DRAM traffic per decode launch from one ncu capture, valid only while the
@@ -84,6 +89,31 @@ def _gen_bits(args):
     w = W.make(name)
     k, v = w.kv_bits(s, lo, hi)
     return s, lo, hi, k, v
+
+
+def _oracle_prefill_worker(args):
+    """Times the fp64 oracle's chunked prefill on the last `rows` queries of one
+    sequence; returns (flops, t_start, t_end)."""
+    name, s, rows, k_scale, v_scale = args
+    import oracle
+    from paged_kv_cache_270_gb300 import workloads as W
+    w = W.make(name)
+    n = int(w.ctx_lens[s])
+    nb = -(-n // 16)
+    nbytes = oracle.pool_bytes(w.kv_dtype, nb, 16, w.n_kv_heads, w.head_dim)
+    kp, vp = np.zeros(nbytes, np.uint8), np.zeros(nbytes, np.uint8)
+    k, v = w.kv_bits(s, 0, n)
+    oracle.reshape_and_cache(w.kv_dtype, nb, 16, w.n_kv_heads, w.head_dim, k, v,
+                             np.arange(n, dtype=np.int64), k_scale, v_scale, kp, vp)
+    q = w.prefill_q_bits()[s * w.chunk + w.chunk - rows: (s + 1) * w.chunk]
+    t0 = time.time()
+    oracle.paged_prefill(w.kv_dtype, w.in_dtype, nb, 16, w.n_kv_heads, w.head_dim, kp, vp,
+                         k_scale, v_scale, q, np.array([0, rows], np.int32),
+                         np.arange(nb, dtype=np.int32)[None, :], np.array([n], np.int32),
+                         w.softmax_scale)
+    t1 = time.time()
+    keys = rows * n - rows * (rows - 1) // 2
+    return 4 * w.head_dim * w.n_q_heads * keys, t0, t1
 
 
 def _oracle_worker(args):
@@ -485,6 +515,153 @@ def run_gb300(args, rank, world, local_rank):
     print(json.dumps(line), flush=True)
 
 
+def _peak_tflops():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            return float(json.load(f)["bf16_tflops"]), "measured (bf16_tflops, burst)"
+    except Exception:
+        return 1900.0, "fallback"
+
+
+def run_prefill(args, rank, world, local_rank):
+    """Chunked prefill: per step, write the chunk's K/V into its slots, then the
+    causal attention of the chunk's queries over each sequence's pages."""
+    import torch
+
+    from paged_kv_cache_270_gb300 import _native as N
+    from paged_kv_cache_270_gb300 import workloads as W
+    from paged_kv_cache_270_gb300.pool import KVPool
+    torch.cuda.set_device(local_rank)
+    name = args.workload
+    w = W.make(name)
+    procs = max(1, min(os.cpu_count() or 1, 16))
+    with mp.get_context("spawn").Pool(procs) as pp:
+        chunks = [(name, s, lo, min(int(w.ctx_lens[s]), lo + 16384))
+                  for s in range(w.S) for lo in range(0, int(w.ctx_lens[s]), 16384)]
+        ka = va = 0.0
+        for a_, b_ in pp.imap_unordered(_gen_amax, chunks, chunksize=2):
+            ka, va = max(ka, a_), max(va, b_)
+        w.k_scale = float(np.float32(ka) / np.float32(448.0))
+        w.v_scale = float(np.float32(va) / np.float32(448.0))
+        pool = KVPool(1, w.num_blocks, w.n_kv_heads, w.head_dim, w.kv_dtype, w.k_scale, w.v_scale)
+        in_t = torch.bfloat16
+        new_k, new_v, new_slots = [], [], []
+        for s, lo, hi, k, v in pp.imap(_gen_bits, chunks, chunksize=1):
+            pos = np.arange(lo, hi, dtype=np.int64)
+            slots = w.block_tables[s, pos // 16].astype(np.int64) * 16 + pos % 16
+            pool.reshape_and_cache(torch.from_numpy(k.view(np.int16)).view(in_t).cuda(),
+                                   torch.from_numpy(v.view(np.int16)).view(in_t).cuda(),
+                                   torch.from_numpy(slots).cuda())
+            first = int(w.ctx_lens[s]) - w.chunk  # the chunk's K/V are rewritten every step
+            sel = pos >= first
+            new_k.append(k[sel]); new_v.append(v[sel]); new_slots.append(slots[sel])
+        cpu = None
+        if rank == 0 and world == 1 and not args.no_cpu:
+            rows = 16
+            res = pp.map(_oracle_prefill_worker,
+                         [(name, s % w.S, rows, w.k_scale, w.v_scale) for s in range(procs)])
+            fl = sum(r[0] for r in res)
+            wall = max(r[2] for r in res) - min(r[1] for r in res)
+            cpu = {"value": fl / wall / 1e12, "unit": "TFLOP/s", "cores": procs, "kind": "oracle",
+                   "sample": f"{procs} x the last {rows} queries of a 2048-token chunk "
+                             f"({fl / 1e9:.1f} GFLOP, {wall:.1f} s wall, fp64)"}
+    pin = lambda a_: torch.from_numpy(np.ascontiguousarray(a_)).pin_memory()  # noqa: E731
+    h_q = pin(w.prefill_q_bits().view(np.int16)).view(in_t)
+    h_k = pin(np.concatenate(new_k).view(np.int16)).view(in_t)
+    h_v = pin(np.concatenate(new_v).view(np.int16)).view(in_t)
+    h_slots = pin(np.concatenate(new_slots))
+    h_qs = pin((np.arange(w.S + 1) * w.chunk).astype(np.int32))
+    h_tab = pin(w.block_tables.astype(np.int32))
+    h_ctx = pin(w.ctx_lens.astype(np.int32))
+    hs = [h_q, h_k, h_v, h_slots, h_qs, h_tab, h_ctx]
+    ds = [t.cuda() for t in hs]
+    d_q, d_k, d_v, d_slots, d_qs, d_tab, d_ctx = ds
+    d_out = torch.empty_like(d_q)
+    h_out = torch.empty(d_out.shape, dtype=in_t).pin_memory()
+    stream = torch.cuda.current_stream()
+    sh = int(stream.cuda_stream)
+    T = w.S * w.chunk
+
+    def step(ev=None):
+        N.pa_reshape_and_cache(pool.handle, 0, d_k.data_ptr(), d_v.data_ptr(), d_slots.data_ptr(),
+                               T, sh)
+        if ev is not None:
+            ev[0].record(stream)
+        N.pa_prefill(pool.handle, 0, d_out.data_ptr(), N.PA_BF16, d_q.data_ptr(), d_qs.data_ptr(),
+                     d_tab.data_ptr(), w.max_blocks, d_ctx.data_ptr(), w.S, w.n_q_heads, w.chunk,
+                     w.softmax_scale, sh)
+        if ev is not None:
+            ev[1].record(stream)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    if pool.device_error():
+        raise RuntimeError("device error in prefill warm-up")
+    K = args.steps
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(K)]
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    sampler = ClockSampler(local_rank)
+    _barrier(world)
+    torch.cuda.synchronize()
+    with sampler:
+        e0.record(stream)
+        for k in range(K):
+            step(evs[k])
+        e1.record(stream)
+        torch.cuda.synchronize()
+    _barrier(world)
+    t_max = _max_over_ranks(e0.elapsed_time(e1) / 1e3, world)
+    pre_ms = [ev[0].elapsed_time(ev[1]) for ev in evs]
+    e2e = None
+    if not args.no_e2e:
+        def e2e_step():
+            for d_, h_ in zip(ds, hs):
+                d_.copy_(h_, non_blocking=True)
+            step()
+            h_out.copy_(d_out, non_blocking=True)
+            stream.synchronize()
+        for _ in range(2):
+            e2e_step()
+        _barrier(world)
+        f0, f1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        f0.record(stream)
+        for _ in range(K):
+            e2e_step()
+        f1.record(stream)
+        torch.cuda.synchronize()
+        te = _max_over_ranks(f0.elapsed_time(f1) / 1e3, world)
+        e2e = {"value": round(world * w.prefill_flops() * K / te / 1e12, 2), "unit": "TFLOP/s",
+               "h2d_bytes_per_step": sum(t_.numel() * t_.element_size() for t_ in hs),
+               "d2h_bytes_per_step": h_out.numel() * h_out.element_size(),
+               "ms_per_step": round(te / K * 1e3, 4)}
+    if pool.device_error():
+        raise RuntimeError("device error in prefill")
+    if rank != 0:
+        return
+    flops = w.prefill_flops()
+    peak, peak_kind = _peak_tflops()
+    achieved = flops / (statistics.fmean(pre_ms) / 1e3) / 1e12
+    line = {
+        "metric": PREFILL_METRIC, "value": round(world * flops * K / t_max / 1e12, 2),
+        "unit": "TFLOP/s", "n_gpus": world, "steps": K, "warmup": args.warmup,
+        "ms_per_step": round(t_max / K * 1e3, 4), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "e4m3 KV / f16 tensor-core MMA / f32 accumulate",
+        "data": "synthetic (seeded N(0,1) q/k/v, random block tables)",
+        "config": {"workload": DESCRIPTION[name], "tokens_per_step": T,
+                   "flops_per_step": flops, "parallelism": "1 GPU" if world == 1 else
+                   f"replicas x{world}"},
+        "prefill_ms_median": round(statistics.median(pre_ms), 4),
+        "tokens_per_s": round(world * T * K / t_max, 1),
+        "roofline": {"kernel": "prefill_kernel", "bound": "tensor", "achieved": round(achieved, 1),
+                     "peak": peak, "peak_kind": peak_kind, "unit": "TFLOP/s",
+                     "frac": round(achieved / peak, 4), "traffic": None,
+                     "algorithmic_flops_per_step": flops},
+        "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": 2 * K, "clocks": sampler.summary(),
+    }
+    print(json.dumps(line), flush=True)
+
+
 def run_reference(args, rank, world):
     """The fp64 oracle on the host cores, a bounded sample of the workload per step."""
     if rank != 0:
@@ -551,7 +728,14 @@ def main():
         import torch.distributed as dist
         dist.init_process_group("nccl" if args.impl == "gb300" else "gloo")
     try:
-        if args.impl == "reference":
+        if args.workload.endswith("_prefill"):
+            if args.impl == "reference":
+                if rank == 0:
+                    print(json.dumps({"impl": "reference", "unavailable":
+                                      "the oracle leg covers the decode workloads only"}))
+            else:
+                run_prefill(args, rank, world, local_rank)
+        elif args.impl == "reference":
             run_reference(args, rank, world)
         else:
             run_gb300(args, rank, world, local_rank)

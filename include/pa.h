@@ -261,6 +261,26 @@ PA_API int pa_decode_no_alloc(pa_pool* pool, int layer, void* out, int out_dtype
                               const int32_t* ctx_lens_dev, int S, int n_q_heads,
                               float softmax_scale, int num_splits, void* stream);
 
+/* Chunked prefill: causal attention of a chunk of new tokens per sequence over
+ * its paged history ("Optimización de KV Cache ...", sections 5 and 6.3:
+ * prefill split into packets, e.g. 8,192 tokens, interleaved with decode).
+ * The chunk's K/V must already be in the cache (pa_reshape_and_cache).
+ *   q                 device [T][n_q_heads][head_dim], the pool's query dtype;
+ *                     sequence s's chunk is rows q_start[s] .. q_start[s+1]-1
+ *   q_start_dev       device int32 [S+1], non-decreasing, q_start[0] = 0
+ *   ctx_lens_dev      device int32 [S]: tokens of each sequence in the cache,
+ *                     chunk included (>= its chunk length)
+ *   out               device [T][n_q_heads][head_dim], q's dtype or PA_FP32
+ *   max_chunk         an upper bound on every chunk length (sizes the grid)
+ * Query row j of a chunk of C tokens sits at position ctx - C + j and attends
+ * to tokens [0, ctx - C + j] of its sequence (grouped-query heads as in
+ * pa_decode).  Invalid ids or lengths set PA_ERR_BOUNDS in the device error
+ * word (those rows are then not written).  No scratch memory is needed. */
+PA_API int pa_prefill(pa_pool* pool, int layer, void* out, int out_dtype, const void* q,
+                      const int32_t* q_start_dev, const int32_t* block_tables_dev,
+                      int max_blocks_per_seq, const int32_t* ctx_lens_dev, int S, int n_q_heads,
+                      int max_chunk, float softmax_scale, void* stream);
+
 /* Synchronises `stream`, then reads and clears the current device's error word.
  * *code = PA_OK or the first PA_ERR_* a kernel recorded since the last read.
  * The word is shared by every pool on the device. */

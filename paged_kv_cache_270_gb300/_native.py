@@ -76,6 +76,7 @@ _SIGS = [
     ("pa_decode_num_splits", [_P, _I, _I, _I, ctypes.POINTER(_I)]),
     ("pa_decode_workspace_bytes", [_P, _I, _I, _I, _I, ctypes.POINTER(_SZ)]),
     ("pa_decode", [_P, _I, _P, _I, _P, _P, _I, _P, _I, _I, ctypes.c_float, _I, _P, _SZ, _P]),
+    ("pa_prefill", [_P, _I, _P, _I, _P, _P, _P, _I, _P, _I, _I, _I, ctypes.c_float, _P]),
     ("pa_decode_no_alloc", [_P, _I, _P, _I, _P, _P, _I, _P, _I, _I, ctypes.c_float, _I, _P]),
     ("pa_get_device_error", [_P, ctypes.POINTER(_I), _P]),
 ]
@@ -231,6 +232,14 @@ def pa_decode(pool: int, layer: int, out_ptr: int, out_dtype: int, q_ptr: int, t
     _check(lib().pa_decode(pool, layer, out_ptr, out_dtype, q_ptr, tables_ptr, max_blocks_per_seq,
                            ctx_lens_ptr, S, n_q_heads, softmax_scale, num_splits, workspace_ptr,
                            workspace_bytes, stream))
+
+
+def pa_prefill(pool: int, layer: int, out_ptr: int, out_dtype: int, q_ptr: int, q_start_ptr: int,
+               tables_ptr: int, max_blocks_per_seq: int, ctx_lens_ptr: int, S: int,
+               n_q_heads: int, max_chunk: int, softmax_scale: float, stream: int) -> None:
+    _check(lib().pa_prefill(pool, layer, out_ptr, out_dtype, q_ptr, q_start_ptr, tables_ptr,
+                            max_blocks_per_seq, ctx_lens_ptr, S, n_q_heads, max_chunk,
+                            softmax_scale, stream))
 
 
 def pa_decode_no_alloc(pool: int, layer: int, out_ptr: int, out_dtype: int, q_ptr: int,

@@ -679,7 +679,7 @@ int make_tile_map(CUtensorMap* m, void* base, int row_bytes, long long rows) {
   return PA_OK;
 }
 
-// The K and V maps of `layer`, encoded on first use.
+// The K and V maps of `layer`, encoded on first use (shared with the prefill).
 int layer_maps(pa_pool* pool, int layer, const CUtensorMap** tk, const CUtensorMap** tv) {
   static_assert(sizeof(CUtensorMap) == sizeof(pa_tmap_blob), "tensor map size");
   const pa_pool_desc& d = pool->desc;

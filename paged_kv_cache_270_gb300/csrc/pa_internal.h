@@ -41,3 +41,12 @@ unsigned int* device_error_word();
 int check_pool_layer(const pa_pool* pool, int layer);
 
 }  // namespace pa
+
+struct CUtensorMap_st;
+namespace pa {
+// TMA descriptors (CUtensorMap) of one layer's K and V regions, encoded on
+// first use and kept in the pool; rows of one token of one kv head, a box is
+// one 16-token tile, 128-byte swizzled when a row is 128 or 256 bytes.
+int layer_maps(pa_pool* pool, int layer, const CUtensorMap_st** tk, const CUtensorMap_st** tv);
+
+}  // namespace pa

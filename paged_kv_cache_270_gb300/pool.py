@@ -146,5 +146,28 @@ class KVPool:
                     float(softmax_scale), num_splits, ws_ptr, ws_bytes, _stream_handle(stream))
         return out
 
+    def prefill(self, q: torch.Tensor, q_start: torch.Tensor, block_tables: torch.Tensor,
+                ctx_lens: torch.Tensor, max_chunk: int, out: torch.Tensor | None = None,
+                out_dtype: torch.dtype | None = None, softmax_scale: float | None = None,
+                layer: int = 0, stream=None) -> torch.Tensor:
+        """Causal attention of packed chunks q [T, Hq, D] (rows q_start[s] ..
+        q_start[s+1]-1 for sequence s) over their paged history."""
+        _need(q, "q", self.in_dtype, self.device)
+        _need(q_start, "q_start", torch.int32, self.device)
+        _need(block_tables, "block_tables", torch.int32, self.device)
+        _need(ctx_lens, "ctx_lens", torch.int32, self.device)
+        T, Hq, D = q.shape
+        if out is None:
+            out = torch.empty((T, Hq, D), dtype=out_dtype or q.dtype, device=self.device)
+        _need(out, "out", None, self.device)
+        code = {v: k for k, v in _TORCH_OUT.items()}[out.dtype]
+        if softmax_scale is None:
+            softmax_scale = 1.0 / math.sqrt(D)
+        N.pa_prefill(self.handle, layer, out.data_ptr(), code, q.data_ptr(), q_start.data_ptr(),
+                     block_tables.data_ptr(), block_tables.shape[1], ctx_lens.data_ptr(),
+                     ctx_lens.numel(), Hq, int(max_chunk), float(softmax_scale),
+                     _stream_handle(stream))
+        return out
+
     def device_error(self, stream=None) -> int:
         return N.pa_get_device_error(self.handle, _stream_handle(stream))

@@ -25,6 +25,9 @@ Workloads (shapes follow the model families the pages name: Llama-3.1 8B and
                        one token per sequence
   llama3_70b_fp8_a     Hq 64 / Hkv 8, d 128, FP8: 4 seqs x 131072 tokens
   llama3_70b_fp8_b     same shapes: 256 seqs x 4096 tokens
+  llama3_70b_fp8_prefill  70B shapes, FP8: 4 sequences, each prefilling a
+                       2048-token chunk after 6144 cached tokens (one
+                       8192-token packet of chunked prefill)
   prefix_share_bf16    Hq 32 / Hkv 8, d 128, bf16: 64 requests sharing a
                        2048-token prefix, each with a U[128, 1024] suffix
                        (tables come from the block allocator, not from here)
@@ -40,7 +43,7 @@ BLOCK = 16
 CHUNK = 256  # tokens per independently seeded draw
 
 NAMES = ("tiny_fp16", "llama3_8b_bf16", "llama3_8b_fp8", "llama3_70b_fp8_a",
-         "llama3_70b_fp8_b", "prefix_share_bf16")
+         "llama3_70b_fp8_b", "llama3_70b_fp8_prefill", "prefix_share_bf16")
 
 
 def f32_to_bf16_bits(x: np.ndarray) -> np.ndarray:
@@ -81,6 +84,7 @@ class Workload:
     k_scale: float = 1.0
     v_scale: float = 1.0
     kv_seed: int | None = None
+    chunk: int = 0             # prefill workloads: new tokens per sequence (the last ones)
 
     # ----------------------------------------------------------------- shapes
     @property
@@ -145,6 +149,20 @@ class Workload:
         rq = np.random.default_rng([self.seed, 3, step])
         q = rq.standard_normal((self.S, self.n_q_heads, self.head_dim), dtype=np.float32)
         return self._cast(q)
+
+    def prefill_q_bits(self) -> np.ndarray:
+        """Queries of the chunks, packed [S * chunk, Hq, d] (sequence-major)."""
+        rq = np.random.default_rng([self.seed, 6])
+        q = rq.standard_normal((self.S * self.chunk, self.n_q_heads, self.head_dim),
+                               dtype=np.float32)
+        return self._cast(q)
+
+    def prefill_flops(self) -> int:
+        """QK and PV multiply-adds of the causal chunks: query j of a chunk ending
+        at ctx sees ctx - chunk + j + 1 keys; 4 * head_dim flops per key per head."""
+        keys = sum(int(n) * self.chunk - self.chunk * (self.chunk - 1) // 2
+                   for n in self.ctx_lens)
+        return 4 * self.head_dim * self.n_q_heads * keys
 
     def final_ctx(self) -> np.ndarray:
         """Context lengths after the last decode step."""
@@ -234,6 +252,11 @@ def make(name: str, scale_down: int = 1, steps: int | None = None) -> Workload:
     if name == "llama3_70b_fp8_b":
         return _paged(3, name, "fp8_e4m3", 64, 8, 128, [4096 // sd] * max(2, 256 // sd),
                       kv_seed=1003 + 10_000)
+    if name == "llama3_70b_fp8_prefill":
+        # one 8,192-token prefill packet: 4 sequences x 2,048 new tokens after 6,144 cached
+        w = _paged(5, name, "fp8_e4m3", 64, 8, 128, [(6144 + 2048) // sd] * 4)
+        w.chunk = 2048 // sd
+        return w
     raise KeyError(name)
 
 
