@@ -48,7 +48,10 @@ WORKLOADS = {
     "llama3_8b_bf16": ["llama3_8b_bf16"],
     "llama3_8b_fp8": ["llama3_8b_fp8"],
     "llama3_70b_fp8_prefill": ["llama3_70b_fp8_prefill"],
+    "prefix_cache_bf16": ["prefix_cache_bf16"],
 }
+PREFIX_METRIC = ("prefill with block-hash prefix caching: prompt tokens served per second "
+                 "(shared 2048-token system prompt), 1 GPU")
 PREFILL_METRIC = "chunked prefill attention over a paged FP8 KV cache: TFLOP/s, 1 GPU"
 DESCRIPTION = {
     "llama3_70b_fp8": "Llama-3.1-70B-shaped single-layer decode, FP8 E4M3 paged KV (per-tensor "
@@ -58,6 +61,10 @@ DESCRIPTION = {
     "llama3_70b_fp8_b": "Llama-3.1-70B-shaped FP8 decode, 256 x 4096 tokens",
     "llama3_8b_bf16": "Llama-3.1-8B-shaped bf16 decode, 64 seqs, ctx U[512,4096]",
     "llama3_8b_fp8": "Llama-3.1-8B-shaped FP8 decode, 64 seqs, ctx U[512,4096], 1% K outliers",
+    "prefix_cache_bf16": "Llama-3.1-8B-shaped bf16 (Hq 32 / Hkv 8 / d 128): 64 requests whose "
+                         "prompts share a 2048-token system prompt, each with its own U[128,1024] "
+                         "suffix; a step hashes and looks up every prompt, writes and prefills "
+                         "only the uncached tokens, then releases the requests",
     "llama3_70b_fp8_prefill": "Llama-3.1-70B-shaped chunked prefill, FP8 E4M3 paged KV, Hq 64 / "
                               "Hkv 8 / d 128: 4 sequences each prefilling a 2048-token chunk after "
                               "6144 cached tokens (one 8192-token packet), causal",
@@ -662,6 +669,123 @@ def run_prefill(args, rank, world, local_rank):
     print(json.dumps(line), flush=True)
 
 
+def run_prefix_cache(args, rank, world, local_rank):
+    """Prompts sharing a system prompt, served with and without the prefix cache."""
+    import torch
+
+    from paged_kv_cache_270_gb300 import _native as N
+    from paged_kv_cache_270_gb300 import workloads as W
+    from paged_kv_cache_270_gb300.pool import KVPool
+    torch.cuda.set_device(local_rank)
+    ps = W.PrefixShare()
+    R, P = ps.n_requests, ps.prefix_tokens
+    suf = ps.suffix_lens()
+    rng = np.random.default_rng(ps.seed + 7)
+    system = rng.integers(0, 128000, P).astype(np.int32)
+    prompts = [np.concatenate([system, rng.integers(0, 128000, int(n)).astype(np.int32)])
+               for n in suf]
+    kp, vp = ps.prefix_kv(P)
+    sk = [ps.suffix_kv(r, int(n)) for r, n in enumerate(suf)]
+    bt = lambda a_: torch.from_numpy(np.ascontiguousarray(a_).view(np.int16)).view(torch.bfloat16).cuda()  # noqa: E731
+    d_kp, d_vp = bt(kp), bt(vp)
+    d_ks, d_vs = bt(np.concatenate([k for k, _ in sk])), bt(np.concatenate([v for _, v in sk]))
+    d_kf = bt(np.concatenate([np.concatenate([kp, k]) for k, _ in sk]))
+    d_vf = bt(np.concatenate([np.concatenate([vp, v]) for _, v in sk]))
+    ctx = (P + suf).astype(np.int32)
+    width = int(-(-ctx.max() // 16))
+    q_suf = bt(ps.q_bits(int(suf.sum())))
+    q_full = bt(ps.q_bits(int(ctx.sum()), step=1))
+    d_ctx = torch.from_numpy(ctx).cuda()
+    qs_suf = torch.from_numpy(np.concatenate([[0], np.cumsum(suf)]).astype(np.int32)).cuda()
+    qs_full = torch.from_numpy(np.concatenate([[0], np.cumsum(ctx)]).astype(np.int32)).cuda()
+    out_suf, out_full = torch.empty_like(q_suf), torch.empty_like(q_full)
+    blocks_needed = int(sum(-(-int(c) // 16) for c in ctx))
+    cached = KVPool(1, 128 + blocks_needed, 8, 128, "bf16")
+    plain = KVPool(1, blocks_needed, 8, 128, "bf16")
+    sh = int(torch.cuda.current_stream().cuda_stream)
+    # the system prompt is prefilled once and registered
+    sys_hashes = N.pa_prefix_hash(system)
+    sys_ids = cached.alloc(len(sys_hashes))
+    pos = np.arange(P, dtype=np.int64)
+    cached.reshape_and_cache(d_kp, d_vp, torch.from_numpy(sys_ids[pos // 16].astype(np.int64) * 16
+                                                           + pos % 16).cuda())
+    cached.prefix_register(sys_hashes, sys_ids)
+    N.pa_block_free(cached.handle, sys_ids)  # only the cache holds the system prompt now
+
+    def serve(pool, use_cache):
+        tables = np.zeros((R, width), np.int32)
+        slots, held = [], []
+        lookups = hits = 0
+        for r in range(R):
+            n = int(ctx[r])
+            hit = np.zeros(0, np.int32)
+            if use_cache:
+                hs = N.pa_prefix_hash(prompts[r])
+                hit = N.pa_prefix_lookup(pool.handle, hs)
+                lookups += len(hs)
+                hits += len(hit)
+            own = N.pa_block_alloc(pool.handle, -(-n // 16) - len(hit))
+            row = np.concatenate([hit, own]).astype(np.int32)
+            tables[r, :len(row)] = row
+            held.append(row)
+            first = P if use_cache else 0
+            p_ = np.arange(first, n, dtype=np.int64)
+            slots.append(row[p_ // 16].astype(np.int64) * 16 + p_ % 16)
+        d_slots = torch.from_numpy(np.concatenate(slots)).cuda()
+        d_tab = torch.from_numpy(tables).cuda()
+        if use_cache:
+            N.pa_reshape_and_cache(pool.handle, 0, d_ks.data_ptr(), d_vs.data_ptr(),
+                                   d_slots.data_ptr(), d_slots.numel(), sh)
+            N.pa_prefill(pool.handle, 0, out_suf.data_ptr(), N.PA_BF16, q_suf.data_ptr(),
+                         qs_suf.data_ptr(), d_tab.data_ptr(), width, d_ctx.data_ptr(), R, 32,
+                         int(suf.max()), 1.0 / math.sqrt(128), sh)
+        else:
+            N.pa_reshape_and_cache(pool.handle, 0, d_kf.data_ptr(), d_vf.data_ptr(),
+                                   d_slots.data_ptr(), d_slots.numel(), sh)
+            N.pa_prefill(pool.handle, 0, out_full.data_ptr(), N.PA_BF16, q_full.data_ptr(),
+                         qs_full.data_ptr(), d_tab.data_ptr(), width, d_ctx.data_ptr(), R, 32,
+                         int(ctx.max()), 1.0 / math.sqrt(128), sh)
+        torch.cuda.synchronize()
+        for row in held:
+            N.pa_block_free(pool.handle, row)
+        return lookups, hits
+
+    res = {}
+    for mode, pool in (("cached", cached), ("uncached", plain)):
+        for _ in range(args.warmup):
+            serve(pool, mode == "cached")
+        if pool.device_error():
+            raise RuntimeError("device error in prefix-cache warm-up")
+        _barrier(world)
+        t0 = time.perf_counter()
+        lk = ht = 0
+        for _ in range(args.steps):
+            a_, b_ = serve(pool, mode == "cached")
+            lk += a_
+            ht += b_
+        t = _max_over_ranks(time.perf_counter() - t0, world)
+        res[mode] = (t / args.steps, lk, ht)
+    if rank != 0:
+        return
+    tokens = int(ctx.sum())
+    t_c, lk, ht = res["cached"]
+    t_u = res["uncached"][0]
+    line = {"metric": PREFIX_METRIC, "value": round(world * tokens / t_c, 1), "unit": "tokens/s",
+            "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(t_c * 1e3, 3), "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "bf16 KV / bf16 tensor-core MMA / f32 accumulate",
+            "data": "synthetic (seeded token ids and N(0,1) q/k/v)",
+            "config": {"workload": DESCRIPTION["prefix_cache_bf16"], "prompt_tokens": tokens,
+                       "requests": R, "timing": "host wall clock around whole steps "
+                       "(hashing, lookups, allocation, uploads, kernels, releases)"},
+            "uncached_tokens_per_s": round(world * tokens / t_u, 1),
+            "uncached_ms_per_step": round(t_u * 1e3, 3),
+            "speedup_vs_uncached": round(t_u / t_c, 3),
+            "block_hit_rate": round(ht / max(lk, 1), 4),
+            "gpu_launches": 2 * args.steps, "e2e": None, "cpu_baseline": None}
+    print(json.dumps(line), flush=True)
+
+
 def run_reference(args, rank, world):
     """The fp64 oracle on the host cores, a bounded sample of the workload per step."""
     if rank != 0:
@@ -728,7 +852,14 @@ def main():
         import torch.distributed as dist
         dist.init_process_group("nccl" if args.impl == "gb300" else "gloo")
     try:
-        if args.workload.endswith("_prefill"):
+        if args.workload == "prefix_cache_bf16":
+            if args.impl == "reference":
+                if rank == 0:
+                    print(json.dumps({"impl": "reference", "unavailable":
+                                      "the oracle leg covers the decode workloads only"}))
+            else:
+                run_prefix_cache(args, rank, world, local_rank)
+        elif args.workload.endswith("_prefill"):
             if args.impl == "reference":
                 if rank == 0:
                     print(json.dumps({"impl": "reference", "unavailable":

@@ -165,6 +165,42 @@ PA_API int pa_pool_stats(const pa_pool* pool, int* used, int* free_blocks, int* 
 PA_API int pa_cow_prepare(pa_pool* pool, int32_t* table_row, int ctx_len, int32_t* src, int32_t* dst,
                    int* n_pairs);
 
+/* ---- prefix caching ("Capítulo 8 ...", section 8.3: hash the prompt in
+ * block-size chunks; a request whose leading blocks are already cached points
+ * its block table at them and skips their prefill; new full blocks are
+ * registered after their prefill) ----
+ * A block's key is a chain hash: h_j = FNV-1a-64 over the 8 little-endian bytes
+ * of h_{j-1} followed by the 16 token ids of block j (4 little-endian bytes
+ * each), with h_{-1} = `parent` (0 for the start of a prompt).  Only full
+ * blocks are hashed and cached.  Two different prefixes with equal 64-bit
+ * hashes would share a block (not checked). */
+
+/* Chain hashes of the floor(n_tokens / 16) full blocks of tokens[0..n_tokens),
+ * written to hashes[]; *n_blocks receives their count.  Host only. */
+PA_API int pa_prefix_hash(const int32_t* tokens, int n_tokens, uint64_t parent, uint64_t* hashes,
+                          int* n_blocks);
+
+/* Looks up hashes[0..n) in order and stops at the first miss.  For each hit
+ * (the leading *n_hit of them) ids[i] receives the cached block, which gains a
+ * reference for the caller's table.  Entries hit become the most recently
+ * used. */
+PA_API int pa_prefix_lookup(pa_pool* pool, int n, const uint64_t* hashes, int32_t* ids, int* n_hit);
+
+/* Registers full blocks ids[i] (allocated, holding the K/V of the block whose
+ * chain hash is hashes[i]).  The cache takes one reference to each block it
+ * adds; hashes already cached are left as they are.  PA_ERR_INVALID (no change)
+ * if an id is not an allocated block. */
+PA_API int pa_prefix_register(pa_pool* pool, int n, const uint64_t* hashes, const int32_t* ids);
+
+/* Evicts up to max_blocks cached entries whose block no request references
+ * (refcount 1: only the cache), least recently used first; their blocks go back
+ * on the free list.  *n_evicted receives the count. */
+PA_API int pa_prefix_evict(pa_pool* pool, int max_blocks, int* n_evicted);
+
+/* Cached entries, and the blocks looked up / found since the pool was made;
+ * any output pointer may be NULL. */
+PA_API int pa_prefix_stats(const pa_pool* pool, int* entries, long long* lookups, long long* hits);
+
 /* ---- device operations ---- */
 
 /* For each pair p < n_pairs of pairs_dev (device int32 [n_pairs][2] =

@@ -104,6 +104,58 @@ class AllocatorModel:
         table_row[j] = new
         return (b, new)
 
+    # ------------------------------------------------------- prefix cache
+    # Prompt hashing in block-size chunks ("Capítulo 8 -- Gestión de caché KV de
+    # nueva generación", section 8.3): a request whose leading full blocks are
+    # cached points its table at them; blocks are registered after prefill.
+    # Reading taken: the cache owns one reference per mapped block; lookups stop
+    # at the first miss; eviction removes least-recently-used entries that no
+    # request references (ties by lower block id).
+    def _prefix_init(self):
+        if not hasattr(self, "prefix"):
+            self.prefix = {}      # hash -> [block, last_use]
+            self.tick = 0
+            self.lookups = 0
+            self.hits = 0
+
+    def prefix_lookup(self, hashes):
+        self._prefix_init()
+        self.tick += 1
+        self.lookups += len(hashes)
+        ids = []
+        for h in hashes:
+            e = self.prefix.get(int(h))
+            if e is None:
+                break
+            e[1] = self.tick
+            self.refcount[e[0]] += 1
+            ids.append(e[0])
+        self.hits += len(ids)
+        return ids
+
+    def prefix_register(self, hashes, ids):
+        self._prefix_init()
+        for b in ids:
+            if not (0 <= b < self.num_blocks) or self.refcount[b] == 0:
+                raise InvalidRequest(f"register of unallocated block {b}")
+        self.tick += 1
+        for h, b in zip(hashes, ids):
+            if int(h) in self.prefix:
+                continue
+            self.prefix[int(h)] = [b, self.tick]
+            self.refcount[b] += 1
+
+    def prefix_evict(self, max_blocks):
+        self._prefix_init()
+        cand = sorted((e[1], e[0], h) for h, e in self.prefix.items() if self.refcount[e[0]] == 1)
+        n = 0
+        for _, b, h in cand[:max_blocks]:
+            del self.prefix[h]
+            self.refcount[b] = 0
+            self.free_stack.append(b)
+            n += 1
+        return n
+
     # ----------------------------------------------------------------- views
     def stats(self):
         used = sum(1 for r in self.refcount if r > 0)
@@ -136,3 +188,26 @@ def blocks_for(tokens: int, block_size: int = 16) -> int:
 def internal_waste(reserved_tokens: int, used_tokens: int) -> float:
     """Fraction of a reservation left unused (internal fragmentation)."""
     return 1.0 - used_tokens / reserved_tokens
+
+
+def fnv1a64(data: bytes, h: int = 0xCBF29CE484222325) -> int:
+    """64-bit FNV-1a (Fowler, Noll, Vo): per byte, h ^= b; h *= 0x100000001B3."""
+    for b in data:
+        h ^= b
+        h = (h * 0x100000001B3) & 0xFFFFFFFFFFFFFFFF
+    return h
+
+
+def prefix_chain_hashes(tokens, parent: int = 0, block_size: int = 16):
+    """Chain hash of each full block: FNV-1a-64 of the previous block's hash
+    (8 little-endian bytes) followed by the block's token ids (4 little-endian
+    bytes each); the first block chains from `parent`."""
+    out = []
+    prev = parent
+    for j in range(len(tokens) // block_size):
+        data = prev.to_bytes(8, "little") + b"".join(
+            (int(t) & 0xFFFFFFFF).to_bytes(4, "little")
+            for t in tokens[j * block_size:(j + 1) * block_size])
+        prev = fnv1a64(data)
+        out.append(prev)
+    return out

@@ -71,6 +71,12 @@ _SIGS = [
     ("pa_pool_stats", [_P, ctypes.POINTER(_I), ctypes.POINTER(_I), ctypes.POINTER(_I)]),
     ("pa_cow_prepare", [_P, _P, _I, ctypes.POINTER(ctypes.c_int32),
                         ctypes.POINTER(ctypes.c_int32), ctypes.POINTER(_I)]),
+    ("pa_prefix_hash", [_P, _I, ctypes.c_uint64, _P, ctypes.POINTER(_I)]),
+    ("pa_prefix_lookup", [_P, _I, _P, _P, ctypes.POINTER(_I)]),
+    ("pa_prefix_register", [_P, _I, _P, _P]),
+    ("pa_prefix_evict", [_P, _I, ctypes.POINTER(_I)]),
+    ("pa_prefix_stats", [_P, ctypes.POINTER(_I), ctypes.POINTER(ctypes.c_longlong),
+                         ctypes.POINTER(ctypes.c_longlong)]),
     ("pa_copy_blocks", [_P, _I, _P, _I, _P]),
     ("pa_reshape_and_cache", [_P, _I, _P, _P, _P, _I, _P]),
     ("pa_decode_num_splits", [_P, _I, _I, _I, ctypes.POINTER(_I)]),
@@ -199,6 +205,46 @@ def pa_cow_prepare(pool: int, table_row: np.ndarray, ctx_len: int):
     _check(lib().pa_cow_prepare(pool, _arr_ptr(table_row), ctx_len, ctypes.byref(src),
                                 ctypes.byref(dst), ctypes.byref(n)))
     return (src.value, dst.value) if n.value else None
+
+
+def pa_prefix_hash(tokens, parent: int = 0) -> np.ndarray:
+    """Chain hashes (uint64) of the full 16-token blocks of `tokens`."""
+    tokens = np.ascontiguousarray(tokens, dtype=np.int32)
+    out = np.zeros(max(tokens.size // 16, 1), np.uint64)
+    n = _I()
+    _check(lib().pa_prefix_hash(_arr_ptr(tokens) if tokens.size else None, tokens.size,
+                                ctypes.c_uint64(parent), _arr_ptr(out), ctypes.byref(n)))
+    return out[:n.value]
+
+
+def pa_prefix_lookup(pool: int, hashes) -> np.ndarray:
+    """Block ids of the leading cached blocks (each gains a reference)."""
+    hashes = np.ascontiguousarray(hashes, dtype=np.uint64)
+    ids = np.zeros(max(hashes.size, 1), np.int32)
+    n = _I()
+    _check(lib().pa_prefix_lookup(pool, hashes.size, _arr_ptr(hashes), _arr_ptr(ids),
+                                  ctypes.byref(n)))
+    return ids[:n.value]
+
+
+def pa_prefix_register(pool: int, hashes, ids) -> None:
+    hashes = np.ascontiguousarray(hashes, dtype=np.uint64)
+    ids = np.ascontiguousarray(ids, dtype=np.int32)
+    assert hashes.size == ids.size
+    _check(lib().pa_prefix_register(pool, hashes.size, _arr_ptr(hashes) if hashes.size else None,
+                                    _arr_ptr(ids) if ids.size else None))
+
+
+def pa_prefix_evict(pool: int, max_blocks: int) -> int:
+    n = _I()
+    _check(lib().pa_prefix_evict(pool, max_blocks, ctypes.byref(n)))
+    return n.value
+
+
+def pa_prefix_stats(pool: int):
+    e, lk, h = _I(), ctypes.c_longlong(), ctypes.c_longlong()
+    _check(lib().pa_prefix_stats(pool, ctypes.byref(e), ctypes.byref(lk), ctypes.byref(h)))
+    return e.value, lk.value, h.value
 
 
 # ---------------------------------------------------------------- device calls

@@ -14,6 +14,7 @@
 #include <stdio.h>
 #include <string.h>
 
+#include <algorithm>
 #include <cmath>
 #include <new>
 #include <string>
@@ -248,6 +249,102 @@ int pa_cow_prepare(pa_pool* pool, int32_t* table_row, int ctx_len, int32_t* src,
   *src = old;
   *dst = fresh;
   *n_pairs = 1;
+  return PA_OK;
+}
+
+// ---- prefix caching: block-granular prompt hashing ("Capítulo 8 -- Gestión de
+// caché KV de nueva generación", section 8.3)
+
+static uint64_t fnv1a_bytes(uint64_t h, const unsigned char* p, size_t n) {
+  for (size_t i = 0; i < n; ++i) {
+    h ^= p[i];
+    h *= 1099511628211ull;  // FNV 64-bit prime
+  }
+  return h;
+}
+
+int pa_prefix_hash(const int32_t* tokens, int n_tokens, uint64_t parent, uint64_t* hashes,
+                   int* n_blocks) {
+  if (n_tokens < 0 || (n_tokens > 0 && !tokens) || !n_blocks)
+    return pa::fail(PA_ERR_INVALID, "pa_prefix_hash: bad argument");
+  const int nb = n_tokens / PA_BLOCK_SIZE;
+  if (nb > 0 && !hashes) return pa::fail(PA_ERR_INVALID, "pa_prefix_hash: null output");
+  uint64_t prev = parent;
+  for (int j = 0; j < nb; ++j) {
+    unsigned char buf[8 + 4 * PA_BLOCK_SIZE];
+    for (int b = 0; b < 8; ++b) buf[b] = (unsigned char)(prev >> (8 * b));
+    for (int i = 0; i < PA_BLOCK_SIZE; ++i) {
+      const uint32_t tkn = (uint32_t)tokens[j * PA_BLOCK_SIZE + i];
+      for (int b = 0; b < 4; ++b) buf[8 + 4 * i + b] = (unsigned char)(tkn >> (8 * b));
+    }
+    prev = fnv1a_bytes(14695981039346656037ull, buf, sizeof buf);  // FNV 64-bit offset basis
+    hashes[j] = prev;
+  }
+  *n_blocks = nb;
+  return PA_OK;
+}
+
+int pa_prefix_lookup(pa_pool* pool, int n, const uint64_t* hashes, int32_t* ids, int* n_hit) {
+  if (!pool || n < 0 || (n > 0 && (!hashes || !ids)) || !n_hit)
+    return pa::fail(PA_ERR_INVALID, "pa_prefix_lookup: bad argument");
+  int hit = 0;
+  pool->prefix_lookups += n;
+  const uint64_t tick = ++pool->prefix_tick;
+  for (; hit < n; ++hit) {
+    auto it = pool->prefix.find(hashes[hit]);
+    if (it == pool->prefix.end()) break;
+    it->second.last_use = tick;
+    ids[hit] = it->second.block;
+    ++pool->refcount[it->second.block];
+  }
+  pool->prefix_hits += hit;
+  *n_hit = hit;
+  return PA_OK;
+}
+
+int pa_prefix_register(pa_pool* pool, int n, const uint64_t* hashes, const int32_t* ids) {
+  if (!pool || n < 0 || (n > 0 && (!hashes || !ids)))
+    return pa::fail(PA_ERR_INVALID, "pa_prefix_register: bad argument");
+  for (int i = 0; i < n; ++i)
+    if (ids[i] < 0 || ids[i] >= pool->desc.num_blocks || pool->refcount[ids[i]] == 0)
+      return pa::fail(PA_ERR_INVALID, "register of block %d, which is not allocated", ids[i]);
+  const uint64_t tick = ++pool->prefix_tick;
+  for (int i = 0; i < n; ++i) {
+    if (pool->prefix.count(hashes[i])) continue;
+    pool->prefix[hashes[i]] = pa_pool::prefix_entry{ids[i], tick};
+    ++pool->refcount[ids[i]];
+  }
+  return PA_OK;
+}
+
+int pa_prefix_evict(pa_pool* pool, int max_blocks, int* n_evicted) {
+  if (!pool || max_blocks < 0 || !n_evicted)
+    return pa::fail(PA_ERR_INVALID, "pa_prefix_evict: bad argument");
+  // candidates: entries only the cache references, least recently used first
+  // (ties: lower block id first)
+  std::vector<std::pair<std::pair<uint64_t, int32_t>, uint64_t>> cand;
+  for (const auto& kv : pool->prefix)
+    if (pool->refcount[kv.second.block] == 1)
+      cand.push_back({{kv.second.last_use, kv.second.block}, kv.first});
+  std::sort(cand.begin(), cand.end());
+  int ev = 0;
+  for (const auto& c : cand) {
+    if (ev >= max_blocks) break;
+    const int32_t b = c.first.second;
+    pool->prefix.erase(c.second);
+    pool->refcount[b] = 0;
+    pool->free_stack.push_back(b);
+    ++ev;
+  }
+  *n_evicted = ev;
+  return PA_OK;
+}
+
+int pa_prefix_stats(const pa_pool* pool, int* entries, long long* lookups, long long* hits) {
+  if (!pool) return pa::fail(PA_ERR_INVALID, "null pool");
+  if (entries) *entries = (int)pool->prefix.size();
+  if (lookups) *lookups = pool->prefix_lookups;
+  if (hits) *hits = pool->prefix_hits;
   return PA_OK;
 }
 

@@ -5,6 +5,7 @@
 #include <stddef.h>
 #include <stdint.h>
 
+#include <unordered_map>
 #include <vector>
 
 #include "pa.h"  // include/ is on the include path
@@ -27,6 +28,16 @@ struct pa_pool {
   // encoded on first use by pa_decode.
   std::vector<pa_tmap_blob> tmaps;
   std::vector<char> tmap_ready;  // per layer
+  // Prefix cache: chain hash of a full block -> the block holding its K/V.
+  // The cache owns one reference to each block it maps.
+  struct prefix_entry {
+    int32_t block;
+    uint64_t last_use;  // tick of the last lookup or registration
+  };
+  std::unordered_map<uint64_t, prefix_entry> prefix;
+  uint64_t prefix_tick = 0;
+  long long prefix_lookups = 0;  // blocks asked for
+  long long prefix_hits = 0;     // blocks found
 };
 
 namespace pa {

@@ -85,6 +85,19 @@ class KVPool:
     def cow_prepare(self, table_row: np.ndarray, ctx_len: int):
         return N.pa_cow_prepare(self.handle, table_row, ctx_len)
 
+    # -------------------------------------------------------- prefix cache
+    def prefix_lookup(self, hashes) -> np.ndarray:
+        return N.pa_prefix_lookup(self.handle, hashes)
+
+    def prefix_register(self, hashes, ids) -> None:
+        N.pa_prefix_register(self.handle, hashes, ids)
+
+    def prefix_evict(self, max_blocks: int) -> int:
+        return N.pa_prefix_evict(self.handle, max_blocks)
+
+    def prefix_stats(self):
+        return N.pa_prefix_stats(self.handle)
+
     # --------------------------------------------------------------- views
     def layer_view(self, which: str, layer: int = 0) -> torch.Tensor:
         """uint8 view [num_blocks, n_kv_heads, 16, head_dim * elem_bytes] of one layer."""
