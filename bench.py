@@ -49,7 +49,9 @@ WORKLOADS = {
     "llama3_8b_fp8": ["llama3_8b_fp8"],
     "llama3_70b_fp8_prefill": ["llama3_70b_fp8_prefill"],
     "prefix_cache_bf16": ["prefix_cache_bf16"],
+    "kv_swap_fp8": ["kv_swap_fp8"],
 }
+SWAP_METRIC = "KV page swap to host memory: GB/s out + in (gather / scatter of blocks), 1 GPU"
 PREFIX_METRIC = ("prefill with block-hash prefix caching: prompt tokens served per second "
                  "(shared 2048-token system prompt), 1 GPU")
 PREFILL_METRIC = "chunked prefill attention over a paged FP8 KV cache: TFLOP/s, 1 GPU"
@@ -61,6 +63,9 @@ DESCRIPTION = {
     "llama3_70b_fp8_b": "Llama-3.1-70B-shaped FP8 decode, 256 x 4096 tokens",
     "llama3_8b_bf16": "Llama-3.1-8B-shaped bf16 decode, 64 seqs, ctx U[512,4096]",
     "llama3_8b_fp8": "Llama-3.1-8B-shaped FP8 decode, 64 seqs, ctx U[512,4096], 1% K outliers",
+    "kv_swap_fp8": "Llama-3.1-70B-shaped FP8 pool (Hkv 8, d 128, 16384 blocks of 32 KiB): each "
+                   "step swaps 8192 scattered blocks (256 MiB) out to pinned host memory and back "
+                   "into 8192 other blocks",
     "prefix_cache_bf16": "Llama-3.1-8B-shaped bf16 (Hq 32 / Hkv 8 / d 128): 64 requests whose "
                          "prompts share a 2048-token system prompt, each with its own U[128,1024] "
                          "suffix; a step hashes and looks up every prompt, writes and prefills "
@@ -786,6 +791,64 @@ def run_prefix_cache(args, rank, world, local_rank):
     print(json.dumps(line), flush=True)
 
 
+def run_swap(args, rank, world, local_rank):
+    """Block swap-out / swap-in bandwidth next to contiguous host copies."""
+    import torch
+
+    from paged_kv_cache_270_gb300.pool import KVPool
+    torch.cuda.set_device(local_rank)
+    nb, n = 16384, 8192
+    pool = KVPool(1, nb, 8, 128, "fp8_e4m3", 0.01, 0.01)
+    g = torch.Generator(device="cuda").manual_seed(3)
+    pool.k_cache.copy_(torch.randint(0, 256, (pool.k_cache.numel(),), dtype=torch.uint8,
+                                     device="cuda", generator=g))
+    pool.v_cache.copy_(torch.randint(0, 256, (pool.v_cache.numel(),), dtype=torch.uint8,
+                                     device="cuda", generator=g))
+    perm = np.random.default_rng(9).permutation(nb).astype(np.int32)
+    src = torch.from_numpy(perm[:n]).cuda()
+    dst = torch.from_numpy(perm[n:]).cuda()
+    per = pool.swap_block_bytes()
+    buf = torch.empty(n * per, dtype=torch.uint8).pin_memory()
+    dev = torch.empty(n * per, dtype=torch.uint8, device="cuda")
+    stream = torch.cuda.current_stream()
+    ev = lambda: torch.cuda.Event(enable_timing=True)  # noqa: E731
+
+    def timed(fn):
+        for _ in range(args.warmup):
+            fn()
+        torch.cuda.synchronize()
+        _barrier(world)
+        a_, b_ = ev(), ev()
+        a_.record(stream)
+        for _ in range(args.steps):
+            fn()
+        b_.record(stream)
+        torch.cuda.synchronize()
+        return _max_over_ranks(a_.elapsed_time(b_) / 1e3 / args.steps, world)
+
+    t_out = timed(lambda: pool.swap_out(src, buf))
+    t_in = timed(lambda: pool.swap_in(dst, buf))
+    t_d2h = timed(lambda: buf.copy_(dev, non_blocking=True))
+    t_h2d = timed(lambda: dev.copy_(buf, non_blocking=True))
+    if pool.device_error():
+        raise RuntimeError("device error in swap")
+    if rank != 0:
+        return
+    nbytes = n * per
+    gb = lambda t: round(nbytes / t / 1e9, 1)  # noqa: E731
+    line = {"metric": SWAP_METRIC, "value": round(world * 2 * nbytes / (t_out + t_in) / 1e9, 1),
+            "unit": "GB/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round((t_out + t_in) * 1e3, 3), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "u8",
+            "data": "synthetic (random bytes, random block ids)",
+            "config": {"workload": DESCRIPTION["kv_swap_fp8"], "bytes_each_way": nbytes},
+            "swap_out_gbs": gb(t_out), "swap_in_gbs": gb(t_in),
+            "contiguous_d2h_gbs": gb(t_d2h), "contiguous_h2d_gbs": gb(t_h2d),
+            "frac_of_contiguous": {"out": round(t_d2h / t_out, 3), "in": round(t_h2d / t_in, 3)},
+            "gpu_launches": 2 * args.steps, "e2e": None, "cpu_baseline": None}
+    print(json.dumps(line), flush=True)
+
+
 def run_reference(args, rank, world):
     """The fp64 oracle on the host cores, a bounded sample of the workload per step."""
     if rank != 0:
@@ -852,7 +915,14 @@ def main():
         import torch.distributed as dist
         dist.init_process_group("nccl" if args.impl == "gb300" else "gloo")
     try:
-        if args.workload == "prefix_cache_bf16":
+        if args.workload == "kv_swap_fp8":
+            if args.impl == "reference":
+                if rank == 0:
+                    print(json.dumps({"impl": "reference", "unavailable":
+                                      "the oracle leg covers the decode workloads only"}))
+            else:
+                run_swap(args, rank, world, local_rank)
+        elif args.workload == "prefix_cache_bf16":
             if args.impl == "reference":
                 if rank == 0:
                     print(json.dumps({"impl": "reference", "unavailable":

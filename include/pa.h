@@ -211,6 +211,32 @@ PA_API int pa_prefix_stats(const pa_pool* pool, int* entries, long long* lookups
  * source in the same call. */
 PA_API int pa_copy_blocks(pa_pool* pool, int layer, const int32_t* pairs_dev, int n_pairs, void* stream);
 
+/* ---- page swap to host memory ("KV Cache y PagedAttention", "Cómo
+ * PagedAttention soluciona esto": under memory pressure the system moves small
+ * pages to the CPU instead of whole sequences; "PagedAttention y Gestión de
+ * KV-Cache", KV-cache offloading to system RAM) ----
+ * A swapped block is the K and V of every kv head of every layer:
+ * pa_swap_block_bytes per block, laid out in the host buffer as
+ * [block][layer][K | V][n_kv_heads][block_size][head_dim] elements.  The host
+ * buffer must be page-locked and device-accessible (cudaHostAlloc /
+ * cudaMallocHost, or cudaHostRegister'ed memory); the GPU reads or writes it
+ * directly over the CPU-GPU link. */
+
+/* Bytes one block occupies in a swap buffer. */
+PA_API int pa_swap_block_bytes(const pa_pool* pool, size_t* bytes);
+
+/* Copies blocks ids_dev[0..n) (device int32) into host_buf, block i at offset
+ * i * pa_swap_block_bytes.  The blocks' refcounts are not touched: free them
+ * with pa_block_free once the copy is ordered before any reuse (work later on
+ * the same stream is).  Out-of-range ids are skipped and set PA_ERR_BOUNDS. */
+PA_API int pa_swap_out(pa_pool* pool, int n, const int32_t* ids_dev, void* host_buf, void* stream);
+
+/* Copies host_buf (as written by pa_swap_out) back into blocks ids_dev[0..n),
+ * e.g. freshly allocated ones whose ids then replace the old ones in the block
+ * table.  Out-of-range ids are skipped and set PA_ERR_BOUNDS. */
+PA_API int pa_swap_in(pa_pool* pool, int n, const int32_t* ids_dev, const void* host_buf,
+                      void* stream);
+
 /* Writes T new tokens into their slots of layer `layer` (scatter through the
  * slot mapping; pages are filled on demand, "Optimización de KV Cache ...",
  * section 3).

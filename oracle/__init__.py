@@ -76,6 +76,8 @@ def _load():
         lib.or_paged_prefill.argtypes = [i32, i32, i32, i32, i32, i32, P, P, f32, f32, P, i32, P,
                                           P, i32, P, i32, f64, P]
         lib.or_paged_prefill.restype = i32
+        lib.or_swap_gather.argtypes = [i32, i32, i32, i32, i32, P, i32, P, P, P]
+        lib.or_swap_gather.restype = i32
         lib.or_slab_attention.argtypes = [P, P, i32, i32, i32, P, i32, P, i32, f64, P]
         lib.or_slab_attention.restype = i32
         _lib = lib
@@ -227,3 +229,16 @@ def paged_prefill(kv_dtype: str, q_dtype: str, num_blocks: int, block_size: int,
     if st != 0:
         raise ValueError(f"oracle paged_prefill status {st}")
     return out
+
+
+def swap_gather(kv_dtype: str, num_blocks: int, block_size: int, n_kv_heads: int, head_dim: int,
+                ids: np.ndarray, k_pool: np.ndarray, v_pool: np.ndarray) -> np.ndarray:
+    """One layer's swap buffer of blocks `ids`: [n][K|V][Hkv][block_size][d] bytes."""
+    ids = np.ascontiguousarray(ids, dtype=np.int32)
+    blk = pool_bytes(kv_dtype, 1, block_size, n_kv_heads, head_dim)
+    buf = np.zeros(2 * blk * ids.size, np.uint8)
+    st = _load().or_swap_gather(dtype_code(kv_dtype), num_blocks, block_size, n_kv_heads, head_dim,
+                                _ptr(ids), ids.size, _ptr(k_pool), _ptr(v_pool), _ptr(buf))
+    if st != 0:
+        raise ValueError("oracle swap_gather: id out of range")
+    return buf

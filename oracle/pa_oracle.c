@@ -32,6 +32,9 @@
  *    "Optimización de KV Cache ...", sections 5 and 6.3).  Query j of a chunk
  *    that ends the sequence's ctx tokens sits at position ctx - C + j and sees
  *    tokens [0, ctx - C + j].
+ *  - Swap of whole blocks to host memory: the K and V tiles of every kv head
+ *    of a block, block after block ("KV Cache y PagedAttention", fine-grained
+ *    eviction of pages to the CPU).
  *  - Copy of whole blocks (K and V tiles of every kv head), the copy-on-write
  *    step of shared prefixes ("PagedAttention y Gestión de KV-Cache", section
  *    3.01; "KV Cache y PagedAttention", "Cómo PagedAttention soluciona esto").
@@ -416,5 +419,24 @@ int or_paged_prefill(int kv_dtype, int q_dtype, int num_blocks, int block_size, 
     free(V);
   }
   free(qv);
+  return status;
+}
+
+/* Swap buffer of one layer: for each listed block, its K tiles of every kv
+ * head, then its V tiles ([n][K|V][n_kv_heads][block_size][head_dim]).
+ * Returns -1 if an id is out of range (its slot in buf is left as is). */
+int or_swap_gather(int kv_dtype, int num_blocks, int block_size, int n_kv_heads, int head_dim,
+                   const int32_t* ids, int n, const uint8_t* k_pool, const uint8_t* v_pool,
+                   uint8_t* buf) {
+  long long blk = (long long)n_kv_heads * block_size * head_dim * elem_bytes(kv_dtype);
+  int status = 0;
+  for (int i = 0; i < n; ++i) {
+    if (ids[i] < 0 || ids[i] >= num_blocks) {
+      status = -1;
+      continue;
+    }
+    memcpy(buf + (2LL * i) * blk, k_pool + ids[i] * blk, (size_t)blk);
+    memcpy(buf + (2LL * i + 1) * blk, v_pool + ids[i] * blk, (size_t)blk);
+  }
   return status;
 }

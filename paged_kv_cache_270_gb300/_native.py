@@ -78,6 +78,9 @@ _SIGS = [
     ("pa_prefix_stats", [_P, ctypes.POINTER(_I), ctypes.POINTER(ctypes.c_longlong),
                          ctypes.POINTER(ctypes.c_longlong)]),
     ("pa_copy_blocks", [_P, _I, _P, _I, _P]),
+    ("pa_swap_block_bytes", [_P, ctypes.POINTER(_SZ)]),
+    ("pa_swap_out", [_P, _I, _P, _P, _P]),
+    ("pa_swap_in", [_P, _I, _P, _P, _P]),
     ("pa_reshape_and_cache", [_P, _I, _P, _P, _P, _I, _P]),
     ("pa_decode_num_splits", [_P, _I, _I, _I, ctypes.POINTER(_I)]),
     ("pa_decode_workspace_bytes", [_P, _I, _I, _I, _I, ctypes.POINTER(_SZ)]),
@@ -250,6 +253,20 @@ def pa_prefix_stats(pool: int):
 # ---------------------------------------------------------------- device calls
 def pa_copy_blocks(pool: int, layer: int, pairs_ptr: int, n_pairs: int, stream: int) -> None:
     _check(lib().pa_copy_blocks(pool, layer, pairs_ptr, n_pairs, stream))
+
+
+def pa_swap_block_bytes(pool: int) -> int:
+    n = _SZ()
+    _check(lib().pa_swap_block_bytes(pool, ctypes.byref(n)))
+    return n.value
+
+
+def pa_swap_out(pool: int, n: int, ids_ptr: int, host_ptr: int, stream: int) -> None:
+    _check(lib().pa_swap_out(pool, n, ids_ptr, host_ptr, stream))
+
+
+def pa_swap_in(pool: int, n: int, ids_ptr: int, host_ptr: int, stream: int) -> None:
+    _check(lib().pa_swap_in(pool, n, ids_ptr, host_ptr, stream))
 
 
 def pa_reshape_and_cache(pool: int, layer: int, k_ptr: int, v_ptr: int, slot_mapping_ptr: int,

@@ -123,9 +123,71 @@ __global__ void __launch_bounds__(256) copy_blocks_kernel(const int32_t* __restr
   }
 }
 
+// ---------------------------------------------------------------------------
+// swap: blockIdx.x = block i of the list, blockIdx.y = layer * 2 + (0: K, 1: V).
+// One region = the block's tiles of every kv head in one layer, contiguous in
+// the pool and in the host buffer.  `to_host` selects the direction.
+__global__ void __launch_bounds__(256) swap_kernel(const int32_t* __restrict__ ids, int num_blocks,
+                                                   uint4* kpool, uint4* vpool,
+                                                   long long layer_vecs, long long region_vecs,
+                                                   uint4* host, int to_host, unsigned int* err) {
+  const int i = blockIdx.x;
+  const int layer = blockIdx.y >> 1, which = blockIdx.y & 1;
+  const int b = ids[i];
+  if (b < 0 || b >= num_blocks) {
+    if (threadIdx.x == 0 && blockIdx.y == 0) record_error(err, PA_ERR_BOUNDS);
+    return;
+  }
+  uint4* pool = (which ? vpool : kpool) + layer * layer_vecs + (long long)b * region_vecs;
+  uint4* h = host + ((long long)i * gridDim.y + blockIdx.y) * region_vecs;
+  if (to_host) {
+    for (long long v = threadIdx.x; v < region_vecs; v += blockDim.x) h[v] = pool[v];
+  } else {
+    for (long long v = threadIdx.x; v < region_vecs; v += blockDim.x) pool[v] = h[v];
+  }
+}
+
 }  // namespace pa
 
 using namespace pa;
+
+static int swap_common(pa_pool* pool, int n, const int32_t* ids_dev, const void* host_buf,
+                       int to_host, void* stream) {
+  if (!pool) return fail(PA_ERR_INVALID, "null pool");
+  if (n < 0) return fail(PA_ERR_INVALID, "n must be >= 0");
+  if (n == 0) return PA_OK;
+  if (!ids_dev || !host_buf) return fail(PA_ERR_INVALID, "null argument");
+  if (n > 0x7FFFFFFF / 2 || pool->desc.n_layers * 2 > 65535)
+    return fail(PA_ERR_UNSUPPORTED, "too many blocks or layers for one swap call");
+  // Only page-locked host memory is accepted: on systems where the GPU can also
+  // reach pageable memory, a pageable buffer would otherwise be written directly.
+  cudaPointerAttributes attr;
+  cudaError_t e = cudaPointerGetAttributes(&attr, host_buf);
+  if (e != cudaSuccess || attr.type != cudaMemoryTypeHost) {
+    cudaGetLastError();
+    return fail(PA_ERR_INVALID, "swap buffer is not page-locked host memory");
+  }
+  void* dev_view = attr.devicePointer;
+  if (!dev_view) {
+    e = cudaHostGetDevicePointer(&dev_view, const_cast<void*>(host_buf), 0);
+    if (e != cudaSuccess || !dev_view) {
+      cudaGetLastError();
+      return fail(PA_ERR_INVALID, "swap buffer is not device-accessible");
+    }
+  }
+  if ((uintptr_t)dev_view & 15u) return fail(PA_ERR_INVALID, "swap buffer must be 16-byte aligned");
+  unsigned int* err = device_error_word();
+  if (!err) return PA_ERR_CUDA;
+  const long long region_vecs = (long long)pool->desc.n_kv_heads * pool->tile_bytes / 16;
+  const long long layer_vecs = (long long)pool->layer_bytes / 16;
+  swap_kernel<<<dim3(n, pool->desc.n_layers * 2), 256, 0, static_cast<cudaStream_t>(stream)>>>(
+      ids_dev, pool->desc.num_blocks, reinterpret_cast<uint4*>(pool->k),
+      reinterpret_cast<uint4*>(pool->v), layer_vecs, region_vecs, static_cast<uint4*>(dev_view),
+      to_host, err);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return fail(PA_ERR_CUDA, "swap launch: %s", cudaGetErrorString(e));
+  return PA_OK;
+}
 
 extern "C" {
 
@@ -182,6 +244,20 @@ int pa_copy_blocks(pa_pool* pool, int layer, const int32_t* pairs_dev, int n_pai
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return fail(PA_ERR_CUDA, "copy_blocks launch: %s", cudaGetErrorString(e));
   return PA_OK;
+}
+
+int pa_swap_block_bytes(const pa_pool* pool, size_t* bytes) {
+  if (!pool || !bytes) return fail(PA_ERR_INVALID, "null argument");
+  *bytes = 2ull * pool->desc.n_layers * pool->desc.n_kv_heads * pool->tile_bytes;
+  return PA_OK;
+}
+
+int pa_swap_out(pa_pool* pool, int n, const int32_t* ids_dev, void* host_buf, void* stream) {
+  return swap_common(pool, n, ids_dev, host_buf, 1, stream);
+}
+
+int pa_swap_in(pa_pool* pool, int n, const int32_t* ids_dev, const void* host_buf, void* stream) {
+  return swap_common(pool, n, ids_dev, host_buf, 0, stream);
 }
 
 int pa_get_device_error(pa_pool* pool, int* code, void* stream) {

@@ -123,6 +123,29 @@ class KVPool:
         N.pa_copy_blocks(self.handle, layer, pairs.data_ptr(), pairs.numel() // 2,
                          _stream_handle(stream))
 
+    def swap_block_bytes(self) -> int:
+        return N.pa_swap_block_bytes(self.handle)
+
+    def swap_out(self, ids: torch.Tensor, host_buf: torch.Tensor, stream=None) -> None:
+        """Copy blocks `ids` (device int32) into pinned host memory `host_buf`."""
+        _need(ids, "ids", torch.int32, self.device)
+        if not host_buf.is_pinned():
+            raise ValueError("host_buf must be pinned host memory")
+        if host_buf.numel() * host_buf.element_size() < ids.numel() * self.swap_block_bytes():
+            raise ValueError("host_buf too small")
+        N.pa_swap_out(self.handle, ids.numel(), ids.data_ptr(), host_buf.data_ptr(),
+                      _stream_handle(stream))
+
+    def swap_in(self, ids: torch.Tensor, host_buf: torch.Tensor, stream=None) -> None:
+        """Copy a swap buffer back into blocks `ids` (device int32)."""
+        _need(ids, "ids", torch.int32, self.device)
+        if not host_buf.is_pinned():
+            raise ValueError("host_buf must be pinned host memory")
+        if host_buf.numel() * host_buf.element_size() < ids.numel() * self.swap_block_bytes():
+            raise ValueError("host_buf too small")
+        N.pa_swap_in(self.handle, ids.numel(), ids.data_ptr(), host_buf.data_ptr(),
+                     _stream_handle(stream))
+
     def num_splits(self, S: int, n_q_heads: int, max_blocks_per_seq: int) -> int:
         return N.pa_decode_num_splits(self.handle, S, n_q_heads, max_blocks_per_seq)
 
