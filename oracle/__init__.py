@@ -25,8 +25,9 @@ _BUILD = os.path.join(_HERE, "_build")
 _LIB_PATH = os.path.join(_BUILD, "libpa_oracle.so")
 
 # The oracle's own dtype codes (see pa_oracle.c).
-F16, BF16, E4M3 = 0, 1, 2
-_DTYPE_CODES = {"fp16": F16, "bf16": BF16, "fp8_e4m3": E4M3}
+F16, BF16, E4M3, E4M3_BLK = 0, 1, 2, 3
+_DTYPE_CODES = {"fp16": F16, "bf16": BF16, "fp8_e4m3": E4M3, "fp8_e4m3_block": E4M3_BLK}
+FP8_DTYPES = ("fp8_e4m3", "fp8_e4m3_block")
 
 _lock = threading.Lock()
 _lib = None
@@ -78,6 +79,8 @@ def _load():
         lib.or_paged_prefill.restype = i32
         lib.or_swap_gather.argtypes = [i32, i32, i32, i32, i32, P, i32, P, P, P]
         lib.or_swap_gather.restype = i32
+        lib.or_swap_record_bytes.argtypes = [i32, i32, i32, i32]
+        lib.or_swap_record_bytes.restype = ctypes.c_longlong
         lib.or_slab_attention.argtypes = [P, P, i32, i32, i32, P, i32, P, i32, f64, P]
         lib.or_slab_attention.restype = i32
         _lib = lib
@@ -136,10 +139,30 @@ def e4m3_table() -> np.ndarray:
 
 
 # ---------------------------------------------------------------------- pools
+def tiles_bytes(kv_dtype: str, num_blocks: int, block_size: int, n_kv_heads: int,
+                head_dim: int) -> int:
+    """Bytes of the code tiles of one K or V region."""
+    b = 1 if kv_dtype in FP8_DTYPES else 2
+    return num_blocks * n_kv_heads * block_size * head_dim * b
+
+
 def pool_bytes(kv_dtype: str, num_blocks: int, block_size: int, n_kv_heads: int,
                head_dim: int) -> int:
-    b = 1 if kv_dtype == "fp8_e4m3" else 2
-    return num_blocks * n_kv_heads * block_size * head_dim * b
+    """Bytes of one K or V region: the tiles, then (block-scaled FP8) the fp32
+    scale table [num_blocks][n_kv_heads]."""
+    n = tiles_bytes(kv_dtype, num_blocks, block_size, n_kv_heads, head_dim)
+    if kv_dtype == "fp8_e4m3_block":
+        n += 4 * num_blocks * n_kv_heads
+    return n
+
+
+def tile_scales(kv_dtype: str, num_blocks: int, block_size: int, n_kv_heads: int, head_dim: int,
+                region: np.ndarray) -> np.ndarray:
+    """The scale table of a block-scaled region, as float32 [num_blocks][n_kv_heads]."""
+    assert kv_dtype == "fp8_e4m3_block"
+    off = tiles_bytes(kv_dtype, num_blocks, block_size, n_kv_heads, head_dim)
+    return region[off:off + 4 * num_blocks * n_kv_heads].view(np.float32).reshape(
+        num_blocks, n_kv_heads)
 
 
 def reshape_and_cache(kv_dtype: str, num_blocks: int, block_size: int, n_kv_heads: int,
@@ -233,10 +256,11 @@ def paged_prefill(kv_dtype: str, q_dtype: str, num_blocks: int, block_size: int,
 
 def swap_gather(kv_dtype: str, num_blocks: int, block_size: int, n_kv_heads: int, head_dim: int,
                 ids: np.ndarray, k_pool: np.ndarray, v_pool: np.ndarray) -> np.ndarray:
-    """One layer's swap buffer of blocks `ids`: [n][K|V][Hkv][block_size][d] bytes."""
+    """One layer's swap buffer of blocks `ids`: per block its K tiles, its V tiles
+    and, for block-scaled pools, its K and V scales padded to 16 bytes."""
     ids = np.ascontiguousarray(ids, dtype=np.int32)
-    blk = pool_bytes(kv_dtype, 1, block_size, n_kv_heads, head_dim)
-    buf = np.zeros(2 * blk * ids.size, np.uint8)
+    rec = _load().or_swap_record_bytes(dtype_code(kv_dtype), block_size, n_kv_heads, head_dim)
+    buf = np.zeros(rec * ids.size, np.uint8)
     st = _load().or_swap_gather(dtype_code(kv_dtype), num_blocks, block_size, n_kv_heads, head_dim,
                                 _ptr(ids), ids.size, _ptr(k_pool), _ptr(v_pool), _ptr(buf))
     if st != 0:

@@ -32,6 +32,19 @@
  *    "Optimización de KV Cache ...", sections 5 and 6.3).  Query j of a chunk
  *    that ends the sequence's ctx tokens sits at position ctx - C + j and sees
  *    tokens [0, ctx - C + j].
+ *  - Dynamic per-block FP8 scaling (same page, section 8, dynamic scaling:
+ *    the MaxAbs of each block is taken at inference time and the scale is
+ *    applied on the fly).  Each (block, kv head) tile of K, and of V, has its
+ *    own fp32 scale s = fl32(MaxAbs / 448), 448 being the largest E4M3 value;
+ *    s = 0 marks a tile whose values are all zero (its codes are then 0).
+ *    The page does not say how a block that fills token by token keeps its
+ *    MaxAbs; the reading taken here: the tokens one call writes into a block
+ *    form one run of consecutive slots; a run that starts at offset 0 starts
+ *    the tile afresh; a later run that raises the tile's MaxAbs re-encodes the
+ *    tile's earlier rows with the new scale, from their dequantised fp32
+ *    values (the 16-bit originals are no longer held).  Pool regions of this
+ *    type are the code tiles followed by the scale table
+ *    [num_blocks][n_kv_heads] of fp32.
  *  - Swap of whole blocks to host memory: the K and V tiles of every kv head
  *    of a block, block after block ("KV Cache y PagedAttention", fine-grained
  *    eviction of pages to the CPU).
@@ -40,7 +53,8 @@
  *    3.01; "KV Cache y PagedAttention", "Cómo PagedAttention soluciona esto").
  *
  * Dtype codes used by this file (its own, passed in by its Python wrapper):
- *   0 = IEEE binary16, 1 = bfloat16, 2 = FP8 E4M3FN.
+ *   0 = IEEE binary16, 1 = bfloat16, 2 = FP8 E4M3FN with per-tensor scales,
+ *   3 = FP8 E4M3FN with a dynamic scale per (block, kv head) tile.
  */
 #include <math.h>
 #include <stdint.h>
@@ -50,6 +64,7 @@
 #define OR_F16 0
 #define OR_BF16 1
 #define OR_E4M3 2
+#define OR_E4M3_BLK 3
 
 /* ---------------------------------------------------------------------------
  * Number formats, decoded from their bit-level definitions.
@@ -149,7 +164,25 @@ long long or_kv_bytes_per_token(int n_layers, int n_kv_heads, int d_head, int pr
 }
 
 /* Bytes of one element of the pool for a cache dtype. */
-static int elem_bytes(int kv_dtype) { return kv_dtype == OR_E4M3 ? 1 : 2; }
+static int elem_bytes(int kv_dtype) { return (kv_dtype == OR_E4M3 || kv_dtype == OR_E4M3_BLK) ? 1 : 2; }
+
+/* Bytes of the code tiles of one K or V region: [num_blocks][n_kv_heads]
+ * [block_size][head_dim] elements.  A block-scaled region continues with its
+ * scale table right after them. */
+static long long tiles_bytes(int kv_dtype, int num_blocks, int n_kv_heads, int block_size,
+                             int head_dim) {
+  return (long long)num_blocks * n_kv_heads * block_size * head_dim * elem_bytes(kv_dtype);
+}
+
+/* Scale of tile (block, h) of a block-scaled region, and its update. */
+static float tile_scale_get(const uint8_t* pool, long long tiles, int n_kv_heads, int block, int h) {
+  float s;
+  memcpy(&s, pool + tiles + 4 * ((long long)block * n_kv_heads + h), 4);
+  return s;
+}
+static void tile_scale_set(uint8_t* pool, long long tiles, int n_kv_heads, int block, int h, float s) {
+  memcpy(pool + tiles + 4 * ((long long)block * n_kv_heads + h), &s, 4);
+}
 
 /* Element index of (block, kv head, offset within block, dim) in one layer's
  * K or V pool of layout [num_blocks][n_kv_heads][block_size][head_dim]. */
@@ -160,10 +193,92 @@ static long long pool_index(int block, int h, int off, int i, int n_kv_heads, in
 
 /* Value of pool element idx (already dequantised for FP8). */
 static double pool_value(int kv_dtype, const uint8_t* pool, long long idx, float scale) {
-  if (kv_dtype == OR_E4M3) return or_e4m3_value(pool[idx]) * (double)scale;
+  if (kv_dtype == OR_E4M3 || kv_dtype == OR_E4M3_BLK) return or_e4m3_value(pool[idx]) * (double)scale;
   uint16_t bits;
   memcpy(&bits, pool + 2 * idx, 2);
   return or_value16(kv_dtype, bits);
+}
+
+/* ---------------------------------------------------------------------------
+ * Dynamic per-block scaling of one run of n tokens (rows off0 .. off0+n-1 of
+ * tile (block, h)) of one tensor, K or V.  x: the run's values, row r at
+ * x[r * ld .. r * ld + head_dim).  The tile's scale follows its MaxAbs:
+ *   m     = max |x| over the run (exact: 16-bit values)
+ *   s_run = fl32(m / 448)
+ *   off0 == 0 : s = s_run (the tile starts afresh)
+ *   off0 >  0 : s = max(s_old, s_run); if s > s_old, each earlier code c of
+ *               rows 0 .. off0-1 becomes E4M3(fl32(fl32(value(c) * s_old) / s))
+ * then each new value is stored as E4M3(fl32(x / s)) (code 0 when s = 0). */
+static void write_run_block_scaled(const double* x, long long ld, int n, int off0, int block, int h,
+                                   int n_kv_heads, int block_size, int head_dim, long long tiles,
+                                   uint8_t* pool) {
+  double m = 0.0;
+  for (int r = 0; r < n; ++r)
+    for (int i = 0; i < head_dim; ++i)
+      if (fabs(x[r * ld + i]) > m) m = fabs(x[r * ld + i]);
+  float s = (float)(m / 448.0);
+  if (off0 > 0) {
+    float s_old = tile_scale_get(pool, tiles, n_kv_heads, block, h);
+    if (s > s_old) {
+      for (int r = 0; r < off0; ++r)
+        for (int i = 0; i < head_dim; ++i) {
+          long long idx = pool_index(block, h, r, i, n_kv_heads, block_size, head_dim);
+          float y_old = (float)(or_e4m3_value(pool[idx]) * (double)s_old);
+          pool[idx] = or_quantize_e4m3((double)y_old, s);
+        }
+    } else {
+      s = s_old;
+    }
+  }
+  for (int r = 0; r < n; ++r)
+    for (int i = 0; i < head_dim; ++i) {
+      long long idx = pool_index(block, h, off0 + r, i, n_kv_heads, block_size, head_dim);
+      pool[idx] = s > 0.f ? or_quantize_e4m3(x[r * ld + i], s) : 0x00;
+    }
+  tile_scale_set(pool, tiles, n_kv_heads, block, h, s);
+}
+
+/* reshape_and_cache of a block-scaled FP8 pool: tokens are taken in runs --
+ * a token, then the tokens right after it in slot_mapping whose slots follow
+ * it within the same block -- and each run updates its tiles as above.  (The
+ * tokens one call writes into a block are expected to form a single run.) */
+static int reshape_block_scaled(int num_blocks, int block_size, int n_kv_heads, int head_dim,
+                                const uint16_t* k_in, const uint16_t* v_in,
+                                const int64_t* slot_mapping, int T, uint8_t* k_pool,
+                                uint8_t* v_pool) {
+  int status = 0;
+  long long tiles = tiles_bytes(OR_E4M3_BLK, num_blocks, n_kv_heads, block_size, head_dim);
+  long long row = (long long)n_kv_heads * head_dim;
+  double* xk = (double*)malloc(sizeof(double) * (size_t)(block_size * head_dim));
+  double* xv = (double*)malloc(sizeof(double) * (size_t)(block_size * head_dim));
+  int t = 0;
+  while (t < T) {
+    int64_t slot = slot_mapping[t];
+    if (slot < 0 || slot >= (int64_t)num_blocks * block_size) {
+      if (slot >= 0) status = -1;
+      ++t;
+      continue;
+    }
+    int block = (int)(slot / block_size), off0 = (int)(slot % block_size);
+    int n = 1;
+    while (t + n < T && off0 + n < block_size && slot_mapping[t + n] == slot + n) ++n;
+    for (int h = 0; h < n_kv_heads; ++h) {
+      for (int r = 0; r < n; ++r)
+        for (int i = 0; i < head_dim; ++i) {
+          long long src = (t + r) * row + (long long)h * head_dim + i;
+          xk[r * head_dim + i] = or_bf16_value(k_in[src]);
+          xv[r * head_dim + i] = or_bf16_value(v_in[src]);
+        }
+      write_run_block_scaled(xk, head_dim, n, off0, block, h, n_kv_heads, block_size, head_dim,
+                             tiles, k_pool);
+      write_run_block_scaled(xv, head_dim, n, off0, block, h, n_kv_heads, block_size, head_dim,
+                             tiles, v_pool);
+    }
+    t += n;
+  }
+  free(xk);
+  free(xv);
+  return status;
 }
 
 /* ---------------------------------------------------------------------------
@@ -177,6 +292,9 @@ int or_reshape_and_cache(int kv_dtype, int num_blocks, int block_size, int n_kv_
                          int head_dim, const uint16_t* k_in, const uint16_t* v_in,
                          const int64_t* slot_mapping, int T, float k_scale, float v_scale,
                          uint8_t* k_pool, uint8_t* v_pool) {
+  if (kv_dtype == OR_E4M3_BLK)
+    return reshape_block_scaled(num_blocks, block_size, n_kv_heads, head_dim, k_in, v_in,
+                                slot_mapping, T, k_pool, v_pool);
   int status = 0;
   int in_dtype = (kv_dtype == OR_F16) ? OR_F16 : OR_BF16;
   for (int t = 0; t < T; ++t) {
@@ -219,6 +337,13 @@ int or_copy_blocks(int kv_dtype, int num_blocks, int block_size, int n_kv_heads,
     }
     memmove(k_pool + dst * blk, k_pool + src * blk, (size_t)blk);
     memmove(v_pool + dst * blk, v_pool + src * blk, (size_t)blk);
+    if (kv_dtype == OR_E4M3_BLK) { /* a block's scales travel with its codes */
+      long long tiles = tiles_bytes(kv_dtype, num_blocks, n_kv_heads, block_size, head_dim);
+      for (int h = 0; h < n_kv_heads; ++h) {
+        tile_scale_set(k_pool, tiles, n_kv_heads, dst, h, tile_scale_get(k_pool, tiles, n_kv_heads, src, h));
+        tile_scale_set(v_pool, tiles, n_kv_heads, dst, h, tile_scale_get(v_pool, tiles, n_kv_heads, src, h));
+      }
+    }
   }
   return status;
 }
@@ -298,16 +423,22 @@ int or_paged_attention(int kv_dtype, int q_dtype, int num_blocks, int block_size
     /* Step 1: gather the sequence's pages, in logical order, into contiguous
      * K[n][n_kv_heads][head_dim] and V[...] (dequantising FP8 codes). */
     long long row = (long long)n_kv_heads * head_dim;
+    long long tiles = tiles_bytes(kv_dtype, num_blocks, n_kv_heads, block_size, head_dim);
     double* K = (double*)malloc(sizeof(double) * (size_t)(n > 0 ? n * row : 1));
     double* V = (double*)malloc(sizeof(double) * (size_t)(n > 0 ? n * row : 1));
     for (int tok = 0; tok < n; ++tok) {
       int j = tok / block_size, off = tok % block_size;
       int b = block_tables[(long long)s * max_blocks_per_seq + j];
       for (int h = 0; h < n_kv_heads; ++h) {
+        float ks = k_scale, vs = v_scale;
+        if (kv_dtype == OR_E4M3_BLK) { /* the tile's own scales */
+          ks = tile_scale_get(k_pool, tiles, n_kv_heads, b, h);
+          vs = tile_scale_get(v_pool, tiles, n_kv_heads, b, h);
+        }
         for (int i = 0; i < head_dim; ++i) {
           long long idx = pool_index(b, h, off, i, n_kv_heads, block_size, head_dim);
-          K[tok * row + h * head_dim + i] = pool_value(kv_dtype, k_pool, idx, k_scale);
-          V[tok * row + h * head_dim + i] = pool_value(kv_dtype, v_pool, idx, v_scale);
+          K[tok * row + h * head_dim + i] = pool_value(kv_dtype, k_pool, idx, ks);
+          V[tok * row + h * head_dim + i] = pool_value(kv_dtype, v_pool, idx, vs);
         }
       }
     }
@@ -390,16 +521,22 @@ int or_paged_prefill(int kv_dtype, int q_dtype, int num_blocks, int block_size, 
     }
     /* gather the sequence's pages in logical order (as for decode) */
     long long row = (long long)n_kv_heads * head_dim;
+    long long tiles = tiles_bytes(kv_dtype, num_blocks, n_kv_heads, block_size, head_dim);
     double* K = (double*)malloc(sizeof(double) * (size_t)(n > 0 ? n * row : 1));
     double* V = (double*)malloc(sizeof(double) * (size_t)(n > 0 ? n * row : 1));
     for (int tok = 0; tok < n; ++tok) {
       int j = tok / block_size, off = tok % block_size;
       int b = block_tables[(long long)s * max_blocks_per_seq + j];
       for (int h = 0; h < n_kv_heads; ++h) {
+        float ks = k_scale, vs = v_scale;
+        if (kv_dtype == OR_E4M3_BLK) { /* the tile's own scales */
+          ks = tile_scale_get(k_pool, tiles, n_kv_heads, b, h);
+          vs = tile_scale_get(v_pool, tiles, n_kv_heads, b, h);
+        }
         for (int i = 0; i < head_dim; ++i) {
           long long idx = pool_index(b, h, off, i, n_kv_heads, block_size, head_dim);
-          K[tok * row + h * head_dim + i] = pool_value(kv_dtype, k_pool, idx, k_scale);
-          V[tok * row + h * head_dim + i] = pool_value(kv_dtype, v_pool, idx, v_scale);
+          K[tok * row + h * head_dim + i] = pool_value(kv_dtype, k_pool, idx, ks);
+          V[tok * row + h * head_dim + i] = pool_value(kv_dtype, v_pool, idx, vs);
         }
       }
     }
@@ -422,21 +559,40 @@ int or_paged_prefill(int kv_dtype, int q_dtype, int num_blocks, int block_size, 
   return status;
 }
 
-/* Swap buffer of one layer: for each listed block, its K tiles of every kv
- * head, then its V tiles ([n][K|V][n_kv_heads][block_size][head_dim]).
- * Returns -1 if an id is out of range (its slot in buf is left as is). */
+/* Bytes of one block's record in a one-layer swap buffer: its K tiles of every
+ * kv head, then its V tiles; a block-scaled pool adds the block's K scales and
+ * V scales (n_kv_heads fp32 each) and zero bytes up to a multiple of 16. */
+long long or_swap_record_bytes(int kv_dtype, int block_size, int n_kv_heads, int head_dim) {
+  long long codes = 2LL * n_kv_heads * block_size * head_dim * elem_bytes(kv_dtype);
+  if (kv_dtype != OR_E4M3_BLK) return codes;
+  long long scales = 2LL * n_kv_heads * 4;
+  return codes + (scales + 15) / 16 * 16;
+}
+
+/* Swap buffer of one layer: one record per listed block (above), records
+ * back to back.  Returns -1 if an id is out of range (its record in buf is
+ * left as is). */
 int or_swap_gather(int kv_dtype, int num_blocks, int block_size, int n_kv_heads, int head_dim,
                    const int32_t* ids, int n, const uint8_t* k_pool, const uint8_t* v_pool,
                    uint8_t* buf) {
   long long blk = (long long)n_kv_heads * block_size * head_dim * elem_bytes(kv_dtype);
+  long long rec = or_swap_record_bytes(kv_dtype, block_size, n_kv_heads, head_dim);
+  long long tiles = tiles_bytes(kv_dtype, num_blocks, n_kv_heads, block_size, head_dim);
   int status = 0;
   for (int i = 0; i < n; ++i) {
     if (ids[i] < 0 || ids[i] >= num_blocks) {
       status = -1;
       continue;
     }
-    memcpy(buf + (2LL * i) * blk, k_pool + ids[i] * blk, (size_t)blk);
-    memcpy(buf + (2LL * i + 1) * blk, v_pool + ids[i] * blk, (size_t)blk);
+    uint8_t* r = buf + i * rec;
+    memcpy(r, k_pool + ids[i] * blk, (size_t)blk);
+    memcpy(r + blk, v_pool + ids[i] * blk, (size_t)blk);
+    if (kv_dtype == OR_E4M3_BLK) {
+      memset(r + 2 * blk, 0, (size_t)(rec - 2 * blk));
+      memcpy(r + 2 * blk, k_pool + tiles + 4LL * ids[i] * n_kv_heads, 4 * (size_t)n_kv_heads);
+      memcpy(r + 2 * blk + 4LL * n_kv_heads, v_pool + tiles + 4LL * ids[i] * n_kv_heads,
+             4 * (size_t)n_kv_heads);
+    }
   }
   return status;
 }

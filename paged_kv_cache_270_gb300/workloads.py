@@ -69,7 +69,7 @@ def bits_to_f32(bits: np.ndarray, dtype: str) -> np.ndarray:
 class Workload:
     name: str
     index: int                 # workload index; seed = 1000 + index
-    kv_dtype: str              # "fp16" | "bf16" | "fp8_e4m3"
+    kv_dtype: str              # "fp16" | "bf16" | "fp8_e4m3" | "fp8_e4m3_block"
     n_q_heads: int
     n_kv_heads: int
     head_dim: int
@@ -102,7 +102,12 @@ class Workload:
 
     @property
     def elem_bytes(self) -> int:
-        return 1 if self.kv_dtype == "fp8_e4m3" else 2
+        return 1 if self.kv_dtype in ("fp8_e4m3", "fp8_e4m3_block") else 2
+
+    @property
+    def block_scaled(self) -> bool:
+        """FP8 with a dynamic scale per (block, kv head) tile, for K and for V."""
+        return self.kv_dtype == "fp8_e4m3_block"
 
     @property
     def max_blocks(self) -> int:
@@ -190,10 +195,13 @@ class Workload:
         return blk * self.block_size + pos % self.block_size
 
     def kv_bytes(self, ctx=None) -> int:
-        """Algorithmic K+V bytes one decode pass reads."""
-        ctx = self.ctx_lens if ctx is None else ctx
-        return int(np.sum(ctx, dtype=np.int64)) * 2 * self.n_kv_heads * self.head_dim * \
-            self.elem_bytes
+        """Algorithmic K+V bytes one decode pass reads (block-scaled pools add the
+        two fp32 scales of every (page, kv head) tile read)."""
+        ctx = np.asarray(self.ctx_lens if ctx is None else ctx, dtype=np.int64)
+        n = int(np.sum(ctx)) * 2 * self.n_kv_heads * self.head_dim * self.elem_bytes
+        if self.block_scaled:
+            n += int(np.sum(-(-ctx // self.block_size))) * self.n_kv_heads * 8
+        return n
 
 
 def _tables_from_permutation(rng, ctx, num_blocks, max_blocks):
@@ -233,6 +241,11 @@ def make(name: str, scale_down: int = 1, steps: int | None = None) -> Workload:
     """Build a named workload.  ``scale_down`` > 1 shrinks sequence counts and
     lengths (for quick parity runs) while keeping head shapes and dtypes."""
     sd = max(1, int(scale_down))
+    if "_fp8_block" in name:
+        # the FP8 workload of the same shapes and values, with dynamic per-block scales
+        w = make(name.replace("_fp8_block", "_fp8"), scale_down, steps)
+        w.name, w.kv_dtype, w.k_scale, w.v_scale = name, "fp8_e4m3_block", 1.0, 1.0
+        return w
     if name == "tiny_fp16":
         return _paged(0, name, "fp16", 4, 2, 64, [17, 33, 64, 100], num_blocks=32)
     if name == "llama3_8b_bf16":
