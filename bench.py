@@ -45,6 +45,9 @@ WORKLOADS = {
     "llama3_70b_fp8": ["llama3_70b_fp8_a", "llama3_70b_fp8_b"],
     "llama3_70b_fp8_a": ["llama3_70b_fp8_a"],
     "llama3_70b_fp8_b": ["llama3_70b_fp8_b"],
+    "llama3_70b_fp8_block": ["llama3_70b_fp8_block_a", "llama3_70b_fp8_block_b"],
+    "llama3_70b_fp8_block_a": ["llama3_70b_fp8_block_a"],
+    "llama3_70b_fp8_block_b": ["llama3_70b_fp8_block_b"],
     "llama3_8b_bf16": ["llama3_8b_bf16"],
     "llama3_8b_fp8": ["llama3_8b_fp8"],
     "llama3_70b_fp8_prefill": ["llama3_70b_fp8_prefill"],
@@ -61,6 +64,12 @@ DESCRIPTION = {
                       "tables; batch A 4 x 131072 tokens + batch B 256 x 4096 tokens",
     "llama3_70b_fp8_a": "Llama-3.1-70B-shaped FP8 decode, 4 x 131072 tokens",
     "llama3_70b_fp8_b": "Llama-3.1-70B-shaped FP8 decode, 256 x 4096 tokens",
+    "llama3_70b_fp8_block": "Llama-3.1-70B-shaped single-layer decode, FP8 E4M3 paged KV with a "
+                            "dynamic scale per (block, kv head) tile (MaxAbs/448 taken as tokens "
+                            "are written), Hq 64 / Hkv 8 / d 128, 16-token blocks, random block "
+                            "tables; batch A 4 x 131072 tokens + batch B 256 x 4096 tokens",
+    "llama3_70b_fp8_block_a": "Llama-3.1-70B-shaped block-scaled FP8 decode, 4 x 131072 tokens",
+    "llama3_70b_fp8_block_b": "Llama-3.1-70B-shaped block-scaled FP8 decode, 256 x 4096 tokens",
     "llama3_8b_bf16": "Llama-3.1-8B-shaped bf16 decode, 64 seqs, ctx U[512,4096]",
     "llama3_8b_fp8": "Llama-3.1-8B-shaped FP8 decode, 64 seqs, ctx U[512,4096], 1% K outliers",
     "kv_swap_fp8": "Llama-3.1-70B-shaped FP8 pool (Hkv 8, d 128, 16384 blocks of 32 KiB): each "
@@ -503,8 +512,9 @@ def run_gb300(args, rank, world, local_rank):
         "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world, "steps": K,
         "warmup": args.warmup, "ms_per_step": round(t_max / K * 1e3, 4),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-        "dtype": "e4m3 KV / f16 tensor-core MMA / f32 accumulate"
-        if batches[0].w.kv_dtype == "fp8_e4m3" else f"{batches[0].w.kv_dtype} KV / f32 accumulate",
+        "dtype": ("e4m3 KV / f16 tensor-core MMA / f32 accumulate" if batches[0].w.kv_dtype == "fp8_e4m3"
+                  else "e4m3 KV with f32 scale per tile / f16 tensor-core MMA / f32 accumulate"
+                  if batches[0].w.block_scaled else f"{batches[0].w.kv_dtype} KV / f32 accumulate"),
         "data": "synthetic (seeded N(0,1) q/k/v, random block tables)",
         "config": {"workload": DESCRIPTION[args.workload],
                    "l2": "inputs larger than L2 (KV pool "

@@ -34,6 +34,9 @@
  *   [num_blocks][n_kv_heads][block_size][head_dim] elements, layer l at byte
  *   offset l * num_blocks * n_kv_heads * block_size * head_dim * elem_bytes.
  *   One (block, kv head) tile of block_size * head_dim elements is contiguous.
+ *   A PA_FP8_E4M3_BLOCK region continues, right after the tiles of its last
+ *   layer, with its scale table: fp32 [n_layers][num_blocks][n_kv_heads], the
+ *   scale of each (layer, block, kv head) tile of that region.
  */
 #ifndef PAGED_KV_PA_H
 #define PAGED_KV_PA_H
@@ -66,6 +69,12 @@ extern "C" {
 #define PA_BF16 1     /* bfloat16 */
 #define PA_FP8_E4M3 2 /* OCP FP8 E4M3FN codes, value = decode(code) * scale */
 #define PA_FP32 3     /* IEEE binary32 (decode output only: the fp32 check mode) */
+/* OCP FP8 E4M3FN codes with a dynamic scale per (block, kv head) tile, for K
+ * and for V: value = decode(code) * s, s = fl32(MaxAbs / 448) of the values
+ * the tile holds, kept in the region's scale table ("Optimización de KV Cache
+ * ...", section 8, dynamic scaling: the MaxAbs of each block is computed at
+ * inference time).  s = 0 marks an all-zero tile.  See pa_reshape_and_cache. */
+#define PA_FP8_E4M3_BLOCK 4
 
 #define PA_BLOCK_SIZE 16
 
@@ -75,10 +84,11 @@ extern "C" {
  *   block_size  tokens per block; must be 16
  *   n_kv_heads  KV heads (>= 1)
  *   head_dim    64 or 128
- *   kv_dtype    PA_FP16, PA_BF16 or PA_FP8_E4M3.  FP16 pools take binary16
- *               q/k/v; BF16 and FP8 pools take bfloat16 q/k/v.
- *   k_scale, v_scale  FP8 only: static per-tensor scales (> 0, finite); a code
- *               c stands for decode(c) * scale.  Ignored for 16-bit pools. */
+ *   kv_dtype    PA_FP16, PA_BF16, PA_FP8_E4M3 or PA_FP8_E4M3_BLOCK.  FP16
+ *               pools take binary16 q/k/v; the others take bfloat16 q/k/v.
+ *   k_scale, v_scale  PA_FP8_E4M3 only: static per-tensor scales (> 0,
+ *               finite); a code c stands for decode(c) * scale.  Ignored for
+ *               the other types. */
 typedef struct pa_pool_desc {
   int n_layers;
   int num_blocks;
@@ -104,11 +114,13 @@ PA_API int pa_kv_bytes_per_token(int n_layers, int n_kv_heads, int head_dim, int
                           size_t* bytes);
 
 /* Bytes of device memory the caller must provide for the K region and for the
- * V region of a pool described by *desc (all layers). */
+ * V region of a pool described by *desc (all layers; for PA_FP8_E4M3_BLOCK the
+ * scale table included, the total rounded up to a multiple of 16). */
 PA_API int pa_pool_bytes(const pa_pool_desc* desc, size_t* k_bytes, size_t* v_bytes);
 
-/* Largest num_blocks whose K + V regions fit in budget_bytes (desc->num_blocks
- * is ignored).  PA_ERR_NO_MEMORY if not even one block fits -- the "no
+/* Largest num_blocks whose K + V regions (tiles and, for PA_FP8_E4M3_BLOCK,
+ * 2 * n_layers * n_kv_heads fp32 scales per block) fit in budget_bytes
+ * (desc->num_blocks is ignored).  PA_ERR_NO_MEMORY if not even one block fits -- the "no
  * available memory for the cache blocks" start-up failure ("Optimización de KV
  * Cache ...", section 6.1). */
 PA_API int pa_pool_blocks_for_budget(const pa_pool_desc* desc, size_t budget_bytes, int* num_blocks);
@@ -208,7 +220,8 @@ PA_API int pa_prefix_stats(const pa_pool* pool, int* entries, long long* lookups
  * block dst, in layer `layer` (the device half of copy-on-write).  Pairs with
  * an id outside [0, num_blocks) are skipped and set PA_ERR_BOUNDS in the device
  * error word.  Destinations must be distinct and no destination may also be a
- * source in the same call. */
+ * source in the same call.  PA_FP8_E4M3_BLOCK pools copy the tiles' scales
+ * with them. */
 PA_API int pa_copy_blocks(pa_pool* pool, int layer, const int32_t* pairs_dev, int n_pairs, void* stream);
 
 /* ---- page swap to host memory ("KV Cache y PagedAttention", "Cómo
@@ -217,7 +230,9 @@ PA_API int pa_copy_blocks(pa_pool* pool, int layer, const int32_t* pairs_dev, in
  * KV-Cache", KV-cache offloading to system RAM) ----
  * A swapped block is the K and V of every kv head of every layer:
  * pa_swap_block_bytes per block, laid out in the host buffer as
- * [block][layer][K | V][n_kv_heads][block_size][head_dim] elements.  The host
+ * [block][layer][K | V][n_kv_heads][block_size][head_dim] elements; for
+ * PA_FP8_E4M3_BLOCK each block's record continues with its scales, fp32
+ * [layer][K | V][n_kv_heads], then zero bytes up to a multiple of 16.  The host
  * buffer must be page-locked and device-accessible (cudaHostAlloc /
  * cudaMallocHost, or cudaHostRegister'ed memory); the GPU reads or writes it
  * directly over the CPU-GPU link. */
@@ -248,7 +263,21 @@ PA_API int pa_swap_in(pa_pool* pool, int n, const int32_t* ids_dev, const void* 
  * FP8 pools store code = E4M3(round-to-nearest-even, saturating to +-448) of
  * the IEEE fp32 quotient x / scale ("Optimización de KV Cache ...", sections 4
  * and 8, static calibration).  16-bit pools store x unchanged.  Two tokens with
- * the same slot in one call race. */
+ * the same slot in one call race.
+ *
+ * PA_FP8_E4M3_BLOCK pools (same page, section 8, dynamic scaling) take the
+ * tokens in runs: a token and the tokens right after it in slot_mapping whose
+ * slots follow it within the same block.  For each run and kv head, separately
+ * for K and V, with m = max |x| over the run and s_run = fl32(m / 448):
+ *   - a run starting at offset 0 of its block starts the tile afresh: s = s_run;
+ *   - a run starting at offset o > 0 appends: s = max(s_old, s_run); if s grew,
+ *     every code c of rows 0 .. o-1 is re-encoded as
+ *     E4M3(fl32(fl32(decode(c) * s_old) / s)) (the originals are not kept);
+ *   - the run's values are stored as E4M3(fl32(x / s)), code 0 when s = 0;
+ *   - s goes to the scale table.
+ * The tokens one call writes into one block must form a single run (a
+ * sequence's new tokens in order do); two runs into one block in one call
+ * race.  A tile must be started at offset 0 before it is appended to. */
 PA_API int pa_reshape_and_cache(pa_pool* pool, int layer, const void* k, const void* v,
                          const int64_t* slot_mapping_dev, int T, void* stream);
 

@@ -28,6 +28,7 @@ PA_FP16 = 0
 PA_BF16 = 1
 PA_FP8_E4M3 = 2
 PA_FP32 = 3
+PA_FP8_E4M3_BLOCK = 4
 
 ERROR_NAMES = {PA_OK: "PA_OK", PA_ERR_INVALID: "PA_ERR_INVALID",
                PA_ERR_UNSUPPORTED: "PA_ERR_UNSUPPORTED",

@@ -4,9 +4,10 @@
 // kernel takes the block table as an extra input and gathers each 16-token
 // page of keys and values by indirection instead of slicing a contiguous slab
 // ("Capítulo 8 -- Gestión de caché KV de nueva generación", section 8.1).
-// Pages may hold FP8 E4M3 codes with a static per-tensor scale, dequantised as
-// they are used ("Optimización de KV Cache con PagedAttention y Cuantización
-// FP8 para Contextos Largos (128K)", sections 4 and 8).  Long contexts (up to
+// Pages may hold FP8 E4M3 codes with a static per-tensor scale or with a scale
+// per (block, kv head) tile, dequantised as they are used ("Optimización de KV
+// Cache con PagedAttention y Cuantización FP8 para Contextos Largos (128K)",
+// sections 4 and 8, static calibration and dynamic scaling).  Long contexts (up to
 // the 128K of that page's title) are split along their pages; a second kernel
 // merges the partial softmax states.
 //
@@ -36,6 +37,10 @@
 //    binary16, and the scale is folded back into the softmax exponent.  For
 //    bfloat16 pools (and in fp32-output mode) P is split into a high and a low
 //    16-bit part, two MMAs, so P carries ~16 significant bits.
+//  * Per-tile scales (block-scaled pools) ride with the page: the producer reads
+//    them next to the table entries and hands them over in shared memory; the
+//    K scale joins the softmax exponent's factor, the V scale weights P
+//    relative to the largest V scale seen so far (kept <= 1 for 16-bit P).
 //  * Accumulation follows logical page order within each warp and a fixed warp
 //    order in the merge, so the result is bit-identical under any relabelling
 //    of physical blocks.
@@ -50,7 +55,7 @@
 
 namespace pa {
 
-enum KvKind { KV_F16 = 0, KV_BF16 = 1, KV_E4M3 = 2 };
+enum KvKind { KV_F16 = 0, KV_BF16 = 1, KV_E4M3 = 2, KV_E4M3B = 4 };  // KV_E4M3B: scale per tile
 enum OutKind { OUT_F16 = 0, OUT_BF16 = 1, OUT_F32 = 3 };
 
 constexpr int kConsumerWarps = 4;
@@ -59,7 +64,9 @@ constexpr unsigned kFull = 0xffffffffu;
 
 template <int KV, int D>
 struct Cfg {
-  static constexpr int kElem = (KV == KV_E4M3) ? 1 : 2;
+  static constexpr bool kFp8 = (KV == KV_E4M3) || (KV == KV_E4M3B);
+  static constexpr bool kBlockScaled = (KV == KV_E4M3B);
+  static constexpr int kElem = kFp8 ? 1 : 2;
   static constexpr int kRowBytes = D * kElem;    // one token row of a tile
   static constexpr int kTile = 16 * kRowBytes;   // bytes of one (block, kv head) tile
   // Rows of 128 or 256 bytes are loaded with 128-byte TMA swizzling, which
@@ -75,9 +82,11 @@ struct Cfg {
   // FP8 pools keep the query fragments in shared memory instead of 16 registers
   // per thread ([warp][D/16 pairs][32 lanes] x 8 bytes), which lets five CTAs
   // share an SM; 16-bit pools are limited by their ring size anyway.
-  static constexpr bool kQInSmem = (KV == KV_E4M3);
+  static constexpr bool kQInSmem = kFp8;
   static constexpr int kQBytes = kQInSmem ? kConsumerWarps * (D / 16) * 32 * 8 : 0;
-  static constexpr int kSmem = kDataBytes + 2 * kStages * 8 + kQBytes + kAlign;
+  // block-scaled pools: the (K, V) scales of the page in each stage
+  static constexpr int kScaleBytes = kBlockScaled ? kStages * 8 : 0;
+  static constexpr int kSmem = kDataBytes + 2 * kStages * 8 + kQBytes + kScaleBytes + kAlign;
   // register budget, in CTAs per SM (16-bit pools: what their ring size allows)
   static constexpr int kMinBlocks = kQInSmem ? 5 : (D == 128 ? 3 : 4);
   static constexpr bool kMmaBf16 = (KV == KV_BF16);
@@ -95,7 +104,9 @@ struct DecodeArgs {
   int Hq, Hkv, G, num_blocks;
   int splits, pages_per_split;
   float qk_scale_log2;  // softmax_scale * log2(e) (* k_scale for FP8)
-  float v_scale;        // 1 for 16-bit pools
+  float v_scale;        // 1 for 16-bit and block-scaled pools
+  const float* ksc;     // block-scaled pools: this layer's scales [num_blocks][Hkv]
+  const float* vsc;
   unsigned int* err;
 };
 
@@ -131,6 +142,8 @@ __global__ void __launch_bounds__(kThreads, (Cfg<KV, D>::kMinBlocks)) decode_ker
   using C = Cfg<KV, D>;
   constexpr bool BF = C::kMmaBf16;
   constexpr bool SWZ = C::kSwizzle;
+  constexpr bool F8 = C::kFp8;
+  constexpr bool BLK = C::kBlockScaled;
   constexpr int NT = D / 16;  // MMA steps along the head dim (QK) / m-tiles (PV)
   extern __shared__ __align__(16) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
@@ -138,6 +151,8 @@ __global__ void __launch_bounds__(kThreads, (Cfg<KV, D>::kMinBlocks)) decode_ker
   uint8_t* ring = smem;
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::kDataBytes);
   uint64_t* empty = full + C::kStages;
+  float2* stage_scale =
+      reinterpret_cast<float2*>(smem + C::kDataBytes + 2 * C::kStages * 8 + C::kQBytes);
 
   const int split = blockIdx.x, h = blockIdx.y, seq = blockIdx.z;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -180,20 +195,49 @@ __global__ void __launch_bounds__(kThreads, (Cfg<KV, D>::kMinBlocks)) decode_ker
     // ------------------------------------------------------------ producer
     const int32_t* trow = a.tables + (size_t)seq * a.max_blocks + p_begin;
     const uint64_t policy = l2_evict_first_policy();
+    // Lane i holds the table entry (and, block-scaled, the tile scales) of page
+    // base + i.  The next 32 entries are loaded as soon as a batch starts and
+    // checked, and their scales fetched, a few pages into it, so no load sits
+    // on the path between two batches.
+    auto checked = [&](int raw, int idx) {
+      if (idx < n_local && (raw < 0 || raw >= a.num_blocks)) {
+        record_error(a.err, PA_ERR_BOUNDS);
+        return 0;
+      }
+      return raw;
+    };
+    int phys = checked(lane < n_local ? trow[lane] : 0, lane);
+    float sk = 0.f, sv = 0.f;
+    if constexpr (BLK) {
+      if (lane < n_local) {
+        sk = a.ksc[(size_t)phys * a.Hkv + h];
+        sv = a.vsc[(size_t)phys * a.Hkv + h];
+      }
+    }
     int issued = 0;
     bool abort = false;
     for (int base = 0; base < n_local && !abort; base += 32) {
-      int phys = 0;
-      if (base + lane < n_local) {
-        phys = trow[base + lane];
-        if (phys < 0 || phys >= a.num_blocks) {
-          record_error(a.err, PA_ERR_BOUNDS);
-          phys = 0;
-        }
-      }
+      const int nidx = base + 32 + lane;
+      int phys_next = nidx < n_local ? trow[nidx] : 0;
+      float sk_next = 0.f, sv_next = 0.f;
       const int cnt = min(32, n_local - base);
+      const int fetch_at = min(cnt - 1, 3);
       for (int j = 0; j < cnt; ++j) {
+        if (j == fetch_at) {
+          phys_next = checked(phys_next, nidx);
+          if constexpr (BLK) {
+            if (nidx < n_local) {
+              sk_next = a.ksc[(size_t)phys_next * a.Hkv + h];
+              sv_next = a.vsc[(size_t)phys_next * a.Hkv + h];
+            }
+          }
+        }
         const int ph = __shfl_sync(kFull, phys, j);
+        float skj = 0.f, svj = 0.f;
+        if constexpr (BLK) {
+          skj = __shfl_sync(kFull, sk, j);
+          svj = __shfl_sync(kFull, sv, j);
+        }
         int stop = 0;
         if (lane == 0) {
           const int k = base + j, stage = k % C::kStages;
@@ -203,6 +247,8 @@ __global__ void __launch_bounds__(kThreads, (Cfg<KV, D>::kMinBlocks)) decode_ker
           } else {
             uint8_t* dst = ring + stage * C::kStageBytes;
             const int row0 = (ph * a.Hkv + h) * 16;
+            // the scales are published by the same arrive that starts the copies
+            if constexpr (BLK) stage_scale[stage] = make_float2(skj, svj);
             mbar_arrive_expect_tx(&full[stage], 2 * C::kTile);
             load_tile<C::kTmaRank>(dst, &tmk, row0, &full[stage], policy);
             load_tile<C::kTmaRank>(dst + C::kTile, &tmv, row0, &full[stage], policy);
@@ -214,6 +260,9 @@ __global__ void __launch_bounds__(kThreads, (Cfg<KV, D>::kMinBlocks)) decode_ker
           break;
         }
       }
+      phys = phys_next;
+      sk = sk_next;
+      sv = sv_next;
     }
     // Wait (bounded) until every copy this CTA issued has landed, so no bulk
     // write can still target the ring when it is reused or the CTA exits.
@@ -243,7 +292,7 @@ __global__ void __launch_bounds__(kThreads, (Cfg<KV, D>::kMinBlocks)) decode_ker
         raw[4 * c + 2] = u.z;
         raw[4 * c + 3] = u.w;
       }
-      if constexpr (KV == KV_E4M3) {
+      if constexpr (F8) {
         // bfloat16 q -> binary16 with a power-of-two prescale shared by the group
         float amax = 0.f;
 #pragma unroll
@@ -279,6 +328,10 @@ __global__ void __launch_bounds__(kThreads, (Cfg<KV, D>::kMinBlocks)) decode_ker
     constexpr int KB = D / 4 * C::kElem;  // K bytes per row per thread
     constexpr int VB = D / 8 * C::kElem;  // V bytes per row per thread
     constexpr int RB = C::kRowBytes;
+    // block-scaled pools: V weights are taken relative to the largest V scale
+    // this warp has seen (vref), so P * sv / vref stays <= 1 in 16 bits; the
+    // accumulator is rescaled when vref grows and multiplied by it at the end
+    float vref = 0.f, vref_inv = 0.f;
 
     for (int k = warp; k < n_local; k += kConsumerWarps) {
       const int stage = k % C::kStages;
@@ -290,6 +343,8 @@ __global__ void __launch_bounds__(kThreads, (Cfg<KV, D>::kMinBlocks)) decode_ker
       const uint8_t* Ks = ring + stage * C::kStageBytes;
       const uint8_t* Vs = Ks + C::kTile;
       const int tok0 = (p_begin + k) * 16;
+      float2 psc = make_float2(1.f, 1.f);
+      if constexpr (BLK) psc = stage_scale[stage];
 
       // ---- issue every shared-memory read of the page up front
       constexpr int VW = VB / 4;  // V words per row per thread
@@ -328,7 +383,7 @@ __global__ void __launch_bounds__(kThreads, (Cfg<KV, D>::kMinBlocks)) decode_ker
 #pragma unroll
       for (int c = 0; c < KB / 16; ++c) {
         const uint4 r0 = kr[0][c], r1 = kr[1][c];
-        if constexpr (KV == KV_E4M3) {
+        if constexpr (F8) {
           const uint32_t w0[4] = {r0.x, r0.y, r0.z, r0.w};
           const uint32_t w1[4] = {r1.x, r1.y, r1.z, r1.w};
 #pragma unroll
@@ -348,8 +403,9 @@ __global__ void __launch_bounds__(kThreads, (Cfg<KV, D>::kMinBlocks)) decode_ker
       }
 
       // ---- online softmax over this page (tokens g and g+8; heads 2t, 2t+1)
-      float x0 = s[0] * qk_scale, x1 = s[1] * qk_scale;
-      float x2 = s[2] * qk_scale, x3 = s[3] * qk_scale;
+      const float qks = BLK ? qk_scale * psc.x : qk_scale;
+      float x0 = s[0] * qks, x1 = s[1] * qks;
+      float x2 = s[2] * qks, x3 = s[3] * qks;
       if (tok0 + 16 > ctx) {  // last, partial page (warp-uniform): slots past ctx hold anything
         if (tok0 + g >= ctx) x0 = x1 = -INFINITY;
         if (tok0 + g + 8 >= ctx) x2 = x3 = -INFINITY;
@@ -368,24 +424,42 @@ __global__ void __launch_bounds__(kThreads, (Cfg<KV, D>::kMinBlocks)) decode_ker
       }
       // token 0 of every page is valid, so the new maxima are finite
       const float mn0 = fmaxf(m0, pm0), mn1 = fmaxf(m1, pm1);
-      if (__any_sync(kFull, (mn0 != m0) | (mn1 != m1))) {  // rescale only when a max moved
+      const bool vgrow = BLK && psc.y > vref;  // warp-uniform: one scale per page
+      if (__any_sync(kFull, (mn0 != m0) | (mn1 != m1)) || vgrow) {  // rescale only when needed
         const float al0 = fast_exp2(m0 - mn0), al1 = fast_exp2(m1 - mn1);
         l0 *= al0;
         l1 *= al1;
+        float ov0 = al0, ov1 = al1;
+        if constexpr (BLK) {
+          if (vgrow) {
+            const float r = vref / psc.y;  // 0 on the first page with a nonzero scale
+            ov0 *= r;
+            ov1 *= r;
+            vref = psc.y;
+            vref_inv = 1.f / psc.y;
+          }
+        }
 #pragma unroll
         for (int i = 0; i < NT; ++i) {
-          o[i][0] *= al0;
-          o[i][1] *= al1;
-          o[i][2] *= al0;
-          o[i][3] *= al1;
+          o[i][0] *= ov0;
+          o[i][1] *= ov1;
+          o[i][2] *= ov0;
+          o[i][3] *= ov1;
         }
         m0 = mn0;
         m1 = mn1;
       }
-      const float p0 = fast_exp2(x0 - m0), p1 = fast_exp2(x1 - m1);
-      const float p2 = fast_exp2(x2 - m0), p3 = fast_exp2(x3 - m1);
+      float p0 = fast_exp2(x0 - m0), p1 = fast_exp2(x1 - m1);
+      float p2 = fast_exp2(x2 - m0), p3 = fast_exp2(x3 - m1);
       l0 += p0 + p2;
       l1 += p1 + p3;
+      if constexpr (BLK) {  // weights of this page's V codes: P * sv / vref
+        const float f = psc.y * vref_inv;
+        p0 *= f;
+        p1 *= f;
+        p2 *= f;
+        p3 *= f;
+      }
 
       // ---- P^T as the B operand: rows (tokens 2t, 2t+1 | 2t+8, 2t+9), column head g
       const uint32_t plo = pack2<BF>(p0, p1), phi = pack2<BF>(p2, p3);
@@ -402,7 +476,7 @@ __global__ void __launch_bounds__(kThreads, (Cfg<KV, D>::kMinBlocks)) decode_ker
 #pragma unroll
         for (int i = 0; i < NT; ++i) {
           uint32_t af[4];
-          if constexpr (KV == KV_E4M3) {
+          if constexpr (F8) {
             const uint32_t sel = (i & 1) ? 0x7362u : 0x5140u;
             const uint32_t x01 = __byte_perm(vw[0][i >> 1], vw[1][i >> 1], sel);
             const uint32_t x23 = __byte_perm(vw[2][i >> 1], vw[3][i >> 1], sel);
@@ -427,6 +501,15 @@ __global__ void __launch_bounds__(kThreads, (Cfg<KV, D>::kMinBlocks)) decode_ker
     for (int off = 4; off < 32; off <<= 1) {
       l0 += __shfl_xor_sync(kFull, l0, off);
       l1 += __shfl_xor_sync(kFull, l1, off);
+    }
+    if constexpr (BLK) {  // back to value units (vref = 0 only if every V here is 0)
+#pragma unroll
+      for (int i = 0; i < NT; ++i) {
+        o[i][0] *= vref;
+        o[i][1] *= vref;
+        o[i][2] *= vref;
+        o[i][3] *= vref;
+      }
     }
   }
 
@@ -727,6 +810,8 @@ Dispatch pick(int kv_dtype, int head_dim, int out_dtype) {
       return pick_d<KV_F16>(head_dim, out_dtype);
     case PA_BF16:
       return pick_d<KV_BF16>(head_dim, out_dtype);
+    case PA_FP8_E4M3_BLOCK:
+      return pick_d<KV_E4M3B>(head_dim, out_dtype);
     default:
       return pick_d<KV_E4M3>(head_dim, out_dtype);
   }
@@ -899,6 +984,8 @@ int pa_decode(pa_pool* pool, int layer, void* out, int out_dtype, const void* q,
   const float log2e = 1.4426950408889634f;
   a.qk_scale_log2 = softmax_scale * log2e * (d.kv_dtype == PA_FP8_E4M3 ? d.k_scale : 1.f);
   a.v_scale = d.kv_dtype == PA_FP8_E4M3 ? d.v_scale : 1.f;
+  a.ksc = pool->block_scaled ? layer_scales(pool, pool->k, layer) : nullptr;
+  a.vsc = pool->block_scaled ? layer_scales(pool, pool->v, layer) : nullptr;
   a.err = err;
   cudaError_t e = disp.launch(a, tk, tv, S, static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return fail(PA_ERR_CUDA, "decode launch: %s", cudaGetErrorString(e));

@@ -31,6 +31,7 @@ int elem_bytes_of(int dtype) {
     case PA_BF16:
       return 2;
     case PA_FP8_E4M3:
+    case PA_FP8_E4M3_BLOCK:
       return 1;
     default:
       return 0;
@@ -57,10 +58,19 @@ int check_desc_shape(const pa_pool_desc* d) {
   return PA_OK;
 }
 
-size_t block_bytes_all_layers(const pa_pool_desc* d) {
-  // K + V, every layer, one block
+size_t tile_bytes_all_layers(const pa_pool_desc* d) {
+  // K + V codes, every layer, one block
   return 2ull * (size_t)d->n_layers * (size_t)d->n_kv_heads * (size_t)d->block_size *
          (size_t)d->head_dim * (size_t)elem_bytes_of(d->kv_dtype);
+}
+
+// fp32 scales one block adds to the K and V scale tables (block-scaled FP8 only)
+size_t scale_bytes_per_block(const pa_pool_desc* d) {
+  return d->kv_dtype == PA_FP8_E4M3_BLOCK ? 2ull * d->n_layers * d->n_kv_heads * sizeof(float) : 0;
+}
+
+size_t block_bytes_all_layers(const pa_pool_desc* d) {
+  return tile_bytes_all_layers(d) + scale_bytes_per_block(d);
 }
 }  // namespace
 
@@ -106,7 +116,8 @@ int pa_pool_bytes(const pa_pool_desc* desc, size_t* k_bytes, size_t* v_bytes) {
   int st = check_desc_shape(desc);
   if (st) return st;
   if (desc->num_blocks < 1) return pa::fail(PA_ERR_INVALID, "num_blocks must be >= 1");
-  size_t half = block_bytes_all_layers(desc) / 2 * (size_t)desc->num_blocks;
+  size_t half = tile_bytes_all_layers(desc) / 2 * (size_t)desc->num_blocks;
+  half += (scale_bytes_per_block(desc) / 2 * (size_t)desc->num_blocks + 15) / 16 * 16;
   if (k_bytes) *k_bytes = half;
   if (v_bytes) *v_bytes = half;
   return PA_OK;
@@ -118,6 +129,11 @@ int pa_pool_blocks_for_budget(const pa_pool_desc* desc, size_t budget_bytes, int
   if (!num_blocks) return pa::fail(PA_ERR_INVALID, "null output");
   size_t per = block_bytes_all_layers(desc);
   size_t n = budget_bytes / per;
+  // each scale table is rounded up to 16 bytes: drop blocks while that spills over
+  auto total = [&](size_t nb) {
+    return tile_bytes_all_layers(desc) * nb + 2 * ((scale_bytes_per_block(desc) / 2 * nb + 15) / 16 * 16);
+  };
+  while (n > 0 && total(n) > budget_bytes) --n;
   if (n == 0)
     return pa::fail(PA_ERR_NO_MEMORY,
                     "no available memory for the cache blocks: budget %zu B < one block %zu B",
@@ -143,6 +159,8 @@ int pa_pool_create(const pa_pool_desc* desc, void* k_cache, void* v_cache, pa_po
   p->elem_bytes = elem_bytes_of(desc->kv_dtype);
   p->tile_bytes = (size_t)desc->block_size * desc->head_dim * p->elem_bytes;
   p->layer_bytes = (size_t)desc->num_blocks * desc->n_kv_heads * p->tile_bytes;
+  p->block_scaled = desc->kv_dtype == PA_FP8_E4M3_BLOCK;
+  p->scale_offset = p->block_scaled ? (size_t)desc->n_layers * p->layer_bytes : 0;
   try {
     p->refcount.assign(desc->num_blocks, 0);
     p->free_stack.resize(desc->num_blocks);

@@ -22,6 +22,10 @@ struct pa_pool {
   int elem_bytes;                 // 1 (FP8) or 2
   size_t tile_bytes;              // one (block, kv head) tile: block_size * head_dim * elem_bytes
   size_t layer_bytes;             // one layer of K (or V): num_blocks * n_kv_heads * tile_bytes
+  // PA_FP8_E4M3_BLOCK: byte offset, in the K and in the V region, of the fp32
+  // scale table [n_layers][num_blocks][n_kv_heads] (= n_layers * layer_bytes); 0 otherwise.
+  bool block_scaled = false;
+  size_t scale_offset = 0;
   std::vector<int32_t> refcount;  // per block
   std::vector<int32_t> free_stack;  // top = back()
   // TMA descriptors of each layer's K and V regions ([2 * layer + {0: K, 1: V}]),
@@ -50,6 +54,12 @@ int fail(int code, const char* fmt, ...);
 unsigned int* device_error_word();
 
 int check_pool_layer(const pa_pool* pool, int layer);
+
+// The K and V scale tables of `layer` of a block-scaled pool: fp32 [num_blocks][n_kv_heads].
+inline float* layer_scales(const pa_pool* p, uint8_t* region, int layer) {
+  return reinterpret_cast<float*>(region + p->scale_offset) +
+         (size_t)layer * p->desc.num_blocks * p->desc.n_kv_heads;
+}
 
 }  // namespace pa
 

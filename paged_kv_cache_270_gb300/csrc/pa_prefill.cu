@@ -23,6 +23,10 @@
 //    straight from the S accumulators (16 dims per n-tile pair).  Q and K share
 //    a permutation of the head dim (contiguous 16-byte runs per thread), and the
 //    output dims are permuted so each thread reads contiguous runs of V rows.
+//  * Block-scaled FP8 pools: each page's K and V scales come with the page (the
+//    producer reads them beside the table entries); the K scale joins the
+//    softmax exponent's factor, the V scale weights P relative to the largest V
+//    scale seen so far, as in decode.
 //  * FP8 codes convert exactly to binary16; bf16 q of an FP8 cache is rescaled
 //    by a power of two per warp; P is split into two 16-bit parts for bf16
 //    caches and the fp32 output mode, as in decode.
@@ -39,7 +43,7 @@
 namespace pa {
 namespace {
 
-enum { P_F16 = 0, P_BF16 = 1, P_E4M3 = 2 };
+enum { P_F16 = 0, P_BF16 = 1, P_E4M3 = 2, P_E4M3B = 4 };  // P_E4M3B: scale per tile
 enum { O_F16 = 0, O_BF16 = 1, O_F32 = 3 };
 
 constexpr unsigned kFullMask = 0xffffffffu;
@@ -47,7 +51,9 @@ constexpr int kMaxGroup = 8;
 
 template <int KV, int D>
 struct PCfg {
-  static constexpr int kElem = (KV == P_E4M3) ? 1 : 2;
+  static constexpr bool kFp8 = (KV == P_E4M3) || (KV == P_E4M3B);
+  static constexpr bool kBlockScaled = (KV == P_E4M3B);
+  static constexpr int kElem = kFp8 ? 1 : 2;
   static constexpr int kRowBytes = D * kElem;
   static constexpr int kTile = 16 * kRowBytes;
   static constexpr bool kSwizzle = (kRowBytes % 128) == 0;
@@ -58,7 +64,8 @@ struct PCfg {
   static constexpr int kStageOut = kMaxGroup * 16 * D * 4;  // output staging, fp32
   static constexpr int kDataBytes = kRingBytes > kStageOut ? kRingBytes : kStageOut;
   static constexpr int kAlign = 1024;
-  static constexpr int kSmem = kDataBytes + 2 * kStages * 8 + kAlign;
+  static constexpr int kScaleBytes = kBlockScaled ? kStages * 8 : 0;  // (K, V) scales per stage
+  static constexpr int kSmem = kDataBytes + 2 * kStages * 8 + kScaleBytes + kAlign;
   static constexpr bool kMmaBf16 = (KV == P_BF16);
 };
 
@@ -72,6 +79,8 @@ struct PrefillArgs {
   int Hq, Hkv, G, num_blocks;
   float qk_scale_log2;
   float v_scale;
+  const float* ksc;  // block-scaled pools: this layer's scales [num_blocks][Hkv]
+  const float* vsc;
   unsigned int* err;
 };
 
@@ -102,6 +111,8 @@ __global__ void __launch_bounds__((kMaxGroup + 1) * 32) prefill_kernel(
   using C = PCfg<KV, D>;
   constexpr bool BF = C::kMmaBf16;
   constexpr bool SWZ = C::kSwizzle;
+  constexpr bool F8 = C::kFp8;
+  constexpr bool BLK = C::kBlockScaled;
   constexpr int NTO = D / 8;  // output n-tiles (8 dims each)
   constexpr int QW = D / 8;   // 32-bit words of q per row per thread
   constexpr int KB = D / 4 * C::kElem;
@@ -113,6 +124,7 @@ __global__ void __launch_bounds__((kMaxGroup + 1) * 32) prefill_kernel(
   uint8_t* ring = smem;
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::kDataBytes);
   uint64_t* empty = full + C::kStages;
+  float2* stage_scale = reinterpret_cast<float2*>(smem + C::kDataBytes + 2 * C::kStages * 8);
 
   const int qt = gridDim.x - 1 - blockIdx.x, h = blockIdx.y, seq = blockIdx.z;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -152,16 +164,26 @@ __global__ void __launch_bounds__((kMaxGroup + 1) * 32) prefill_kernel(
     bool abort = false;
     for (int base = 0; base < npages && !abort; base += 32) {
       int phys = 0;
+      float sk = 0.f, sv = 0.f;
       if (base + lane < npages) {
         phys = trow[base + lane];
         if (phys < 0 || phys >= a.num_blocks) {
           record_error(a.err, PA_ERR_BOUNDS);
           phys = 0;
         }
+        if constexpr (BLK) {
+          sk = a.ksc[(size_t)phys * a.Hkv + h];
+          sv = a.vsc[(size_t)phys * a.Hkv + h];
+        }
       }
       const int cnt = min(32, npages - base);
       for (int j = 0; j < cnt; ++j) {
         const int ph = __shfl_sync(kFullMask, phys, j);
+        float skj = 0.f, svj = 0.f;
+        if constexpr (BLK) {
+          skj = __shfl_sync(kFullMask, sk, j);
+          svj = __shfl_sync(kFullMask, sv, j);
+        }
         int stop = 0;
         if (lane == 0) {
           const int k = base + j, stage = k % C::kStages;
@@ -171,6 +193,7 @@ __global__ void __launch_bounds__((kMaxGroup + 1) * 32) prefill_kernel(
           } else {
             uint8_t* dst = ring + stage * C::kStageBytes;
             const int row0 = (ph * a.Hkv + h) * 16;
+            if constexpr (BLK) stage_scale[stage] = make_float2(skj, svj);  // published by the arrive
             mbar_arrive_expect_tx(&full[stage], 2 * C::kTile);
             load_page_tile<C::kTmaRank>(dst, &tmk, row0, &full[stage], policy);
             load_page_tile<C::kTmaRank>(dst + C::kTile, &tmv, row0, &full[stage], policy);
@@ -217,7 +240,7 @@ __global__ void __launch_bounds__((kMaxGroup + 1) * 32) prefill_kernel(
       raw0[4 * c] = u0.x; raw0[4 * c + 1] = u0.y; raw0[4 * c + 2] = u0.z; raw0[4 * c + 3] = u0.w;
       raw1[4 * c] = u1.x; raw1[4 * c + 1] = u1.y; raw1[4 * c + 2] = u1.z; raw1[4 * c + 3] = u1.w;
     }
-    if constexpr (KV == P_E4M3) {
+    if constexpr (F8) {
       float amax = 0.f;
 #pragma unroll
       for (int w = 0; w < QW; ++w) {
@@ -253,6 +276,8 @@ __global__ void __launch_bounds__((kMaxGroup + 1) * 32) prefill_kernel(
   float o[NTO][4];
 #pragma unroll
   for (int i = 0; i < NTO; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
+  // block-scaled pools: V weights relative to the largest V scale seen (as in decode)
+  float vref = 0.f, vref_inv = 0.f;
 
   for (int k = 0; k < npages; ++k) {
     const int stage = k % C::kStages;
@@ -263,6 +288,8 @@ __global__ void __launch_bounds__((kMaxGroup + 1) * 32) prefill_kernel(
     const uint8_t* Ks = ring + stage * C::kStageBytes;
     const uint8_t* Vs = Ks + C::kTile;
     const int key0 = 16 * k;
+    float2 psc = make_float2(1.f, 1.f);
+    if constexpr (BLK) psc = stage_scale[stage];
 
     // ---- S[row][key] = Q K^T, keys g + 8 nt of this page per n-tile nt
     float s[2][4];
@@ -274,7 +301,7 @@ __global__ void __launch_bounds__((kMaxGroup + 1) * 32) prefill_kernel(
       for (int c = 0; c < KB / 16; ++c) {
         const uint4 r = lds128(Ks + toff<SWZ>(kro + 16 * c));
         const uint32_t w[4] = {r.x, r.y, r.z, r.w};
-        if constexpr (KV == P_E4M3) {
+        if constexpr (F8) {
 #pragma unroll
           for (int jj = 0; jj < 4; ++jj) {
             const int j = 4 * c + jj;  // dims t*D/4 + 4j .. 4j+3
@@ -294,10 +321,11 @@ __global__ void __launch_bounds__((kMaxGroup + 1) * 32) prefill_kernel(
 
     // ---- causal mask (pages that reach the tile's first query) and online softmax
     float x[2][4];
+    const float qks = BLK ? qk_scale * psc.x : qk_scale;
 #pragma unroll
     for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
-      for (int e = 0; e < 4; ++e) x[nt][e] = s[nt][e] * qk_scale;
+      for (int e = 0; e < 4; ++e) x[nt][e] = s[nt][e] * qks;
     if (key0 + 15 > pos0) {
 #pragma unroll
       for (int nt = 0; nt < 2; ++nt) {
@@ -317,16 +345,27 @@ __global__ void __launch_bounds__((kMaxGroup + 1) * 32) prefill_kernel(
     }
     // key 0 (page 0) is visible to every row, so the maxima are finite from there on
     const float mn0 = fmaxf(m0, pm0), mn1 = fmaxf(m1, pm1);
-    if (__any_sync(kFullMask, (mn0 != m0) | (mn1 != m1))) {
+    const bool vgrow = BLK && psc.y > vref;  // warp-uniform
+    if (__any_sync(kFullMask, (mn0 != m0) | (mn1 != m1)) || vgrow) {
       const float al0 = fast_exp2(m0 - mn0), al1 = fast_exp2(m1 - mn1);
       l0 *= al0;
       l1 *= al1;
+      float ov0 = al0, ov1 = al1;
+      if constexpr (BLK) {
+        if (vgrow) {
+          const float r = vref / psc.y;
+          ov0 *= r;
+          ov1 *= r;
+          vref = psc.y;
+          vref_inv = 1.f / psc.y;
+        }
+      }
 #pragma unroll
       for (int i = 0; i < NTO; ++i) {
-        o[i][0] *= al0;
-        o[i][1] *= al0;
-        o[i][2] *= al1;
-        o[i][3] *= al1;
+        o[i][0] *= ov0;
+        o[i][1] *= ov0;
+        o[i][2] *= ov1;
+        o[i][3] *= ov1;
       }
       m0 = mn0;
       m1 = mn1;
@@ -340,6 +379,13 @@ __global__ void __launch_bounds__((kMaxGroup + 1) * 32) prefill_kernel(
       p[nt][3] = fast_exp2(x[nt][3] - m1);
       l0 += p[nt][0] + p[nt][1];
       l1 += p[nt][2] + p[nt][3];
+    }
+    if constexpr (BLK) {  // weights of this page's V codes: P * sv / vref
+      const float f = psc.y * vref_inv;
+#pragma unroll
+      for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) p[nt][e] *= f;
     }
     // P as the A operand: rows g / g+8, keys 2t,2t+1 (a0,a1) and 2t+8,2t+9 (a2,a3)
     uint32_t pa[4] = {pack2<BF>(p[0][0], p[0][1]), pack2<BF>(p[0][2], p[0][3]),
@@ -388,7 +434,7 @@ __global__ void __launch_bounds__((kMaxGroup + 1) * 32) prefill_kernel(
 #pragma unroll
       for (int nt = 0; nt < NTO; ++nt) {
         uint32_t b0, b1;
-        if constexpr (KV == P_E4M3) {
+        if constexpr (F8) {
           const int w = nt >> 2, e = nt & 3;
           const uint32_t sel = (e < 2) ? 0x5140u : 0x7362u;
           const uint32_t x01 = __byte_perm(vw[0][w], vw[1][w], sel);
@@ -418,8 +464,9 @@ __global__ void __launch_bounds__((kMaxGroup + 1) * 32) prefill_kernel(
 
   // stage rows g / g+8: accumulator column c of n-tile nt is dim c * D/8 + nt
   float* st = reinterpret_cast<float*>(smem) + warp * 16 * D;
-  const float i0 = l0 > 0.f ? a.v_scale / l0 : 0.f;
-  const float i1 = l1 > 0.f ? a.v_scale / l1 : 0.f;
+  const float vs = BLK ? vref : a.v_scale;
+  const float i0 = l0 > 0.f ? vs / l0 : 0.f;
+  const float i1 = l1 > 0.f ? vs / l1 : 0.f;
   const int c0 = (2 * t) * (D / 8), c1 = (2 * t + 1) * (D / 8);
 #pragma unroll
   for (int nt = 0; nt < NTO; ++nt) {
@@ -479,10 +526,17 @@ PDispatch ppick_out(int out_dtype) {
 }
 
 PDispatch ppick(int kv_dtype, int head_dim, int out_dtype) {
-  const int kv = kv_dtype == PA_FP16 ? P_F16 : kv_dtype == PA_BF16 ? P_BF16 : P_E4M3;
-  if (kv == P_F16) return head_dim == 64 ? ppick_out<P_F16, 64>(out_dtype) : ppick_out<P_F16, 128>(out_dtype);
-  if (kv == P_BF16) return head_dim == 64 ? ppick_out<P_BF16, 64>(out_dtype) : ppick_out<P_BF16, 128>(out_dtype);
-  return head_dim == 64 ? ppick_out<P_E4M3, 64>(out_dtype) : ppick_out<P_E4M3, 128>(out_dtype);
+  const bool d64 = head_dim == 64;
+  switch (kv_dtype) {
+    case PA_FP16:
+      return d64 ? ppick_out<P_F16, 64>(out_dtype) : ppick_out<P_F16, 128>(out_dtype);
+    case PA_BF16:
+      return d64 ? ppick_out<P_BF16, 64>(out_dtype) : ppick_out<P_BF16, 128>(out_dtype);
+    case PA_FP8_E4M3_BLOCK:
+      return d64 ? ppick_out<P_E4M3B, 64>(out_dtype) : ppick_out<P_E4M3B, 128>(out_dtype);
+    default:
+      return d64 ? ppick_out<P_E4M3, 64>(out_dtype) : ppick_out<P_E4M3, 128>(out_dtype);
+  }
 }
 
 int pconfigure(PInfo& pi) {
@@ -550,6 +604,8 @@ int pa_prefill(pa_pool* pool, int layer, void* out, int out_dtype, const void* q
   a.num_blocks = d.num_blocks;
   a.qk_scale_log2 = softmax_scale * 1.4426950408889634f * (d.kv_dtype == PA_FP8_E4M3 ? d.k_scale : 1.f);
   a.v_scale = d.kv_dtype == PA_FP8_E4M3 ? d.v_scale : 1.f;
+  a.ksc = pool->block_scaled ? layer_scales(pool, pool->k, layer) : nullptr;
+  a.vsc = pool->block_scaled ? layer_scales(pool, pool->v, layer) : nullptr;
   a.err = err;
   const int tiles = (max_chunk + 15) / 16;
   cudaError_t e = disp.launch(a, tk, tv, tiles, S, static_cast<cudaStream_t>(stream));

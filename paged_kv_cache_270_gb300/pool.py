@@ -14,7 +14,8 @@ import torch
 
 from . import _native as N
 
-KV_DTYPES = {"fp16": N.PA_FP16, "bf16": N.PA_BF16, "fp8_e4m3": N.PA_FP8_E4M3}
+KV_DTYPES = {"fp16": N.PA_FP16, "bf16": N.PA_BF16, "fp8_e4m3": N.PA_FP8_E4M3,
+             "fp8_e4m3_block": N.PA_FP8_E4M3_BLOCK}
 _TORCH_OUT = {N.PA_FP16: torch.float16, N.PA_BF16: torch.bfloat16, N.PA_FP32: torch.float32}
 
 
@@ -50,7 +51,11 @@ class KVPool:
         self.handle = N.pa_pool_create(self.desc, self.k_cache.data_ptr(), self.v_cache.data_ptr())
         self.n_layers, self.num_blocks = n_layers, num_blocks
         self.n_kv_heads, self.head_dim = n_kv_heads, head_dim
-        self.elem_bytes = 1 if kv_dtype == "fp8_e4m3" else 2
+        self.elem_bytes = 1 if kv_dtype in ("fp8_e4m3", "fp8_e4m3_block") else 2
+        self.block_scaled = kv_dtype == "fp8_e4m3_block"
+        # bytes of one layer's tiles in each region (a block-scaled region ends
+        # with the scale table [n_layers][num_blocks][n_kv_heads] of fp32)
+        self.layer_bytes = num_blocks * n_kv_heads * 16 * head_dim * self.elem_bytes
         self.in_dtype = torch.float16 if kv_dtype == "fp16" else torch.bfloat16
         self.in_code = N.PA_FP16 if kv_dtype == "fp16" else N.PA_BF16
 
@@ -102,9 +107,19 @@ class KVPool:
     def layer_view(self, which: str, layer: int = 0) -> torch.Tensor:
         """uint8 view [num_blocks, n_kv_heads, 16, head_dim * elem_bytes] of one layer."""
         buf = self.k_cache if which == "k" else self.v_cache
-        per = buf.numel() // self.n_layers
+        per = self.layer_bytes
         return buf[layer * per:(layer + 1) * per].view(self.num_blocks, self.n_kv_heads, 16,
                                                          self.head_dim * self.elem_bytes)
+
+    def scale_view(self, which: str, layer: int = 0) -> torch.Tensor:
+        """float32 view [num_blocks, n_kv_heads] of one layer's K or V tile scales
+        (block-scaled FP8 pools)."""
+        if not self.block_scaled:
+            raise ValueError("only block-scaled FP8 pools keep per-tile scales")
+        buf = self.k_cache if which == "k" else self.v_cache
+        n = self.num_blocks * self.n_kv_heads * 4
+        off = self.n_layers * self.layer_bytes + layer * n
+        return buf[off:off + n].view(torch.float32).view(self.num_blocks, self.n_kv_heads)
 
     # --------------------------------------------------------- device calls
     def reshape_and_cache(self, k: torch.Tensor, v: torch.Tensor, slot_mapping: torch.Tensor,

@@ -88,9 +88,18 @@ def gpu_decode(w: W.Workload, pool: KVPool, q_bits, ctx=None, tables=None, out_d
     return out
 
 
-def vmax_of(w: W.Workload, opools) -> float:
+def vmax_of(w: W.Workload, opools, num_blocks=None) -> float:
     """max |V| over the values the oracle reads (dequantised for FP8)."""
     vp = opools[1]
+    if w.kv_dtype == "fp8_e4m3_block":
+        nb = num_blocks or w.num_blocks
+        n = oracle.tiles_bytes(w.kv_dtype, nb, 16, w.n_kv_heads, w.head_dim)
+        table = np.abs(oracle.e4m3_table())
+        table[np.isnan(table)] = 0
+        sc = oracle.tile_scales(w.kv_dtype, nb, 16, w.n_kv_heads, w.head_dim, vp).astype(np.float64)
+        sc[~np.isfinite(sc)] = 0
+        tile_max = table[vp[:n].reshape(nb, w.n_kv_heads, -1)].max(axis=2)
+        return float((tile_max * sc).max())
     if w.kv_dtype == "fp8_e4m3":
         table = np.abs(oracle.e4m3_table()) * w.v_scale
         table[np.isnan(table)] = 0
@@ -127,9 +136,18 @@ def pool_bytes_equal(pool: KVPool, opools, blocks=None):
     or the listed physical ids)."""
     for which, op in (("k", opools[0]), ("v", opools[1])):
         dev = pool.layer_view(which).cpu().numpy()
-        ref = op.reshape(dev.shape)
+        ref = op[:dev.size].reshape(dev.shape)
         if blocks is not None:
             dev, ref = dev[blocks], ref[blocks]
         if not np.array_equal(dev, ref):
             bad = np.argwhere(dev != ref)
             raise AssertionError(f"{which} pool differs at {len(bad)} bytes, first {bad[:4]}")
+        if pool.block_scaled:  # the tiles' scales, bit for bit
+            ds = pool.scale_view(which).cpu().numpy().view(np.uint32)
+            rs = oracle.tile_scales(pool.kv_dtype, pool.num_blocks, 16, pool.n_kv_heads,
+                                    pool.head_dim, op).view(np.uint32)
+            if blocks is not None:
+                ds, rs = ds[blocks], rs[blocks]
+            if not np.array_equal(ds, rs):
+                bad = np.argwhere(ds != rs)
+                raise AssertionError(f"{which} scales differ at {len(bad)} tiles, first {bad[:4]}")

@@ -64,6 +64,31 @@ def test_pool_bytes_and_budget(lib, layers, heads, d, dt):
     assert e.value.code == N.PA_ERR_NO_MEMORY
 
 
+@pytest.mark.parametrize("layers,heads,nb", [(1, 2, 7), (80, 8, 100), (3, 1, 5)])
+def test_block_scaled_pool_sizes(lib, layers, heads, nb):
+    """Block-scaled FP8: the tiles as for FP8, plus one fp32 scale per (layer,
+    block, kv head) at the end of each region, rounded up to 16 bytes; the
+    swap record carries the block's 2 * layers * heads scales, padded."""
+    d = 128
+    desc = N.make_desc(layers, nb, heads, d, N.PA_FP8_E4M3_BLOCK)
+    kb, vb = N.pa_pool_bytes(desc)
+    tiles = layers * nb * heads * 16 * d
+    table = -(-(layers * nb * heads * 4) // 16) * 16
+    assert kb == vb == tiles + table
+    assert N.pa_kv_bytes_per_token(layers, heads, d, N.PA_FP8_E4M3_BLOCK) == 2 * layers * heads * d
+    per_block = 2 * layers * heads * (16 * d + 4)
+    n = N.pa_pool_blocks_for_budget(desc, per_block * 9 + 64)
+    desc9 = N.make_desc(layers, n, heads, d, N.PA_FP8_E4M3_BLOCK)
+    assert sum(N.pa_pool_bytes(desc9)) <= per_block * 9 + 64
+    assert n in (8, 9)
+    h = N.pa_pool_create(desc, FAKE_K, FAKE_V)
+    try:
+        rec = N.pa_swap_block_bytes(h)
+        assert rec == 2 * layers * heads * 16 * d + -(-(2 * layers * heads * 4) // 16) * 16
+    finally:
+        N.pa_pool_destroy(h)
+
+
 def test_invalid_descriptions(lib):
     bad = [N.make_desc(1, 10, 2, 96, N.PA_FP16),            # head_dim
            N.make_desc(1, 10, 2, 64, N.PA_FP16, block_size=32),
