@@ -87,8 +87,9 @@ struct Cfg {
   // block-scaled pools: the (K, V) scales of the page in each stage
   static constexpr int kScaleBytes = kBlockScaled ? kStages * 8 : 0;
   static constexpr int kSmem = kDataBytes + 2 * kStages * 8 + kQBytes + kScaleBytes + kAlign;
-  // register budget, in CTAs per SM (16-bit pools: what their ring size allows)
-  static constexpr int kMinBlocks = kQInSmem ? 5 : (D == 128 ? 3 : 4);
+  // register budget, in CTAs per SM (16-bit pools: what their ring size allows;
+  // block-scaled FP8 spills at five, so it keeps four)
+  static constexpr int kMinBlocks = kBlockScaled ? 4 : (kQInSmem ? 5 : (D == 128 ? 3 : 4));
   static constexpr bool kMmaBf16 = (KV == KV_BF16);
   static_assert(kStageBytes % kAlign == 0 || !kSwizzle, "tiles must stay 1 KiB aligned");
 };
@@ -199,39 +200,24 @@ __global__ void __launch_bounds__(kThreads, (Cfg<KV, D>::kMinBlocks)) decode_ker
     // base + i.  The next 32 entries are loaded as soon as a batch starts and
     // checked, and their scales fetched, a few pages into it, so no load sits
     // on the path between two batches.
-    auto checked = [&](int raw, int idx) {
-      if (idx < n_local && (raw < 0 || raw >= a.num_blocks)) {
-        record_error(a.err, PA_ERR_BOUNDS);
-        return 0;
-      }
-      return raw;
-    };
-    int phys = checked(lane < n_local ? trow[lane] : 0, lane);
-    float sk = 0.f, sv = 0.f;
-    if constexpr (BLK) {
-      if (lane < n_local) {
-        sk = a.ksc[(size_t)phys * a.Hkv + h];
-        sv = a.vsc[(size_t)phys * a.Hkv + h];
-      }
-    }
     int issued = 0;
     bool abort = false;
     for (int base = 0; base < n_local && !abort; base += 32) {
-      const int nidx = base + 32 + lane;
-      int phys_next = nidx < n_local ? trow[nidx] : 0;
-      float sk_next = 0.f, sv_next = 0.f;
-      const int cnt = min(32, n_local - base);
-      const int fetch_at = min(cnt - 1, 3);
-      for (int j = 0; j < cnt; ++j) {
-        if (j == fetch_at) {
-          phys_next = checked(phys_next, nidx);
-          if constexpr (BLK) {
-            if (nidx < n_local) {
-              sk_next = a.ksc[(size_t)phys_next * a.Hkv + h];
-              sv_next = a.vsc[(size_t)phys_next * a.Hkv + h];
-            }
-          }
+      int phys = 0;
+      float sk = 0.f, sv = 0.f;
+      if (base + lane < n_local) {
+        phys = trow[base + lane];
+        if (phys < 0 || phys >= a.num_blocks) {
+          record_error(a.err, PA_ERR_BOUNDS);
+          phys = 0;
         }
+        if constexpr (BLK) {
+          sk = a.ksc[(size_t)phys * a.Hkv + h];
+          sv = a.vsc[(size_t)phys * a.Hkv + h];
+        }
+      }
+      const int cnt = min(32, n_local - base);
+      for (int j = 0; j < cnt; ++j) {
         const int ph = __shfl_sync(kFull, phys, j);
         float skj = 0.f, svj = 0.f;
         if constexpr (BLK) {
@@ -260,9 +246,6 @@ __global__ void __launch_bounds__(kThreads, (Cfg<KV, D>::kMinBlocks)) decode_ker
           break;
         }
       }
-      phys = phys_next;
-      sk = sk_next;
-      sv = sv_next;
     }
     // Wait (bounded) until every copy this CTA issued has landed, so no bulk
     // write can still target the ring when it is reused or the CTA exits.
