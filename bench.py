@@ -668,14 +668,16 @@ def run_prefill(args, rank, world, local_rank):
         "metric": PREFILL_METRIC, "value": round(world * flops * K / t_max / 1e12, 2),
         "unit": "TFLOP/s", "n_gpus": world, "steps": K, "warmup": args.warmup,
         "ms_per_step": round(t_max / K * 1e3, 4), "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "e4m3 KV / f16 tensor-core MMA / f32 accumulate",
+        "vs_baseline": None,
+        "dtype": "e4m3 KV; tcgen05 MMA: e4m3 x e4m3 (Q K^T, q as two e4m3 terms) and f16 x f16 (P V); "
+                 "f32 accumulate in tensor memory",
         "data": "synthetic (seeded N(0,1) q/k/v, random block tables)",
         "config": {"workload": DESCRIPTION[name], "tokens_per_step": T,
                    "flops_per_step": flops, "parallelism": "1 GPU" if world == 1 else
                    f"replicas x{world}"},
         "prefill_ms_median": round(statistics.median(pre_ms), 4),
         "tokens_per_s": round(world * T * K / t_max, 1),
-        "roofline": {"kernel": "prefill_kernel", "bound": "tensor", "achieved": round(achieved, 1),
+        "roofline": {"kernel": "prefill_tc_kernel (tcgen05)", "bound": "tensor", "achieved": round(achieved, 1),
                      "peak": peak, "peak_kind": peak_kind, "unit": "TFLOP/s",
                      "frac": round(achieved / peak, 4), "traffic": None,
                      "algorithmic_flops_per_step": flops},

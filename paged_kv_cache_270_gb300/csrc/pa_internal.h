@@ -70,4 +70,12 @@ namespace pa {
 // one 16-token tile, 128-byte swizzled when a row is 128 or 256 bytes.
 int layer_maps(pa_pool* pool, int layer, const CUtensorMap_st** tk, const CUtensorMap_st** tv);
 
+// Chunked prefill on the tcgen05 tensor cores, for the shapes it covers (FP8
+// pools, head_dim 128, 8 query heads per KV head, bf16 or fp32 output); the
+// arguments are those of pa_prefill, already validated.
+bool prefill_tc_supported(const pa_pool* pool, int n_q_heads, int out_dtype);
+int prefill_tc(pa_pool* pool, int layer, void* out, int out_dtype, const void* q, const int32_t* q_start,
+               const int32_t* tables, int max_blocks, const int32_t* ctx, int S, int n_q_heads,
+               int max_chunk, float softmax_scale, unsigned int* err, struct CUstream_st* st);
+
 }  // namespace pa

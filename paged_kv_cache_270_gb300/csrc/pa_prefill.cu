@@ -586,6 +586,10 @@ int pa_prefill(pa_pool* pool, int layer, void* out, int out_dtype, const void* q
   if (((uintptr_t)out | (uintptr_t)q) & 15u) return fail(PA_ERR_INVALID, "q and out must be 16-byte aligned");
   unsigned int* err = device_error_word();
   if (!err) return PA_ERR_CUDA;
+  if (prefill_tc_supported(pool, n_q_heads, out_dtype))
+    return prefill_tc(pool, layer, out, out_dtype, q, q_start_dev, block_tables_dev, max_blocks_per_seq,
+                      ctx_lens_dev, S, n_q_heads, max_chunk, softmax_scale, err,
+                      static_cast<cudaStream_t>(stream));
   PDispatch disp = ppick(d.kv_dtype, d.head_dim, out_dtype);
   if (!pconfigure(*disp.info)) return fail(PA_ERR_CUDA, "prefill kernel configuration failed");
   const CUtensorMap_st *tk = nullptr, *tv = nullptr;

@@ -1,0 +1,630 @@
+// pa_prefill_tc.cu -- chunked prefill over an FP8 paged KV cache on the
+// fifth-generation tensor cores (tcgen05 MMA, accumulators in tensor memory).
+//
+// Same operation as pa_prefill.cu: a chunk of new tokens per sequence, already
+// in the cache, attends causally to the sequence's pages ("Optimización de KV
+// Cache con PagedAttention y Cuantización FP8 para Contextos Largos (128K)",
+// sections 5 and 6.3: prefill in packets interleaved with decode; "Capítulo 8
+// -- Gestión de caché KV de nueva generación", section 8.1: pages gathered
+// through the block table).  This kernel takes the shapes where a CTA's rows
+// fill a 128-row MMA: head_dim 128 and 8 query heads per KV head (16 query
+// tokens x 8 heads), FP8 E4M3 pages with a per-tensor or per-tile scale.
+//
+// Design (the pages give none):
+//  * grid = (16-token query tile, kv head, sequence), longest tiles first; one
+//    CTA per SM (about 200 KB of shared memory, 384 of the 512 TMEM columns).
+//  * warp 0 streams the K and V pages of 128-key blocks (8 pages) with TMA into
+//    a two-block ring; the K pages land 128-byte swizzled, back to back, which
+//    is exactly the K-major operand layout of the MMA, so S = Q K^T reads them
+//    in place (kind::f8f6f4, M = N = 128, fp32 accumulate in TMEM).
+//  * Q is FP8 too: each bf16 query row is scaled by a power of two and split
+//    into two E4M3 terms, hi = E4M3(x) and lo = E4M3(x - hi); their sum
+//    carries the row's 8 significant bits, so S = hi K^T + lo K^T (two MMA
+//    passes into one accumulator) is exact up to fp32 accumulation order.
+//  * warps 2-3 convert each V block to binary16 (exact), laid out 128-byte
+//    swizzled with the head dim contiguous, which the MMA reads as its B
+//    operand in MN-major form: O += P V is kind::f16 with P in binary16 (plus
+//    a second pass with P's low part in the fp32-output mode).
+//  * warps 4-7 run the online softmax, one thread per row: S comes out of
+//    TMEM, the max moves only when it grows by more than 2^8 (so P <= 2^8),
+//    and then the thread rescales its own O row in TMEM before the next P V.
+//  * warp 1 allocates TMEM and one lane issues every MMA; completion is
+//    signalled through mbarriers (tcgen05.commit).  Every wait is bounded: a
+//    timeout records PA_ERR_TIMEOUT, raises a CTA-wide abort flag that ends
+//    every role's loop, and the CTA drains its MMAs and copies before it frees
+//    TMEM and exits.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cmath>
+#include <mutex>
+
+#include "pa_device.cuh"
+
+namespace pa {
+namespace {
+
+constexpr int kD = 128;         // head dim
+constexpr int kG = 8;           // query heads per kv head
+constexpr int kThreads = 256;   // 8 warps
+constexpr unsigned kAll = 0xffffffffu;
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kOCol = 256;  // TMEM columns: S buffers at 0 and 128, O at 256
+
+// shared memory, from a 1024-byte aligned base
+constexpr int kQHi = 0;               // [128 rows][128 B] E4M3, swizzled
+constexpr int kQLo = kQHi + 16384;
+constexpr int kKRing = kQLo + 16384;  // [2][8 pages][16 keys][128 B] E4M3 (TMA, swizzled)
+constexpr int kVRing = kKRing + 32768;
+constexpr int kVT = kVRing + 32768;   // [2][2 dim blocks][128 keys][128 B] binary16, swizzled
+constexpr int kP = kVT + 65536;       // [2 key blocks][128 rows][128 B] binary16, swizzled
+constexpr int kPLo = kP + 32768;
+__host__ __device__ constexpr int data_bytes(bool psplit) { return psplit ? kPLo + 32768 : kPLo; }
+
+struct Ctrl {
+  uint64_t kv_full[2], kv_empty[2], s_full[2], s_empty[2], vt_full[2], vt_empty[2];
+  uint64_t sc_full[2], sc_empty[2], p_full, o_done, drain;
+  float2 sc[2][8];  // block-scaled pools: (K scale, V scale) of each page of a ring block
+  uint32_t tmem;
+  int abort;
+};
+constexpr int smem_bytes(bool psplit) { return 1024 + data_bytes(psplit) + (int)sizeof(Ctrl); }
+static_assert(smem_bytes(true) <= 232448, "shared memory budget");
+
+struct TcArgs {
+  const uint16_t* q;
+  void* out;
+  const int32_t* q_start;
+  const int32_t* ctx;
+  const int32_t* tables;
+  const float* ksc;  // block-scaled pools: this layer's scales [num_blocks][Hkv]
+  const float* vsc;
+  int max_blocks, Hq, Hkv, num_blocks;
+  float qk_scale_log2;  // softmax_scale * log2(e) (* k_scale for a static FP8 pool)
+  float v_scale;        // static FP8 pool's V scale (1 for block-scaled pools)
+  unsigned int* err;
+};
+
+// ---------------------------------------------------------------- tcgen05
+// Shared-memory matrix descriptor, 128-byte swizzle: start address, leading
+// and stride byte offsets (>> 4), descriptor version 1, layout SWIZZLE_128B.
+__device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+  return (uint64_t)((saddr & 0x3FFFFu) >> 4) | ((uint64_t)((lbo >> 4) & 0x3FFFu) << 16) |
+         ((uint64_t)((sbo >> 4) & 0x3FFFu) << 32) | ((uint64_t)1 << 46) | ((uint64_t)2 << 61);
+}
+// K-major operand: rows of 128 bytes, 8-row groups 1024 bytes apart.
+__device__ __forceinline__ uint64_t kmajor(uint32_t saddr) { return sw128_desc(saddr, 16, 1024); }
+// MN-major operand: 64-element blocks of the MN dim 16 KiB apart, 8 K-rows 1024 bytes apart.
+__device__ __forceinline__ uint64_t mnmajor(uint32_t saddr) { return sw128_desc(saddr, 16384, 1024); }
+
+// Instruction descriptors: fp32 accumulate, M = N = 128; S = E4M3 x E4M3 with
+// both operands K-major; O = binary16 x binary16 with B MN-major.
+constexpr uint32_t kIdescQK = (1u << 4) | ((128u >> 3) << 17) | ((128u >> 4) << 24);
+constexpr uint32_t kIdescPV = (1u << 4) | (1u << 16) | ((128u >> 3) << 17) | ((128u >> 4) << 24);
+
+__device__ __forceinline__ void mma_f8(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
+  asm volatile("{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+               "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}"
+               ::"r"(d), "l"(a), "l"(b), "r"(idesc), "r"(acc) : "memory");
+}
+__device__ __forceinline__ void mma_f16(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
+  asm volatile("{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+               "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}"
+               ::"r"(d), "l"(a), "l"(b), "r"(idesc), "r"(acc) : "memory");
+}
+// The mbarrier gets one arrival once every MMA this thread issued so far is done.
+__device__ __forceinline__ void mma_commit(uint64_t* bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];"
+               ::"r"(smem_addr(bar)) : "memory");
+}
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void fence_proxy_async() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
+
+// 32 consecutive fp32 columns of this thread's TMEM lane (warp-collective).
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, float* v) {
+  uint32_t r[32];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,"
+      "%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+        "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]),
+        "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]),
+        "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr));
+#pragma unroll
+  for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+}
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const float* v) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,"
+      "%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};"
+      ::"r"(taddr), "r"(__float_as_uint(v[0])), "r"(__float_as_uint(v[1])), "r"(__float_as_uint(v[2])),
+        "r"(__float_as_uint(v[3])), "r"(__float_as_uint(v[4])), "r"(__float_as_uint(v[5])),
+        "r"(__float_as_uint(v[6])), "r"(__float_as_uint(v[7])), "r"(__float_as_uint(v[8])),
+        "r"(__float_as_uint(v[9])), "r"(__float_as_uint(v[10])), "r"(__float_as_uint(v[11])),
+        "r"(__float_as_uint(v[12])), "r"(__float_as_uint(v[13])), "r"(__float_as_uint(v[14])),
+        "r"(__float_as_uint(v[15])), "r"(__float_as_uint(v[16])), "r"(__float_as_uint(v[17])),
+        "r"(__float_as_uint(v[18])), "r"(__float_as_uint(v[19])), "r"(__float_as_uint(v[20])),
+        "r"(__float_as_uint(v[21])), "r"(__float_as_uint(v[22])), "r"(__float_as_uint(v[23])),
+        "r"(__float_as_uint(v[24])), "r"(__float_as_uint(v[25])), "r"(__float_as_uint(v[26])),
+        "r"(__float_as_uint(v[27])), "r"(__float_as_uint(v[28])), "r"(__float_as_uint(v[29])),
+        "r"(__float_as_uint(v[30])), "r"(__float_as_uint(v[31]))
+      : "memory");
+}
+__device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+__device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
+
+// Bounded wait that also gives up as soon as another role has aborted.
+__device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
+                                              unsigned int* err) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = global_ns();
+  while (!mbar_try_wait(bar, parity)) {
+    if (*abort_flag) return false;
+    if (global_ns() - t0 > kWaitLimitNs) {
+      *abort_flag = 1;
+      record_error(err, PA_ERR_TIMEOUT);
+      return false;
+    }
+  }
+  return true;
+}
+
+template <int OUT>
+__device__ __forceinline__ void store_row32(void* out, size_t idx, const float* v, float s) {
+  if constexpr (OUT == PA_FP32) {
+    float4* o = reinterpret_cast<float4*>(static_cast<float*>(out) + idx);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) o[i] = make_float4(v[4 * i] * s, v[4 * i + 1] * s, v[4 * i + 2] * s, v[4 * i + 3] * s);
+  } else {
+    uint4* o = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(out) + idx);
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+      o[i] = make_uint4(pack2<true>(v[8 * i] * s, v[8 * i + 1] * s), pack2<true>(v[8 * i + 2] * s, v[8 * i + 3] * s),
+                        pack2<true>(v[8 * i + 4] * s, v[8 * i + 5] * s), pack2<true>(v[8 * i + 6] * s, v[8 * i + 7] * s));
+  }
+}
+
+template <bool BLK, int OUT, bool PSPLIT>
+__global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const TcArgs a,
+                                                                  const __grid_constant__ CUtensorMap tmk,
+                                                                  const __grid_constant__ CUtensorMap tmv) {
+  extern __shared__ __align__(16) uint8_t smem_raw[];
+  uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  Ctrl* ctl = reinterpret_cast<Ctrl*>(sm + data_bytes(PSPLIT));
+  volatile int* abort_flag = &ctl->abort;
+
+  const int qt = gridDim.x - 1 - blockIdx.x, h = blockIdx.y, seq = blockIdx.z;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int q0 = a.q_start[seq];
+  const int Cn = a.q_start[seq + 1] - q0;
+  const int tok_lo = 16 * qt;
+  if (tok_lo >= Cn) return;
+  const int ctx = a.ctx[seq];
+  if (Cn < 0 || ctx < Cn || ctx > a.max_blocks * 16) {
+    if (threadIdx.x == 0) record_error(a.err, PA_ERR_BOUNDS);
+    return;
+  }
+  const int n_tok = min(16, Cn - tok_lo);
+  const int pos0 = ctx - Cn + tok_lo;  // position of the tile's first query
+  const int pos_last = pos0 + n_tok - 1;
+  const int npages = pos_last / 16 + 1;
+  const int nblk = (npages + 7) / 8;
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&ctl->kv_full[i], 1);
+      mbar_init(&ctl->kv_empty[i], 3);  // the QK MMAs' commit + the two converter warps
+      mbar_init(&ctl->s_full[i], 1);
+      mbar_init(&ctl->s_empty[i], 4);
+      mbar_init(&ctl->vt_full[i], 2);
+      mbar_init(&ctl->vt_empty[i], 1);
+      mbar_init(&ctl->sc_full[i], 1);
+      mbar_init(&ctl->sc_empty[i], 4);
+    }
+    mbar_init(&ctl->p_full, 4);
+    mbar_init(&ctl->o_done, 1);
+    mbar_init(&ctl->drain, 1);
+    ctl->abort = 0;
+    fence_barrier_init();
+  }
+  if (warp == 0 && lane == 0) {
+    prefetch_tensormap(&tmk);
+    prefetch_tensormap(&tmv);
+  }
+  if (warp == 1) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;"
+                 ::"r"(smem_addr(&ctl->tmem)), "r"(kTmemCols) : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+
+  // Softmax rows: r = 8 * (query token) + head; Q rows go to shared memory as
+  // two E4M3 terms after a power-of-two scaling that puts max |q| in [128, 256).
+  const int r = threadIdx.x - 128;
+  const int tl = r >> 3, hh = r & 7;
+  const bool row_valid = warp >= 4 && tl < n_tok;
+  float row_scale = a.qk_scale_log2;
+  if (warp >= 4) {
+    uint32_t qw[64];  // the row's 128 bfloat16 values, two per word
+    const uint4* src = reinterpret_cast<const uint4*>(
+        a.q + ((size_t)(q0 + tok_lo + tl) * a.Hq + (size_t)h * kG + hh) * kD);
+#pragma unroll
+    for (int c = 0; c < 16; ++c) {
+      const uint4 v = row_valid ? src[c] : make_uint4(0, 0, 0, 0);
+      qw[4 * c] = v.x;
+      qw[4 * c + 1] = v.y;
+      qw[4 * c + 2] = v.z;
+      qw[4 * c + 3] = v.w;
+    }
+    float amax = 0.f;
+#pragma unroll
+    for (int w = 0; w < 64; ++w)
+      amax = fmaxf(amax, fmaxf(fabsf(bf16_bits_to_float(qw[w] & 0xFFFFu)), fabsf(bf16_bits_to_float(qw[w] >> 16))));
+    int ex = 0;
+    if (amax > 0.f) frexpf(amax, &ex);
+    const float qs = amax > 0.f ? ldexpf(1.f, 8 - ex) : 1.f;
+    if (amax > 0.f) row_scale = a.qk_scale_log2 * ldexpf(1.f, ex - 8);
+#pragma unroll
+    for (int c = 0; c < 8; ++c) {  // 16 dims per 16-byte chunk of E4M3 codes
+      uint32_t hi[4], lo[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const uint32_t w0 = qw[8 * c + 2 * i], w1 = qw[8 * c + 2 * i + 1];
+        // dims 16c + 4i .. 16c + 4i + 3: (w0 lo, w0 hi, w1 lo, w1 hi)
+        const float2 x01 = make_float2(bf16_bits_to_float(w0 & 0xFFFFu) * qs, bf16_bits_to_float(w0 >> 16) * qs);
+        const float2 x23 = make_float2(bf16_bits_to_float(w1 & 0xFFFFu) * qs, bf16_bits_to_float(w1 >> 16) * qs);
+        const uint32_t h01 = __nv_cvt_float2_to_fp8x2(x01, __NV_SATFINITE, __NV_E4M3);
+        const uint32_t h23 = __nv_cvt_float2_to_fp8x2(x23, __NV_SATFINITE, __NV_E4M3);
+        const float2 d01 = unpack2<false>(e4m3x2_to_f16x2(h01));
+        const float2 d23 = unpack2<false>(e4m3x2_to_f16x2(h23));
+        const uint32_t l01 = __nv_cvt_float2_to_fp8x2(make_float2(x01.x - d01.x, x01.y - d01.y), __NV_SATFINITE, __NV_E4M3);
+        const uint32_t l23 = __nv_cvt_float2_to_fp8x2(make_float2(x23.x - d23.x, x23.y - d23.y), __NV_SATFINITE, __NV_E4M3);
+        hi[i] = (h01 & 0xFFFFu) | (h23 << 16);
+        lo[i] = (l01 & 0xFFFFu) | (l23 << 16);
+      }
+      const uint32_t off = r * 128 + ((c ^ (r & 7)) << 4);
+      *reinterpret_cast<uint4*>(sm + kQHi + off) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+      *reinterpret_cast<uint4*>(sm + kQLo + off) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+    }
+    fence_proxy_async();  // the MMA reads Q through the async proxy
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = ctl->tmem;
+
+  if (warp == 0) {
+    // ---------------------------------------------------------- TMA producer
+    const int32_t* trow = a.tables + (size_t)seq * a.max_blocks;
+    const uint64_t policy = l2_evict_first_policy();
+    int issued = 0;
+    for (int j = 0; j < nblk; ++j) {
+      const int half = j & 1, u = j >> 1;
+      if (j >= 2 && !__all_sync(kAll, wait_or_abort(&ctl->kv_empty[half], (u - 1) & 1, abort_flag, a.err))) break;
+      const int cnt = min(8, npages - 8 * j);
+      int phys = 0;
+      float sk = 1.f, sv = 0.f;
+      if (lane < cnt) {
+        phys = trow[8 * j + lane];
+        if (phys < 0 || phys >= a.num_blocks) {
+          record_error(a.err, PA_ERR_BOUNDS);
+          phys = 0;
+        }
+        if constexpr (BLK) {
+          sk = a.ksc[(size_t)phys * a.Hkv + h];
+          sv = a.vsc[(size_t)phys * a.Hkv + h];
+        }
+      }
+      if constexpr (BLK) {
+        if (j >= 2 && !__all_sync(kAll, wait_or_abort(&ctl->sc_empty[half], (u - 1) & 1, abort_flag, a.err))) break;
+        float2 v[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) v[i] = make_float2(__shfl_sync(kAll, sk, i), __shfl_sync(kAll, sv, i));
+        if (lane == 0) {
+#pragma unroll
+          for (int i = 0; i < 8; ++i) ctl->sc[half][i] = v[i];
+          mbar_arrive(&ctl->sc_full[half]);
+        }
+      }
+      if (lane == 0) mbar_arrive_expect_tx(&ctl->kv_full[half], (uint32_t)cnt * 4096u);
+      for (int i = 0; i < cnt; ++i) {
+        const int ph = __shfl_sync(kAll, phys, i);
+        if (lane == 0) {
+          const int row0 = (ph * a.Hkv + h) * 16;
+          tma_load_2d(sm + kKRing + half * 16384 + i * 2048, &tmk, 0, row0, &ctl->kv_full[half], policy);
+          tma_load_2d(sm + kVRing + half * 16384 + i * 2048, &tmv, 0, row0, &ctl->kv_full[half], policy);
+        }
+      }
+      ++issued;
+    }
+    // no copy may still target shared memory when the CTA exits
+    if (lane == 0)
+      for (int j = max(0, issued - 2); j < issued; ++j)
+        if (!mbar_wait(&ctl->kv_full[j & 1], (j >> 1) & 1)) record_error(a.err, PA_ERR_TIMEOUT);
+  } else if (warp == 1) {
+    // ---------------------------------------------------------- MMA issue
+    if (lane == 0) {
+      const uint32_t qhi = smem_addr(sm + kQHi), qlo = smem_addr(sm + kQLo);
+      for (int j = 0; j <= nblk; ++j) {
+        if (j < nblk) {  // S(j) = Q K(j)^T, after the softmax has read S(j - 2)
+          const int sb = j & 1, u = j >> 1;
+          if (!wait_or_abort(&ctl->kv_full[sb], u & 1, abort_flag, a.err)) break;
+          if (j >= 2 && !wait_or_abort(&ctl->s_empty[sb], (u - 1) & 1, abort_flag, a.err)) break;
+          tc_fence_after();
+          const uint32_t kb = smem_addr(sm + kKRing + sb * 16384);
+#pragma unroll
+          for (int t = 0; t < 2; ++t)
+#pragma unroll
+            for (int k = 0; k < 4; ++k)
+              mma_f8(tmem + sb * 128, kmajor((t ? qlo : qhi) + 32 * k), kmajor(kb + 32 * k), kIdescQK,
+                     (uint32_t)(t | k));
+          mma_commit(&ctl->s_full[sb]);
+          mma_commit(&ctl->kv_empty[sb]);
+        }
+        if (j >= 1) {  // O += P(i) V(i), i = j - 1, once P is written and V converted
+          const int i = j - 1, vb = i & 1;
+          if (!wait_or_abort(&ctl->p_full, i & 1, abort_flag, a.err)) break;
+          if (!wait_or_abort(&ctl->vt_full[vb], (i >> 1) & 1, abort_flag, a.err)) break;
+          tc_fence_after();
+          const uint32_t vt = smem_addr(sm + kVT + vb * 32768);
+#pragma unroll
+          for (int part = 0; part < (PSPLIT ? 2 : 1); ++part) {
+            const uint32_t pb = smem_addr(sm + (part ? kPLo : kP));
+#pragma unroll
+            for (int k = 0; k < 8; ++k)
+              mma_f16(tmem + kOCol, kmajor(pb + (k >> 2) * 16384 + (k & 3) * 32), mnmajor(vt + k * 2048),
+                      kIdescPV, (uint32_t)(i | k | part));
+          }
+          mma_commit(&ctl->o_done);
+          mma_commit(&ctl->vt_empty[vb]);
+        }
+      }
+      // every MMA issued above has finished before TMEM is released
+      mma_commit(&ctl->drain);
+      if (!mbar_wait(&ctl->drain, 0)) record_error(a.err, PA_ERR_TIMEOUT);
+    }
+    __syncwarp();
+  } else if (warp < 4) {
+    // ---------------------------------------------------------- V to binary16
+    const int ct = threadIdx.x - 64;
+    for (int j = 0; j < nblk; ++j) {
+      const int half = j & 1, u = j >> 1;
+      if (!__all_sync(kAll, wait_or_abort(&ctl->kv_full[half], u & 1, abort_flag, a.err))) break;
+      if (j >= 2 && !__all_sync(kAll, wait_or_abort(&ctl->vt_empty[half], (u - 1) & 1, abort_flag, a.err))) break;
+      const int nvalid = min(128, pos_last + 1 - 128 * j);  // keys past the last query: zero
+      const uint8_t* vr = sm + kVRing + half * 16384;
+      uint8_t* vt = sm + kVT + half * 32768;
+#pragma unroll 4
+      for (int it = 0; it < 16; ++it) {
+        const int idx = ct + 64 * it, key = idx >> 3, ch = idx & 7;
+        uint4 w = make_uint4(0, 0, 0, 0);
+        if (key < nvalid) w = lds128(vr + (key >> 4) * 2048 + (key & 15) * 128 + ((ch ^ (key & 7)) << 4));
+        const uint32_t cw[4] = {w.x, w.y, w.z, w.w};
+        uint32_t hv[8];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          hv[2 * q] = e4m3x2_to_f16x2(cw[q]);
+          hv[2 * q + 1] = e4m3x2_to_f16x2(cw[q] >> 16);
+        }
+        uint8_t* row = vt + (ch >> 2) * 16384 + key * 128;
+        const int c0 = (ch & 3) * 2;
+        *reinterpret_cast<uint4*>(row + ((c0 ^ (key & 7)) << 4)) = make_uint4(hv[0], hv[1], hv[2], hv[3]);
+        *reinterpret_cast<uint4*>(row + (((c0 + 1) ^ (key & 7)) << 4)) = make_uint4(hv[4], hv[5], hv[6], hv[7]);
+      }
+      fence_proxy_async();
+      __syncwarp();
+      if (lane == 0) {
+        mbar_arrive(&ctl->vt_full[half]);
+        mbar_arrive(&ctl->kv_empty[half]);
+      }
+    }
+  } else {
+    // ---------------------------------------------------------- softmax rows
+    const uint32_t trow = tmem + ((uint32_t)((warp & 3) * 32) << 16);
+    const int qp = pos0 + min(tl, n_tok - 1);  // causal limit of the row
+    float m = -INFINITY, l = 0.f, vref = 0.f;
+    bool ok = true;
+    float x[128];
+    for (int j = 0; j < nblk; ++j) {
+      const int sb = j & 1, u = j >> 1;
+      float2 psc[8];
+      if constexpr (BLK) {
+        ok = __all_sync(kAll, wait_or_abort(&ctl->sc_full[sb], u & 1, abort_flag, a.err));
+        if (!ok) break;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) psc[i] = ctl->sc[sb][i];
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&ctl->sc_empty[sb]);
+      }
+      ok = __all_sync(kAll, wait_or_abort(&ctl->s_full[sb], u & 1, abort_flag, a.err));
+      if (!ok) break;
+      tc_fence_after();
+#pragma unroll
+      for (int c = 0; c < 4; ++c) tmem_ld32(trow + sb * 128 + 32 * c, x + 32 * c);
+      tmem_wait_ld();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&ctl->s_empty[sb]);
+
+      // scores in log2 units, causal mask, block max
+      const int key0 = 128 * j;
+      float mx = -INFINITY;
+#pragma unroll
+      for (int c = 0; c < 128; ++c) {
+        const float f = BLK ? row_scale * psc[c >> 4].x : row_scale;
+        const float v = (key0 + c > qp) ? -INFINITY : x[c] * f;
+        x[c] = v;
+        mx = fmaxf(mx, v);
+      }
+      float ov = 1.f;  // factor for this row's O accumulator
+      if (mx > m + 8.f) {  // the first visible block, or a max that grew by more than 2^8
+        const float alpha = fast_exp2(m - mx);
+        l *= alpha;
+        ov = alpha;
+        m = mx;
+      }
+      float vmul[8];
+      if constexpr (BLK) {  // V weights relative to the largest V scale seen (<= 1)
+        float vb = vref;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) vb = fmaxf(vb, psc[i].y);
+        if (vb > vref) {
+          ov *= vref / vb;
+          vref = vb;
+        }
+        const float inv = vref > 0.f ? 1.f / vref : 0.f;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) vmul[i] = psc[i].y * inv;
+      }
+      float rs = 0.f;
+#pragma unroll
+      for (int c = 0; c < 128; ++c) {
+        const float p = fast_exp2(x[c] - m);
+        rs += p;
+        x[c] = BLK ? p * vmul[c >> 4] : p;
+      }
+      l += rs;
+
+      // P V of the previous block is done: P may be overwritten, O rescaled
+      if (j > 0) {
+        ok = __all_sync(kAll, wait_or_abort(&ctl->o_done, (j - 1) & 1, abort_flag, a.err));
+        if (!ok) break;
+        tc_fence_after();
+        if (__any_sync(kAll, ov != 1.f)) {
+#pragma unroll
+          for (int c = 0; c < 4; ++c) {
+            float o[32];
+            tmem_ld32(trow + kOCol + 32 * c, o);
+            tmem_wait_ld();
+#pragma unroll
+            for (int e = 0; e < 32; ++e) o[e] *= ov;
+            tmem_st32(trow + kOCol + 32 * c, o);
+          }
+          tmem_wait_st();
+        }
+      }
+      // P row: 16 chunks of 8 keys, binary16 (and the low part in fp32 mode)
+#pragma unroll
+      for (int cc = 0; cc < 16; ++cc) {
+        uint32_t ph[4], pl[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          ph[e] = pack2<false>(x[8 * cc + 2 * e], x[8 * cc + 2 * e + 1]);
+          if constexpr (PSPLIT) {
+            const float2 hv = unpack2<false>(ph[e]);
+            pl[e] = pack2<false>(x[8 * cc + 2 * e] - hv.x, x[8 * cc + 2 * e + 1] - hv.y);
+          }
+        }
+        const uint32_t off = (cc >> 3) * 16384 + r * 128 + (((cc & 7) ^ (r & 7)) << 4);
+        *reinterpret_cast<uint4*>(sm + kP + off) = make_uint4(ph[0], ph[1], ph[2], ph[3]);
+        if constexpr (PSPLIT) *reinterpret_cast<uint4*>(sm + kPLo + off) = make_uint4(pl[0], pl[1], pl[2], pl[3]);
+      }
+      fence_proxy_async();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&ctl->p_full);
+    }
+    // output rows: O / l (times the V scale)
+    if (ok) ok = __all_sync(kAll, wait_or_abort(&ctl->o_done, (nblk - 1) & 1, abort_flag, a.err));
+    if (ok) {
+      tc_fence_after();
+      const float s = l > 0.f ? (BLK ? vref : a.v_scale) / l : 0.f;
+      const size_t orow = ((size_t)(q0 + tok_lo + tl) * a.Hq + (size_t)h * kG + hh) * kD;
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        float o[32];
+        tmem_ld32(trow + kOCol + 32 * c, o);
+        tmem_wait_ld();
+        if (row_valid) store_row32<OUT>(a.out, orow + 32 * c, o, s);
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTmemCols) : "memory");
+  }
+}
+
+struct TcInfo {
+  const void* fn;
+  int smem;
+  bool configured[128];
+};
+
+template <bool BLK, int OUT, bool PSPLIT>
+TcInfo& tc_info() {
+  static TcInfo ti = {reinterpret_cast<const void*>(&prefill_tc_kernel<BLK, OUT, PSPLIT>), smem_bytes(PSPLIT), {}};
+  return ti;
+}
+
+template <bool BLK, int OUT, bool PSPLIT>
+cudaError_t tc_launch(const TcArgs& a, const CUtensorMap* tk, const CUtensorMap* tv, int tiles, int S,
+                      cudaStream_t st) {
+  static std::mutex mu;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  TcInfo& ti = tc_info<BLK, OUT, PSPLIT>();
+  {
+    std::lock_guard<std::mutex> lock(mu);
+    if (dev < 0 || dev >= 128) return cudaErrorInvalidDevice;
+    if (!ti.configured[dev]) {
+      e = cudaFuncSetAttribute(ti.fn, cudaFuncAttributeMaxDynamicSharedMemorySize, ti.smem);
+      if (e != cudaSuccess) return e;
+      ti.configured[dev] = true;
+    }
+  }
+  prefill_tc_kernel<BLK, OUT, PSPLIT><<<dim3(tiles, a.Hkv, S), kThreads, ti.smem, st>>>(a, *tk, *tv);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+bool prefill_tc_supported(const pa_pool* pool, int n_q_heads, int out_dtype) {
+  const pa_pool_desc& d = pool->desc;
+  return (d.kv_dtype == PA_FP8_E4M3 || d.kv_dtype == PA_FP8_E4M3_BLOCK) && d.head_dim == kD &&
+         n_q_heads == kG * d.n_kv_heads && (out_dtype == PA_BF16 || out_dtype == PA_FP32);
+}
+
+int prefill_tc(pa_pool* pool, int layer, void* out, int out_dtype, const void* q, const int32_t* q_start,
+               const int32_t* tables, int max_blocks, const int32_t* ctx, int S, int n_q_heads,
+               int max_chunk, float softmax_scale, unsigned int* err, cudaStream_t st) {
+  const pa_pool_desc& d = pool->desc;
+  const CUtensorMap_st *tk = nullptr, *tv = nullptr;
+  int rc = layer_maps(pool, layer, &tk, &tv);
+  if (rc) return rc;
+  TcArgs a;
+  a.q = static_cast<const uint16_t*>(q);
+  a.out = out;
+  a.q_start = q_start;
+  a.ctx = ctx;
+  a.tables = tables;
+  a.ksc = pool->block_scaled ? layer_scales(pool, pool->k, layer) : nullptr;
+  a.vsc = pool->block_scaled ? layer_scales(pool, pool->v, layer) : nullptr;
+  a.max_blocks = max_blocks;
+  a.Hq = n_q_heads;
+  a.Hkv = d.n_kv_heads;
+  a.num_blocks = d.num_blocks;
+  a.qk_scale_log2 = softmax_scale * 1.4426950408889634f * (pool->block_scaled ? 1.f : d.k_scale);
+  a.v_scale = pool->block_scaled ? 1.f : d.v_scale;
+  a.err = err;
+  const int tiles = (max_chunk + 15) / 16;
+  cudaError_t e;
+  const bool f32 = out_dtype == PA_FP32;
+  if (pool->block_scaled)
+    e = f32 ? tc_launch<true, PA_FP32, true>(a, tk, tv, tiles, S, st)
+            : tc_launch<true, PA_BF16, false>(a, tk, tv, tiles, S, st);
+  else
+    e = f32 ? tc_launch<false, PA_FP32, true>(a, tk, tv, tiles, S, st)
+            : tc_launch<false, PA_BF16, false>(a, tk, tv, tiles, S, st);
+  if (e != cudaSuccess) return fail(PA_ERR_CUDA, "prefill (tcgen05) launch: %s", cudaGetErrorString(e));
+  return PA_OK;
+}
+
+}  // namespace pa
