@@ -265,8 +265,10 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const TcArgs a,
       amax = fmaxf(amax, fmaxf(fabsf(bf16_bits_to_float(qw[w] & 0xFFFFu)), fabsf(bf16_bits_to_float(qw[w] >> 16))));
     int ex = 0;
     if (amax > 0.f) frexpf(amax, &ex);
-    const float qs = amax > 0.f ? ldexpf(1.f, 8 - ex) : 1.f;
-    if (amax > 0.f) row_scale = a.qk_scale_log2 * ldexpf(1.f, ex - 8);
+    // a negative score scale goes into q, so the per-row factor is positive
+    const float sgn = a.qk_scale_log2 < 0.f ? -1.f : 1.f;
+    const float qs = sgn * (amax > 0.f ? ldexpf(1.f, 8 - ex) : 1.f);
+    row_scale = fabsf(a.qk_scale_log2) * (amax > 0.f ? ldexpf(1.f, ex - 8) : 1.f);
 #pragma unroll
     for (int c = 0; c < 8; ++c) {  // 16 dims per 16-byte chunk of E4M3 codes
       uint32_t hi[4], lo[4];
@@ -449,15 +451,27 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const TcArgs a,
       __syncwarp();
       if (lane == 0) mbar_arrive(&ctl->s_empty[sb]);
 
-      // scores in log2 units, causal mask, block max
+      // Scores in log2 units are x * f_page (f_page > 0): the causal mask (only
+      // on blocks that reach the tile's first query) and the block max work on
+      // raw scores, per page and as trees, so no long dependency chain forms.
       const int key0 = 128 * j;
+      if (key0 + 127 > pos0) {
+#pragma unroll
+        for (int c = 0; c < 128; ++c)
+          if (key0 + c > qp) x[c] = -INFINITY;
+      }
+      float fpg[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i)  // a zero K scale (all-zero tile) must not turn -inf into NaN
+        fpg[i] = BLK ? row_scale * fmaxf(psc[i].x, 1.17549435e-38f) : row_scale;
       float mx = -INFINITY;
 #pragma unroll
-      for (int c = 0; c < 128; ++c) {
-        const float f = BLK ? row_scale * psc[c >> 4].x : row_scale;
-        const float v = (key0 + c > qp) ? -INFINITY : x[c] * f;
-        x[c] = v;
-        mx = fmaxf(mx, v);
+      for (int i = 0; i < 8; ++i) {
+        float t[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e)
+          t[e] = fmaxf(fmaxf(x[16 * i + e], x[16 * i + 4 + e]), fmaxf(x[16 * i + 8 + e], x[16 * i + 12 + e]));
+        mx = fmaxf(mx, fmaxf(fmaxf(t[0], t[1]), fmaxf(t[2], t[3])) * fpg[i]);
       }
       float ov = 1.f;  // factor for this row's O accumulator
       if (mx > m + 8.f) {  // the first visible block, or a max that grew by more than 2^8
@@ -479,14 +493,19 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const TcArgs a,
 #pragma unroll
         for (int i = 0; i < 8; ++i) vmul[i] = psc[i].y * inv;
       }
-      float rs = 0.f;
+      float rsp[8];
 #pragma unroll
-      for (int c = 0; c < 128; ++c) {
-        const float p = fast_exp2(x[c] - m);
-        rs += p;
-        x[c] = BLK ? p * vmul[c >> 4] : p;
+      for (int i = 0; i < 8; ++i) {
+        float t[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int e = 0; e < 16; ++e) {
+          const float p = fast_exp2(fmaf(x[16 * i + e], fpg[i], -m));
+          t[e & 3] += p;
+          x[16 * i + e] = BLK ? p * vmul[i] : p;
+        }
+        rsp[i] = (t[0] + t[1]) + (t[2] + t[3]);
       }
-      l += rs;
+      l += ((rsp[0] + rsp[1]) + (rsp[2] + rsp[3])) + ((rsp[4] + rsp[5]) + (rsp[6] + rsp[7]));
 
       // P V of the previous block is done: P may be overwritten, O rescaled
       if (j > 0) {
