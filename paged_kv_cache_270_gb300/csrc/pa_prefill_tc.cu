@@ -50,21 +50,22 @@ constexpr int kG = 8;           // query heads per kv head
 constexpr int kThreads = 256;   // 8 warps
 constexpr unsigned kAll = 0xffffffffu;
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kOCol = 256;  // TMEM columns: S buffers at 0 and 128, O at 256
+// TMEM columns (one lane per row): S(j) in buffer j % 2 at 0 / 128, overwritten
+// by P(j) in binary16 (columns 0-63 of the buffer; P's low part in 64-127 in
+// the fp32-output mode); O at 256; the two E4M3 terms of Q at 384 and 416.
+constexpr uint32_t kOCol = 256;
+constexpr uint32_t kQHiCol = 384;
+constexpr uint32_t kQLoCol = 416;
 
 // shared memory, from a 1024-byte aligned base
-constexpr int kQHi = 0;               // [128 rows][128 B] E4M3, swizzled
-constexpr int kQLo = kQHi + 16384;
-constexpr int kKRing = kQLo + 16384;  // [2][8 pages][16 keys][128 B] E4M3 (TMA, swizzled)
+constexpr int kKRing = 0;             // [2][8 pages][16 keys][128 B] E4M3 (TMA, swizzled)
 constexpr int kVRing = kKRing + 32768;
 constexpr int kVT = kVRing + 32768;   // [2][2 dim blocks][128 keys][128 B] binary16, swizzled
-constexpr int kP = kVT + 65536;       // [2 key blocks][128 rows][128 B] binary16, swizzled
-constexpr int kPLo = kP + 32768;
-__host__ __device__ constexpr int data_bytes(bool psplit) { return psplit ? kPLo + 32768 : kPLo; }
+__host__ __device__ constexpr int data_bytes(bool) { return kVT + 65536; }
 
 struct Ctrl {
-  uint64_t kv_full[2], kv_empty[2], s_full[2], s_empty[2], vt_full[2], vt_empty[2];
-  uint64_t sc_full[2], sc_empty[2], p_full, o_done, drain;
+  uint64_t kv_full[2], kv_empty[2], s_full[2], vt_full[2], vt_empty[2];
+  uint64_t sc_full[2], sc_empty[2], q_ready, p_full, o_done, drain;
   float2 sc[2][8];  // block-scaled pools: (K scale, V scale) of each page of a ring block
   uint32_t tmem;
   int abort;
@@ -103,15 +104,17 @@ __device__ __forceinline__ uint64_t mnmajor(uint32_t saddr) { return sw128_desc(
 constexpr uint32_t kIdescQK = (1u << 4) | ((128u >> 3) << 17) | ((128u >> 4) << 24);
 constexpr uint32_t kIdescPV = (1u << 4) | (1u << 16) | ((128u >> 3) << 17) | ((128u >> 4) << 24);
 
-__device__ __forceinline__ void mma_f8(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
+// D (TMEM) = A x B (+ D): A in tensor memory (row i in lane i, consecutive K
+// elements packed little-endian into 32-bit columns), B in shared memory.
+__device__ __forceinline__ void mma_f8_ts(uint32_t d, uint32_t a_tmem, uint64_t b, uint32_t idesc, uint32_t acc) {
   asm volatile("{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
-               "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}"
-               ::"r"(d), "l"(a), "l"(b), "r"(idesc), "r"(acc) : "memory");
+               "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], [%1], %2, %3, p;\n\t}"
+               ::"r"(d), "r"(a_tmem), "l"(b), "r"(idesc), "r"(acc) : "memory");
 }
-__device__ __forceinline__ void mma_f16(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
+__device__ __forceinline__ void mma_f16_ts(uint32_t d, uint32_t a_tmem, uint64_t b, uint32_t idesc, uint32_t acc) {
   asm volatile("{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
-               "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}"
-               ::"r"(d), "l"(a), "l"(b), "r"(idesc), "r"(acc) : "memory");
+               "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}"
+               ::"r"(d), "r"(a_tmem), "l"(b), "r"(idesc), "r"(acc) : "memory");
 }
 // The mbarrier gets one arrival once every MMA this thread issued so far is done.
 __device__ __forceinline__ void mma_commit(uint64_t* bar) {
@@ -137,6 +140,7 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float* v) {
 #pragma unroll
   for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
 }
+__device__ __forceinline__ void tmem_st32u(uint32_t taddr, const uint32_t* w);
 __device__ __forceinline__ void tmem_st32(uint32_t taddr, const float* v) {
   asm volatile(
       "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,"
@@ -152,6 +156,16 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const float* v) {
         "r"(__float_as_uint(v[24])), "r"(__float_as_uint(v[25])), "r"(__float_as_uint(v[26])),
         "r"(__float_as_uint(v[27])), "r"(__float_as_uint(v[28])), "r"(__float_as_uint(v[29])),
         "r"(__float_as_uint(v[30])), "r"(__float_as_uint(v[31]))
+      : "memory");
+}
+__device__ __forceinline__ void tmem_st32u(uint32_t taddr, const uint32_t* w) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,"
+      "%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};"
+      ::"r"(taddr), "r"(w[0]), "r"(w[1]), "r"(w[2]), "r"(w[3]), "r"(w[4]), "r"(w[5]), "r"(w[6]), "r"(w[7]),
+        "r"(w[8]), "r"(w[9]), "r"(w[10]), "r"(w[11]), "r"(w[12]), "r"(w[13]), "r"(w[14]), "r"(w[15]),
+        "r"(w[16]), "r"(w[17]), "r"(w[18]), "r"(w[19]), "r"(w[20]), "r"(w[21]), "r"(w[22]), "r"(w[23]),
+        "r"(w[24]), "r"(w[25]), "r"(w[26]), "r"(w[27]), "r"(w[28]), "r"(w[29]), "r"(w[30]), "r"(w[31])
       : "memory");
 }
 __device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
@@ -219,12 +233,12 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const TcArgs a,
       mbar_init(&ctl->kv_full[i], 1);
       mbar_init(&ctl->kv_empty[i], 3);  // the QK MMAs' commit + the two converter warps
       mbar_init(&ctl->s_full[i], 1);
-      mbar_init(&ctl->s_empty[i], 4);
       mbar_init(&ctl->vt_full[i], 2);
       mbar_init(&ctl->vt_empty[i], 1);
       mbar_init(&ctl->sc_full[i], 1);
       mbar_init(&ctl->sc_empty[i], 4);
     }
+    mbar_init(&ctl->q_ready, 4);
     mbar_init(&ctl->p_full, 4);
     mbar_init(&ctl->o_done, 1);
     mbar_init(&ctl->drain, 1);
@@ -247,6 +261,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const TcArgs a,
   const int tl = r >> 3, hh = r & 7;
   const bool row_valid = warp >= 4 && tl < n_tok;
   float row_scale = a.qk_scale_log2;
+  uint32_t qhi[32], qlo[32];  // the row's E4M3 terms, 4 dims per word (dim order)
   if (warp >= 4) {
     uint32_t qw[64];  // the row's 128 bfloat16 values, two per word
     const uint4* src = reinterpret_cast<const uint4*>(
@@ -271,7 +286,6 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const TcArgs a,
     row_scale = fabsf(a.qk_scale_log2) * (amax > 0.f ? ldexpf(1.f, ex - 8) : 1.f);
 #pragma unroll
     for (int c = 0; c < 8; ++c) {  // 16 dims per 16-byte chunk of E4M3 codes
-      uint32_t hi[4], lo[4];
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
         const uint32_t w0 = qw[8 * c + 2 * i], w1 = qw[8 * c + 2 * i + 1];
@@ -284,19 +298,24 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const TcArgs a,
         const float2 d23 = unpack2<false>(e4m3x2_to_f16x2(h23));
         const uint32_t l01 = __nv_cvt_float2_to_fp8x2(make_float2(x01.x - d01.x, x01.y - d01.y), __NV_SATFINITE, __NV_E4M3);
         const uint32_t l23 = __nv_cvt_float2_to_fp8x2(make_float2(x23.x - d23.x, x23.y - d23.y), __NV_SATFINITE, __NV_E4M3);
-        hi[i] = (h01 & 0xFFFFu) | (h23 << 16);
-        lo[i] = (l01 & 0xFFFFu) | (l23 << 16);
+        qhi[4 * c + i] = (h01 & 0xFFFFu) | (h23 << 16);
+        qlo[4 * c + i] = (l01 & 0xFFFFu) | (l23 << 16);
       }
-      const uint32_t off = r * 128 + ((c ^ (r & 7)) << 4);
-      *reinterpret_cast<uint4*>(sm + kQHi + off) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
-      *reinterpret_cast<uint4*>(sm + kQLo + off) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
     }
-    fence_proxy_async();  // the MMA reads Q through the async proxy
   }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = ctl->tmem;
+  if (warp >= 4) {  // Q into tensor memory, the A operand of S = Q K^T
+    const uint32_t tq = tmem + ((uint32_t)((warp & 3) * 32) << 16);
+    tmem_st32u(tq + kQHiCol, qhi);
+    tmem_st32u(tq + kQLoCol, qlo);
+    tmem_wait_st();
+    tc_fence_before();
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&ctl->q_ready);
+  }
 
   if (warp == 0) {
     // ---------------------------------------------------------- TMA producer
@@ -348,21 +367,20 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const TcArgs a,
         if (!mbar_wait(&ctl->kv_full[j & 1], (j >> 1) & 1)) record_error(a.err, PA_ERR_TIMEOUT);
   } else if (warp == 1) {
     // ---------------------------------------------------------- MMA issue
-    if (lane == 0) {
-      const uint32_t qhi = smem_addr(sm + kQHi), qlo = smem_addr(sm + kQLo);
+    if (lane == 0 && wait_or_abort(&ctl->q_ready, 0, abort_flag, a.err)) {
       for (int j = 0; j <= nblk; ++j) {
-        if (j < nblk) {  // S(j) = Q K(j)^T, after the softmax has read S(j - 2)
+        if (j < nblk) {  // S(j) = Q K(j)^T, once P V(j - 2) has read P(j - 2) from this buffer
           const int sb = j & 1, u = j >> 1;
           if (!wait_or_abort(&ctl->kv_full[sb], u & 1, abort_flag, a.err)) break;
-          if (j >= 2 && !wait_or_abort(&ctl->s_empty[sb], (u - 1) & 1, abort_flag, a.err)) break;
+          if (j >= 2 && !wait_or_abort(&ctl->o_done, (j - 2) & 1, abort_flag, a.err)) break;
           tc_fence_after();
           const uint32_t kb = smem_addr(sm + kKRing + sb * 16384);
 #pragma unroll
           for (int t = 0; t < 2; ++t)
 #pragma unroll
             for (int k = 0; k < 4; ++k)
-              mma_f8(tmem + sb * 128, kmajor((t ? qlo : qhi) + 32 * k), kmajor(kb + 32 * k), kIdescQK,
-                     (uint32_t)(t | k));
+              mma_f8_ts(tmem + sb * 128, tmem + (t ? kQLoCol : kQHiCol) + 8 * k, kmajor(kb + 32 * k), kIdescQK,
+                        (uint32_t)(t | k));
           mma_commit(&ctl->s_full[sb]);
           mma_commit(&ctl->kv_empty[sb]);
         }
@@ -373,18 +391,16 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const TcArgs a,
           tc_fence_after();
           const uint32_t vt = smem_addr(sm + kVT + vb * 32768);
 #pragma unroll
-          for (int part = 0; part < (PSPLIT ? 2 : 1); ++part) {
-            const uint32_t pb = smem_addr(sm + (part ? kPLo : kP));
+          for (int part = 0; part < (PSPLIT ? 2 : 1); ++part)
 #pragma unroll
             for (int k = 0; k < 8; ++k)
-              mma_f16(tmem + kOCol, kmajor(pb + (k >> 2) * 16384 + (k & 3) * 32), mnmajor(vt + k * 2048),
-                      kIdescPV, (uint32_t)(i | k | part));
-          }
+              mma_f16_ts(tmem + kOCol, tmem + vb * 128 + part * 64 + 8 * k, mnmajor(vt + k * 2048), kIdescPV,
+                         (uint32_t)(i | k | part));
           mma_commit(&ctl->o_done);
           mma_commit(&ctl->vt_empty[vb]);
         }
       }
-      // every MMA issued above has finished before TMEM is released
+      // every MMA issued above has finished before O is read and TMEM released
       mma_commit(&ctl->drain);
       if (!mbar_wait(&ctl->drain, 0)) record_error(a.err, PA_ERR_TIMEOUT);
     }
@@ -447,9 +463,6 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const TcArgs a,
 #pragma unroll
       for (int c = 0; c < 4; ++c) tmem_ld32(trow + sb * 128 + 32 * c, x + 32 * c);
       tmem_wait_ld();
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&ctl->s_empty[sb]);
 
       // Scores in log2 units are x * f_page (f_page > 0): the causal mask (only
       // on blocks that reach the tile's first query) and the block max work on
@@ -507,12 +520,14 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const TcArgs a,
       }
       l += ((rsp[0] + rsp[1]) + (rsp[2] + rsp[3])) + ((rsp[4] + rsp[5]) + (rsp[6] + rsp[7]));
 
-      // P V of the previous block is done: P may be overwritten, O rescaled
-      if (j > 0) {
+      // O is rescaled once the previous block's P V is done (rarely needed).
+      // Phase distance: QK(j) waited for P V(j - 2), and P V(j) needs this
+      // block's P, so o_done has completed j - 1 or j phases here.
+      if (j > 0 && __any_sync(kAll, ov != 1.f)) {
         ok = __all_sync(kAll, wait_or_abort(&ctl->o_done, (j - 1) & 1, abort_flag, a.err));
         if (!ok) break;
         tc_fence_after();
-        if (__any_sync(kAll, ov != 1.f)) {
+        {
 #pragma unroll
           for (int c = 0; c < 4; ++c) {
             float o[32];
@@ -525,29 +540,35 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const TcArgs a,
           tmem_wait_st();
         }
       }
-      // P row: 16 chunks of 8 keys, binary16 (and the low part in fp32 mode)
+      // P over S in this row's lane: binary16, 2 keys per column (and the low part in fp32 mode)
+      {
+        uint32_t ph[64], pl[64];
 #pragma unroll
-      for (int cc = 0; cc < 16; ++cc) {
-        uint32_t ph[4], pl[4];
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          ph[e] = pack2<false>(x[8 * cc + 2 * e], x[8 * cc + 2 * e + 1]);
+        for (int e = 0; e < 64; ++e) {
+          ph[e] = pack2<false>(x[2 * e], x[2 * e + 1]);
           if constexpr (PSPLIT) {
             const float2 hv = unpack2<false>(ph[e]);
-            pl[e] = pack2<false>(x[8 * cc + 2 * e] - hv.x, x[8 * cc + 2 * e + 1] - hv.y);
+            pl[e] = pack2<false>(x[2 * e] - hv.x, x[2 * e + 1] - hv.y);
           }
         }
-        const uint32_t off = (cc >> 3) * 16384 + r * 128 + (((cc & 7) ^ (r & 7)) << 4);
-        *reinterpret_cast<uint4*>(sm + kP + off) = make_uint4(ph[0], ph[1], ph[2], ph[3]);
-        if constexpr (PSPLIT) *reinterpret_cast<uint4*>(sm + kPLo + off) = make_uint4(pl[0], pl[1], pl[2], pl[3]);
+        const uint32_t ps = trow + sb * 128;
+        tmem_st32u(ps, ph);
+        tmem_st32u(ps + 32, ph + 32);
+        if constexpr (PSPLIT) {
+          tmem_st32u(ps + 64, pl);
+          tmem_st32u(ps + 96, pl + 32);
+        }
+        tmem_wait_st();
       }
-      fence_proxy_async();
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&ctl->p_full);
     }
-    // output rows: O / l (times the V scale)
-    if (ok) ok = __all_sync(kAll, wait_or_abort(&ctl->o_done, (nblk - 1) & 1, abort_flag, a.err));
+    // output rows: O / l (times the V scale), once every MMA is done.  (The
+    // final P V is awaited through the one-phase drain barrier: o_done may be
+    // two phases behind here, since it is only awaited to rescale O, and a
+    // parity wait tells phases apart only one phase ahead.)
+    if (ok) ok = __all_sync(kAll, wait_or_abort(&ctl->drain, 0, abort_flag, a.err));
     if (ok) {
       tc_fence_after();
       const float s = l > 0.f ? (BLK ? vref : a.v_scale) / l : 0.f;
