@@ -51,8 +51,9 @@ constexpr int kThreads = 256;   // 8 warps
 constexpr unsigned kAll = 0xffffffffu;
 constexpr uint32_t kTmemCols = 512;
 // TMEM columns (one lane per row): S(j) in buffer j % 2 at 0 / 128, overwritten
-// by P(j) in binary16 (columns 0-63 of the buffer; P's low part in 64-127 in
-// the fp32-output mode); O at 256; the two E4M3 terms of Q at 384 and 416.
+// by P(j) in binary16: keys 32c .. 32c+31 in columns 32c .. 32c+15 of the
+// buffer (P's low part, fp32-output mode, in 32c+16 .. 32c+31); O at 256; the
+// two E4M3 terms of Q at 384 and 416.
 constexpr uint32_t kOCol = 256;
 constexpr uint32_t kQHiCol = 384;
 constexpr uint32_t kQLoCol = 416;
@@ -166,6 +167,14 @@ __device__ __forceinline__ void tmem_st32u(uint32_t taddr, const uint32_t* w) {
         "r"(w[8]), "r"(w[9]), "r"(w[10]), "r"(w[11]), "r"(w[12]), "r"(w[13]), "r"(w[14]), "r"(w[15]),
         "r"(w[16]), "r"(w[17]), "r"(w[18]), "r"(w[19]), "r"(w[20]), "r"(w[21]), "r"(w[22]), "r"(w[23]),
         "r"(w[24]), "r"(w[25]), "r"(w[26]), "r"(w[27]), "r"(w[28]), "r"(w[29]), "r"(w[30]), "r"(w[31])
+      : "memory");
+}
+__device__ __forceinline__ void tmem_st16u(uint32_t taddr, const uint32_t* w) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,"
+      "%14,%15,%16};"
+      ::"r"(taddr), "r"(w[0]), "r"(w[1]), "r"(w[2]), "r"(w[3]), "r"(w[4]), "r"(w[5]), "r"(w[6]), "r"(w[7]),
+        "r"(w[8]), "r"(w[9]), "r"(w[10]), "r"(w[11]), "r"(w[12]), "r"(w[13]), "r"(w[14]), "r"(w[15])
       : "memory");
 }
 __device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
@@ -394,8 +403,8 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const TcArgs a,
           for (int part = 0; part < (PSPLIT ? 2 : 1); ++part)
 #pragma unroll
             for (int k = 0; k < 8; ++k)
-              mma_f16_ts(tmem + kOCol, tmem + vb * 128 + part * 64 + 8 * k, mnmajor(vt + k * 2048), kIdescPV,
-                         (uint32_t)(i | k | part));
+              mma_f16_ts(tmem + kOCol, tmem + vb * 128 + 32 * (k >> 1) + 16 * part + 8 * (k & 1),
+                         mnmajor(vt + k * 2048), kIdescPV, (uint32_t)(i | k | part));
           mma_commit(&ctl->o_done);
           mma_commit(&ctl->vt_empty[vb]);
         }
@@ -417,7 +426,9 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const TcArgs a,
       uint8_t* vt = sm + kVT + half * 32768;
 #pragma unroll 4
       for (int it = 0; it < 16; ++it) {
-        const int idx = ct + 64 * it, key = idx >> 3, ch = idx & 7;
+        // consecutive lanes take consecutive keys of one 16-byte chunk, so each
+        // 8-lane phase of a 16-byte access covers 8 distinct (swizzled) chunks
+        const int idx = ct + 64 * it, key = idx & 127, ch = idx >> 7;
         uint4 w = make_uint4(0, 0, 0, 0);
         if (key < nvalid) w = lds128(vr + (key >> 4) * 2048 + (key & 15) * 128 + ((ch ^ (key & 7)) << 4));
         const uint32_t cw[4] = {w.x, w.y, w.z, w.w};
@@ -445,81 +456,57 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const TcArgs a,
     const int qp = pos0 + min(tl, n_tok - 1);  // causal limit of the row
     float m = -INFINITY, l = 0.f, vref = 0.f;
     bool ok = true;
-    float x[128];
     for (int j = 0; j < nblk; ++j) {
       const int sb = j & 1, u = j >> 1;
-      float2 psc[8];
-      if constexpr (BLK) {
+      float ov = 1.f, vinv = 1.f;  // factor for this row's O accumulator; 1 / vref
+      if constexpr (BLK) {  // V weights are taken relative to the largest V scale seen (<= 1)
         ok = __all_sync(kAll, wait_or_abort(&ctl->sc_full[sb], u & 1, abort_flag, a.err));
         if (!ok) break;
+        float vb = vref;
 #pragma unroll
-        for (int i = 0; i < 8; ++i) psc[i] = ctl->sc[sb][i];
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&ctl->sc_empty[sb]);
+        for (int i = 0; i < 8; ++i) vb = fmaxf(vb, ctl->sc[sb][i].y);
+        if (vb > vref) {
+          ov = vref / vb;
+          vref = vb;
+        }
+        vinv = vref > 0.f ? 1.f / vref : 0.f;
       }
       ok = __all_sync(kAll, wait_or_abort(&ctl->s_full[sb], u & 1, abort_flag, a.err));
       if (!ok) break;
       tc_fence_after();
-#pragma unroll
-      for (int c = 0; c < 4; ++c) tmem_ld32(trow + sb * 128 + 32 * c, x + 32 * c);
-      tmem_wait_ld();
-
-      // Scores in log2 units are x * f_page (f_page > 0): the causal mask (only
-      // on blocks that reach the tile's first query) and the block max work on
-      // raw scores, per page and as trees, so no long dependency chain forms.
+      // Scores in log2 units are s * f_page, f_page > 0.  S is read 32 columns
+      // at a time, twice: the block max first, then the exponentials; the causal
+      // mask runs only on blocks that reach the tile's first query.
       const int key0 = 128 * j;
-      if (key0 + 127 > pos0) {
-#pragma unroll
-        for (int c = 0; c < 128; ++c)
-          if (key0 + c > qp) x[c] = -INFINITY;
-      }
-      float fpg[8];
-#pragma unroll
-      for (int i = 0; i < 8; ++i)  // a zero K scale (all-zero tile) must not turn -inf into NaN
-        fpg[i] = BLK ? row_scale * fmaxf(psc[i].x, 1.17549435e-38f) : row_scale;
+      const bool diag = key0 + 127 > pos0;
+      const uint32_t sbase = trow + sb * 128;
       float mx = -INFINITY;
+#pragma unroll 1
+      for (int c = 0; c < 4; ++c) {
+        float v[32];
+        tmem_ld32(sbase + 32 * c, v);
+        tmem_wait_ld();
+        if (diag) {
 #pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        float t[4];
+          for (int e = 0; e < 32; ++e)
+            if (key0 + 32 * c + e > qp) v[e] = -INFINITY;
+        }
 #pragma unroll
-        for (int e = 0; e < 4; ++e)
-          t[e] = fmaxf(fmaxf(x[16 * i + e], x[16 * i + 4 + e]), fmaxf(x[16 * i + 8 + e], x[16 * i + 12 + e]));
-        mx = fmaxf(mx, fmaxf(fmaxf(t[0], t[1]), fmaxf(t[2], t[3])) * fpg[i]);
+        for (int hp = 0; hp < 2; ++hp) {  // the chunk's two pages
+          const float f = BLK ? row_scale * fmaxf(ctl->sc[sb][2 * c + hp].x, 1.17549435e-38f) : row_scale;
+          float t[4];
+#pragma unroll
+          for (int e = 0; e < 4; ++e)
+            t[e] = fmaxf(fmaxf(v[16 * hp + e], v[16 * hp + 4 + e]), fmaxf(v[16 * hp + 8 + e], v[16 * hp + 12 + e]));
+          mx = fmaxf(mx, fmaxf(fmaxf(t[0], t[1]), fmaxf(t[2], t[3])) * f);
+        }
       }
-      float ov = 1.f;  // factor for this row's O accumulator
       if (mx > m + 8.f) {  // the first visible block, or a max that grew by more than 2^8
         const float alpha = fast_exp2(m - mx);
         l *= alpha;
-        ov = alpha;
+        ov *= alpha;
         m = mx;
       }
-      float vmul[8];
-      if constexpr (BLK) {  // V weights relative to the largest V scale seen (<= 1)
-        float vb = vref;
-#pragma unroll
-        for (int i = 0; i < 8; ++i) vb = fmaxf(vb, psc[i].y);
-        if (vb > vref) {
-          ov *= vref / vb;
-          vref = vb;
-        }
-        const float inv = vref > 0.f ? 1.f / vref : 0.f;
-#pragma unroll
-        for (int i = 0; i < 8; ++i) vmul[i] = psc[i].y * inv;
-      }
-      float rsp[8];
-#pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        float t[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-        for (int e = 0; e < 16; ++e) {
-          const float p = fast_exp2(fmaf(x[16 * i + e], fpg[i], -m));
-          t[e & 3] += p;
-          x[16 * i + e] = BLK ? p * vmul[i] : p;
-        }
-        rsp[i] = (t[0] + t[1]) + (t[2] + t[3]);
-      }
-      l += ((rsp[0] + rsp[1]) + (rsp[2] + rsp[3])) + ((rsp[4] + rsp[5]) + (rsp[6] + rsp[7]));
-
       // O is rescaled once the previous block's P V is done (rarely needed).
       // Phase distance: QK(j) waited for P V(j - 2), and P V(j) needs this
       // block's P, so o_done has completed j - 1 or j phases here.
@@ -527,42 +514,63 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const TcArgs a,
         ok = __all_sync(kAll, wait_or_abort(&ctl->o_done, (j - 1) & 1, abort_flag, a.err));
         if (!ok) break;
         tc_fence_after();
-        {
+#pragma unroll 1
+        for (int c = 0; c < 4; ++c) {
+          float o[32];
+          tmem_ld32(trow + kOCol + 32 * c, o);
+          tmem_wait_ld();
 #pragma unroll
-          for (int c = 0; c < 4; ++c) {
-            float o[32];
-            tmem_ld32(trow + kOCol + 32 * c, o);
-            tmem_wait_ld();
-#pragma unroll
-            for (int e = 0; e < 32; ++e) o[e] *= ov;
-            tmem_st32(trow + kOCol + 32 * c, o);
-          }
-          tmem_wait_st();
-        }
-      }
-      // P over S in this row's lane: binary16, 2 keys per column (and the low part in fp32 mode)
-      {
-        uint32_t ph[64], pl[64];
-#pragma unroll
-        for (int e = 0; e < 64; ++e) {
-          ph[e] = pack2<false>(x[2 * e], x[2 * e + 1]);
-          if constexpr (PSPLIT) {
-            const float2 hv = unpack2<false>(ph[e]);
-            pl[e] = pack2<false>(x[2 * e] - hv.x, x[2 * e + 1] - hv.y);
-          }
-        }
-        const uint32_t ps = trow + sb * 128;
-        tmem_st32u(ps, ph);
-        tmem_st32u(ps + 32, ph + 32);
-        if constexpr (PSPLIT) {
-          tmem_st32u(ps + 64, pl);
-          tmem_st32u(ps + 96, pl + 32);
+          for (int e = 0; e < 32; ++e) o[e] *= ov;
+          tmem_st32(trow + kOCol + 32 * c, o);
         }
         tmem_wait_st();
       }
+      // P in binary16 over the chunk's own S columns: keys 32c .. 32c+31 go to
+      // columns 32c .. 32c+15 (the low part, fp32 mode, to 32c+16 .. 32c+31)
+      float rs = 0.f;
+#pragma unroll 1
+      for (int c = 0; c < 4; ++c) {
+        float v[32];
+        tmem_ld32(sbase + 32 * c, v);
+        tmem_wait_ld();
+        if (diag) {
+#pragma unroll
+          for (int e = 0; e < 32; ++e)
+            if (key0 + 32 * c + e > qp) v[e] = -INFINITY;
+        }
+#pragma unroll
+        for (int hp = 0; hp < 2; ++hp) {
+          const float f = BLK ? row_scale * fmaxf(ctl->sc[sb][2 * c + hp].x, 1.17549435e-38f) : row_scale;
+          const float vm = BLK ? ctl->sc[sb][2 * c + hp].y * vinv : 1.f;
+          float t[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+          for (int e = 0; e < 16; ++e) {
+            const float pe = fast_exp2(fmaf(v[16 * hp + e], f, -m));
+            t[e & 3] += pe;
+            v[16 * hp + e] = BLK ? pe * vm : pe;
+          }
+          rs += (t[0] + t[1]) + (t[2] + t[3]);
+        }
+        uint32_t ph[16], pl[16];
+#pragma unroll
+        for (int e = 0; e < 16; ++e) {
+          ph[e] = pack2<false>(v[2 * e], v[2 * e + 1]);
+          if constexpr (PSPLIT) {
+            const float2 hv = unpack2<false>(ph[e]);
+            pl[e] = pack2<false>(v[2 * e] - hv.x, v[2 * e + 1] - hv.y);
+          }
+        }
+        tmem_st16u(sbase + 32 * c, ph);
+        if constexpr (PSPLIT) tmem_st16u(sbase + 32 * c + 16, pl);
+      }
+      l += rs;
+      tmem_wait_st();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&ctl->p_full);
+      if (lane == 0) {
+        if constexpr (BLK) mbar_arrive(&ctl->sc_empty[sb]);
+        mbar_arrive(&ctl->p_full);
+      }
     }
     // output rows: O / l (times the V scale), once every MMA is done.  (The
     // final P V is awaited through the one-phase drain barrier: o_done may be
