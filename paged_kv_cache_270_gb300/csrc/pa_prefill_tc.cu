@@ -21,13 +21,14 @@
 //    into two E4M3 terms, hi = E4M3(x) and lo = E4M3(x - hi); their sum
 //    carries the row's 8 significant bits, so S = hi K^T + lo K^T (two MMA
 //    passes into one accumulator) is exact up to fp32 accumulation order.
-//  * warps 2-3 convert each V block to binary16 (exact), laid out 128-byte
+//  * four warps convert each V block to binary16 (exact), laid out 128-byte
 //    swizzled with the head dim contiguous, which the MMA reads as its B
 //    operand in MN-major form: O += P V is kind::f16 with P in binary16 (plus
 //    a second pass with P's low part in the fp32-output mode).
-//  * warps 4-7 run the online softmax, one thread per row: S comes out of
-//    TMEM, the max moves only when it grows by more than 2^8 (so P <= 2^8),
-//    and then the thread rescales its own O row in TMEM before the next P V.
+//  * eight warps run the online softmax, two threads per row (each takes half
+//    of every key block and of the row's O): S comes out of TMEM, the max moves
+//    only when it grows by more than 2^8 (so P <= 2^8), and then the threads
+//    rescale their halves of the O row in TMEM before the next P V.
 //  * warp 1 allocates TMEM and one lane issues every MMA; completion is
 //    signalled through mbarriers (tcgen05.commit).  Every wait is bounded: a
 //    timeout records PA_ERR_TIMEOUT, raises a CTA-wide abort flag that ends
@@ -47,7 +48,7 @@ namespace {
 
 constexpr int kD = 128;         // head dim
 constexpr int kG = 8;           // query heads per kv head
-constexpr int kThreads = 256;   // 8 warps
+constexpr int kThreads = 448;   // 14 warps: producer, MMA, 4 converters, 8 softmax
 constexpr unsigned kAll = 0xffffffffu;
 constexpr uint32_t kTmemCols = 512;
 // TMEM columns (one lane per row): S(j) in buffer j % 2 at 0 / 128, overwritten
@@ -66,8 +67,9 @@ __host__ __device__ constexpr int data_bytes(bool) { return kVT + 65536; }
 
 struct Ctrl {
   uint64_t kv_full[2], kv_empty[2], s_full[2], vt_full[2], vt_empty[2];
-  uint64_t sc_full[2], sc_empty[2], q_ready, p_full, o_done, drain;
+  uint64_t sc_full[2], sc_empty[2], q_ready, p_full, o_done, drain, xchg;
   float2 sc[2][8];  // block-scaled pools: (K scale, V scale) of each page of a ring block
+  float xbuf[2][128][2];  // the two half-row threads' partials (Q amax, block max, row sum)
   uint32_t tmem;
   int abort;
 };
@@ -196,6 +198,10 @@ __device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, vo
   return true;
 }
 
+// causal limit of a row: the position of its query token (rows past the
+// tile's last token reuse the last one)
+__device__ __forceinline__ int qp_of(int pos0, int tl, int n_tok) { return pos0 + min(tl, n_tok - 1); }
+
 template <int OUT>
 __device__ __forceinline__ void store_row32(void* out, size_t idx, const float* v, float s) {
   if constexpr (OUT == PA_FP32) {
@@ -240,17 +246,18 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const TcArgs a,
   if (threadIdx.x == 0) {
     for (int i = 0; i < 2; ++i) {
       mbar_init(&ctl->kv_full[i], 1);
-      mbar_init(&ctl->kv_empty[i], 3);  // the QK MMAs' commit + the two converter warps
+      mbar_init(&ctl->kv_empty[i], 5);  // the QK MMAs' commit + the four converter warps
       mbar_init(&ctl->s_full[i], 1);
-      mbar_init(&ctl->vt_full[i], 2);
+      mbar_init(&ctl->vt_full[i], 4);
       mbar_init(&ctl->vt_empty[i], 1);
       mbar_init(&ctl->sc_full[i], 1);
-      mbar_init(&ctl->sc_empty[i], 4);
+      mbar_init(&ctl->sc_empty[i], 8);
     }
-    mbar_init(&ctl->q_ready, 4);
-    mbar_init(&ctl->p_full, 4);
+    mbar_init(&ctl->q_ready, 8);
+    mbar_init(&ctl->p_full, 8);
     mbar_init(&ctl->o_done, 1);
     mbar_init(&ctl->drain, 1);
+    mbar_init(&ctl->xchg, 8);
     ctl->abort = 0;
     fence_barrier_init();
   }
@@ -263,68 +270,10 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const TcArgs a,
                  ::"r"(smem_addr(&ctl->tmem)), "r"(kTmemCols) : "memory");
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
   }
-
-  // Softmax rows: r = 8 * (query token) + head; Q rows go to shared memory as
-  // two E4M3 terms after a power-of-two scaling that puts max |q| in [128, 256).
-  const int r = threadIdx.x - 128;
-  const int tl = r >> 3, hh = r & 7;
-  const bool row_valid = warp >= 4 && tl < n_tok;
-  float row_scale = a.qk_scale_log2;
-  uint32_t qhi[32], qlo[32];  // the row's E4M3 terms, 4 dims per word (dim order)
-  if (warp >= 4) {
-    uint32_t qw[64];  // the row's 128 bfloat16 values, two per word
-    const uint4* src = reinterpret_cast<const uint4*>(
-        a.q + ((size_t)(q0 + tok_lo + tl) * a.Hq + (size_t)h * kG + hh) * kD);
-#pragma unroll
-    for (int c = 0; c < 16; ++c) {
-      const uint4 v = row_valid ? src[c] : make_uint4(0, 0, 0, 0);
-      qw[4 * c] = v.x;
-      qw[4 * c + 1] = v.y;
-      qw[4 * c + 2] = v.z;
-      qw[4 * c + 3] = v.w;
-    }
-    float amax = 0.f;
-#pragma unroll
-    for (int w = 0; w < 64; ++w)
-      amax = fmaxf(amax, fmaxf(fabsf(bf16_bits_to_float(qw[w] & 0xFFFFu)), fabsf(bf16_bits_to_float(qw[w] >> 16))));
-    int ex = 0;
-    if (amax > 0.f) frexpf(amax, &ex);
-    // a negative score scale goes into q, so the per-row factor is positive
-    const float sgn = a.qk_scale_log2 < 0.f ? -1.f : 1.f;
-    const float qs = sgn * (amax > 0.f ? ldexpf(1.f, 8 - ex) : 1.f);
-    row_scale = fabsf(a.qk_scale_log2) * (amax > 0.f ? ldexpf(1.f, ex - 8) : 1.f);
-#pragma unroll
-    for (int c = 0; c < 8; ++c) {  // 16 dims per 16-byte chunk of E4M3 codes
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const uint32_t w0 = qw[8 * c + 2 * i], w1 = qw[8 * c + 2 * i + 1];
-        // dims 16c + 4i .. 16c + 4i + 3: (w0 lo, w0 hi, w1 lo, w1 hi)
-        const float2 x01 = make_float2(bf16_bits_to_float(w0 & 0xFFFFu) * qs, bf16_bits_to_float(w0 >> 16) * qs);
-        const float2 x23 = make_float2(bf16_bits_to_float(w1 & 0xFFFFu) * qs, bf16_bits_to_float(w1 >> 16) * qs);
-        const uint32_t h01 = __nv_cvt_float2_to_fp8x2(x01, __NV_SATFINITE, __NV_E4M3);
-        const uint32_t h23 = __nv_cvt_float2_to_fp8x2(x23, __NV_SATFINITE, __NV_E4M3);
-        const float2 d01 = unpack2<false>(e4m3x2_to_f16x2(h01));
-        const float2 d23 = unpack2<false>(e4m3x2_to_f16x2(h23));
-        const uint32_t l01 = __nv_cvt_float2_to_fp8x2(make_float2(x01.x - d01.x, x01.y - d01.y), __NV_SATFINITE, __NV_E4M3);
-        const uint32_t l23 = __nv_cvt_float2_to_fp8x2(make_float2(x23.x - d23.x, x23.y - d23.y), __NV_SATFINITE, __NV_E4M3);
-        qhi[4 * c + i] = (h01 & 0xFFFFu) | (h23 << 16);
-        qlo[4 * c + i] = (l01 & 0xFFFFu) | (l23 << 16);
-      }
-    }
-  }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = ctl->tmem;
-  if (warp >= 4) {  // Q into tensor memory, the A operand of S = Q K^T
-    const uint32_t tq = tmem + ((uint32_t)((warp & 3) * 32) << 16);
-    tmem_st32u(tq + kQHiCol, qhi);
-    tmem_st32u(tq + kQLoCol, qlo);
-    tmem_wait_st();
-    tc_fence_before();
-    __syncwarp();
-    if (lane == 0) mbar_arrive(&ctl->q_ready);
-  }
 
   if (warp == 0) {
     // ---------------------------------------------------------- TMA producer
@@ -414,9 +363,12 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const TcArgs a,
       if (!mbar_wait(&ctl->drain, 0)) record_error(a.err, PA_ERR_TIMEOUT);
     }
     __syncwarp();
-  } else if (warp < 4) {
+  } else if (warp < 4 || warp >= 12) {
     // ---------------------------------------------------------- V to binary16
-    const int ct = threadIdx.x - 64;
+    // four warps, one per scheduler; consecutive lanes take consecutive keys of
+    // one 16-byte chunk, so each 8-lane phase of a 16-byte access covers 8
+    // distinct (swizzled) chunks
+    const int ct = 32 * (warp < 4 ? warp - 2 : warp - 10) + lane;  // 0 .. 127
     for (int j = 0; j < nblk; ++j) {
       const int half = j & 1, u = j >> 1;
       if (!__all_sync(kAll, wait_or_abort(&ctl->kv_full[half], u & 1, abort_flag, a.err))) break;
@@ -425,10 +377,8 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const TcArgs a,
       const uint8_t* vr = sm + kVRing + half * 16384;
       uint8_t* vt = sm + kVT + half * 32768;
 #pragma unroll 4
-      for (int it = 0; it < 16; ++it) {
-        // consecutive lanes take consecutive keys of one 16-byte chunk, so each
-        // 8-lane phase of a 16-byte access covers 8 distinct (swizzled) chunks
-        const int idx = ct + 64 * it, key = idx & 127, ch = idx >> 7;
+      for (int it = 0; it < 8; ++it) {
+        const int idx = ct + 128 * it, key = idx & 127, ch = idx >> 7;
         uint4 w = make_uint4(0, 0, 0, 0);
         if (key < nvalid) w = lds128(vr + (key >> 4) * 2048 + (key & 15) * 128 + ((ch ^ (key & 7)) << 4));
         const uint32_t cw[4] = {w.x, w.y, w.z, w.w};
@@ -452,16 +402,87 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const TcArgs a,
     }
   } else {
     // ---------------------------------------------------------- softmax rows
+    // Two threads per row: row r (= 8 * query token + head) in TMEM lane r; the
+    // thread of half hf takes keys 64 hf .. 64 hf + 63 of every block (two
+    // 32-column chunks), O columns 64 hf .. 64 hf + 63, and Q dims 64 hf ...
+    // The halves exchange partials through shared memory, one xchg phase each
+    // (Q amax, then every block's max, then the row sum).  Every softmax warp
+    // runs every block and arrives at every phase even after an abort (its
+    // waits then return at once), so the phases of xchg stay in step.
+    const int sw = warp - 4, hf = sw >> 2;
+    const int r = (sw & 3) * 32 + lane;
+    const int tl = r >> 3, hh = r & 7;
+    const bool row_valid = tl < n_tok;
     const uint32_t trow = tmem + ((uint32_t)((warp & 3) * 32) << 16);
-    const int qp = pos0 + min(tl, n_tok - 1);  // causal limit of the row
-    float m = -INFINITY, l = 0.f, vref = 0.f;
+    int xk = 0;  // next xchg phase
     bool ok = true;
+    auto exchange = [&](float mine, float& lo_half, float& hi_half) {
+      ctl->xbuf[xk & 1][r][hf] = mine;
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&ctl->xchg);
+      ok = __all_sync(kAll, (ok && wait_or_abort(&ctl->xchg, xk & 1, abort_flag, a.err)));
+      lo_half = ctl->xbuf[xk & 1][r][0];
+      hi_half = ctl->xbuf[xk & 1][r][1];
+      ++xk;
+    };
+
+    // Q: scaled by a power of two (max |q| of the row in [128, 256)) and split
+    // into two E4M3 terms, stored in TMEM as the A operand of S = Q K^T
+    float row_scale = a.qk_scale_log2;
+    {
+      uint32_t qw[32];  // this half's 64 bfloat16 values, two per word
+      const uint4* src = reinterpret_cast<const uint4*>(
+          a.q + ((size_t)(q0 + tok_lo + tl) * a.Hq + (size_t)h * kG + hh) * kD + 64 * hf);
+#pragma unroll
+      for (int c = 0; c < 8; ++c) {
+        const uint4 v = row_valid ? src[c] : make_uint4(0, 0, 0, 0);
+        qw[4 * c] = v.x;
+        qw[4 * c + 1] = v.y;
+        qw[4 * c + 2] = v.z;
+        qw[4 * c + 3] = v.w;
+      }
+      float am = 0.f;
+#pragma unroll
+      for (int w = 0; w < 32; ++w)
+        am = fmaxf(am, fmaxf(fabsf(bf16_bits_to_float(qw[w] & 0xFFFFu)), fabsf(bf16_bits_to_float(qw[w] >> 16))));
+      float a0, a1;
+      exchange(am, a0, a1);
+      const float amax = fmaxf(a0, a1);
+      int ex = 0;
+      if (amax > 0.f) frexpf(amax, &ex);
+      // a negative score scale goes into q, so the per-row factor is positive
+      const float sgn = a.qk_scale_log2 < 0.f ? -1.f : 1.f;
+      const float qs = sgn * (amax > 0.f ? ldexpf(1.f, 8 - ex) : 1.f);
+      row_scale = fabsf(a.qk_scale_log2) * (amax > 0.f ? ldexpf(1.f, ex - 8) : 1.f);
+      uint32_t qhi[16], qlo[16];  // 4 dims per word, dim order
+#pragma unroll
+      for (int c = 0; c < 16; ++c) {
+        const uint32_t w0 = qw[2 * c], w1 = qw[2 * c + 1];
+        const float2 x01 = make_float2(bf16_bits_to_float(w0 & 0xFFFFu) * qs, bf16_bits_to_float(w0 >> 16) * qs);
+        const float2 x23 = make_float2(bf16_bits_to_float(w1 & 0xFFFFu) * qs, bf16_bits_to_float(w1 >> 16) * qs);
+        const uint32_t h01 = __nv_cvt_float2_to_fp8x2(x01, __NV_SATFINITE, __NV_E4M3);
+        const uint32_t h23 = __nv_cvt_float2_to_fp8x2(x23, __NV_SATFINITE, __NV_E4M3);
+        const float2 d01 = unpack2<false>(e4m3x2_to_f16x2(h01));
+        const float2 d23 = unpack2<false>(e4m3x2_to_f16x2(h23));
+        const uint32_t l01 = __nv_cvt_float2_to_fp8x2(make_float2(x01.x - d01.x, x01.y - d01.y), __NV_SATFINITE, __NV_E4M3);
+        const uint32_t l23 = __nv_cvt_float2_to_fp8x2(make_float2(x23.x - d23.x, x23.y - d23.y), __NV_SATFINITE, __NV_E4M3);
+        qhi[c] = (h01 & 0xFFFFu) | (h23 << 16);
+        qlo[c] = (l01 & 0xFFFFu) | (l23 << 16);
+      }
+      tmem_st16u(trow + kQHiCol + 16 * hf, qhi);
+      tmem_st16u(trow + kQLoCol + 16 * hf, qlo);
+      tmem_wait_st();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&ctl->q_ready);
+    }
+
+    float m = -INFINITY, l = 0.f, vref = 0.f;
     for (int j = 0; j < nblk; ++j) {
       const int sb = j & 1, u = j >> 1;
       float ov = 1.f, vinv = 1.f;  // factor for this row's O accumulator; 1 / vref
       if constexpr (BLK) {  // V weights are taken relative to the largest V scale seen (<= 1)
-        ok = __all_sync(kAll, wait_or_abort(&ctl->sc_full[sb], u & 1, abort_flag, a.err));
-        if (!ok) break;
+        ok = __all_sync(kAll, ok && wait_or_abort(&ctl->sc_full[sb], u & 1, abort_flag, a.err));
         float vb = vref;
 #pragma unroll
         for (int i = 0; i < 8; ++i) vb = fmaxf(vb, ctl->sc[sb][i].y);
@@ -471,36 +492,41 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const TcArgs a,
         }
         vinv = vref > 0.f ? 1.f / vref : 0.f;
       }
-      ok = __all_sync(kAll, wait_or_abort(&ctl->s_full[sb], u & 1, abort_flag, a.err));
-      if (!ok) break;
-      tc_fence_after();
+      ok = __all_sync(kAll, ok && wait_or_abort(&ctl->s_full[sb], u & 1, abort_flag, a.err));
       // Scores in log2 units are s * f_page, f_page > 0.  S is read 32 columns
       // at a time, twice: the block max first, then the exponentials; the causal
       // mask runs only on blocks that reach the tile's first query.
       const int key0 = 128 * j;
       const bool diag = key0 + 127 > pos0;
       const uint32_t sbase = trow + sb * 128;
-      float mx = -INFINITY;
+      float mh = -INFINITY;
+      if (ok) {
+        tc_fence_after();
 #pragma unroll 1
-      for (int c = 0; c < 4; ++c) {
-        float v[32];
-        tmem_ld32(sbase + 32 * c, v);
-        tmem_wait_ld();
-        if (diag) {
+        for (int cc = 0; cc < 2; ++cc) {
+          const int c = 2 * hf + cc;
+          float v[32];
+          tmem_ld32(sbase + 32 * c, v);
+          tmem_wait_ld();
+          if (diag) {
 #pragma unroll
-          for (int e = 0; e < 32; ++e)
-            if (key0 + 32 * c + e > qp) v[e] = -INFINITY;
-        }
+            for (int e = 0; e < 32; ++e)
+              if (key0 + 32 * c + e > qp_of(pos0, tl, n_tok)) v[e] = -INFINITY;
+          }
 #pragma unroll
-        for (int hp = 0; hp < 2; ++hp) {  // the chunk's two pages
-          const float f = BLK ? row_scale * fmaxf(ctl->sc[sb][2 * c + hp].x, 1.17549435e-38f) : row_scale;
-          float t[4];
+          for (int hp = 0; hp < 2; ++hp) {  // the chunk's two pages
+            const float f = BLK ? row_scale * fmaxf(ctl->sc[sb][2 * c + hp].x, 1.17549435e-38f) : row_scale;
+            float t[4];
 #pragma unroll
-          for (int e = 0; e < 4; ++e)
-            t[e] = fmaxf(fmaxf(v[16 * hp + e], v[16 * hp + 4 + e]), fmaxf(v[16 * hp + 8 + e], v[16 * hp + 12 + e]));
-          mx = fmaxf(mx, fmaxf(fmaxf(t[0], t[1]), fmaxf(t[2], t[3])) * f);
+            for (int e = 0; e < 4; ++e)
+              t[e] = fmaxf(fmaxf(v[16 * hp + e], v[16 * hp + 4 + e]), fmaxf(v[16 * hp + 8 + e], v[16 * hp + 12 + e]));
+            mh = fmaxf(mh, fmaxf(fmaxf(t[0], t[1]), fmaxf(t[2], t[3])) * f);
+          }
         }
       }
+      float m0, m1;
+      exchange(mh, m0, m1);
+      const float mx = fmaxf(m0, m1);
       if (mx > m + 8.f) {  // the first visible block, or a max that grew by more than 2^8
         const float alpha = fast_exp2(m - mx);
         l *= alpha;
@@ -510,61 +536,66 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const TcArgs a,
       // O is rescaled once the previous block's P V is done (rarely needed).
       // Phase distance: QK(j) waited for P V(j - 2), and P V(j) needs this
       // block's P, so o_done has completed j - 1 or j phases here.
-      if (j > 0 && __any_sync(kAll, ov != 1.f)) {
+      if (ok && j > 0 && __any_sync(kAll, ov != 1.f)) {
         ok = __all_sync(kAll, wait_or_abort(&ctl->o_done, (j - 1) & 1, abort_flag, a.err));
-        if (!ok) break;
-        tc_fence_after();
+        if (ok) {
+          tc_fence_after();
 #pragma unroll 1
-        for (int c = 0; c < 4; ++c) {
-          float o[32];
-          tmem_ld32(trow + kOCol + 32 * c, o);
-          tmem_wait_ld();
+          for (int cc = 0; cc < 2; ++cc) {
+            float o[32];
+            const uint32_t oc = trow + kOCol + 64 * hf + 32 * cc;
+            tmem_ld32(oc, o);
+            tmem_wait_ld();
 #pragma unroll
-          for (int e = 0; e < 32; ++e) o[e] *= ov;
-          tmem_st32(trow + kOCol + 32 * c, o);
+            for (int e = 0; e < 32; ++e) o[e] *= ov;
+            tmem_st32(oc, o);
+          }
+          tmem_wait_st();
         }
-        tmem_wait_st();
       }
       // P in binary16 over the chunk's own S columns: keys 32c .. 32c+31 go to
       // columns 32c .. 32c+15 (the low part, fp32 mode, to 32c+16 .. 32c+31)
-      float rs = 0.f;
+      if (ok) {
+        float rs = 0.f;
 #pragma unroll 1
-      for (int c = 0; c < 4; ++c) {
-        float v[32];
-        tmem_ld32(sbase + 32 * c, v);
-        tmem_wait_ld();
-        if (diag) {
+        for (int cc = 0; cc < 2; ++cc) {
+          const int c = 2 * hf + cc;
+          float v[32];
+          tmem_ld32(sbase + 32 * c, v);
+          tmem_wait_ld();
+          if (diag) {
 #pragma unroll
-          for (int e = 0; e < 32; ++e)
-            if (key0 + 32 * c + e > qp) v[e] = -INFINITY;
-        }
+            for (int e = 0; e < 32; ++e)
+              if (key0 + 32 * c + e > qp_of(pos0, tl, n_tok)) v[e] = -INFINITY;
+          }
 #pragma unroll
-        for (int hp = 0; hp < 2; ++hp) {
-          const float f = BLK ? row_scale * fmaxf(ctl->sc[sb][2 * c + hp].x, 1.17549435e-38f) : row_scale;
-          const float vm = BLK ? ctl->sc[sb][2 * c + hp].y * vinv : 1.f;
-          float t[4] = {0.f, 0.f, 0.f, 0.f};
+          for (int hp = 0; hp < 2; ++hp) {
+            const float f = BLK ? row_scale * fmaxf(ctl->sc[sb][2 * c + hp].x, 1.17549435e-38f) : row_scale;
+            const float vm = BLK ? ctl->sc[sb][2 * c + hp].y * vinv : 1.f;
+            float t[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+            for (int e = 0; e < 16; ++e) {
+              const float pe = fast_exp2(fmaf(v[16 * hp + e], f, -m));
+              t[e & 3] += pe;
+              v[16 * hp + e] = BLK ? pe * vm : pe;
+            }
+            rs += (t[0] + t[1]) + (t[2] + t[3]);
+          }
+          uint32_t ph[16], pl[16];
 #pragma unroll
           for (int e = 0; e < 16; ++e) {
-            const float pe = fast_exp2(fmaf(v[16 * hp + e], f, -m));
-            t[e & 3] += pe;
-            v[16 * hp + e] = BLK ? pe * vm : pe;
+            ph[e] = pack2<false>(v[2 * e], v[2 * e + 1]);
+            if constexpr (PSPLIT) {
+              const float2 hv = unpack2<false>(ph[e]);
+              pl[e] = pack2<false>(v[2 * e] - hv.x, v[2 * e + 1] - hv.y);
+            }
           }
-          rs += (t[0] + t[1]) + (t[2] + t[3]);
+          tmem_st16u(sbase + 32 * c, ph);
+          if constexpr (PSPLIT) tmem_st16u(sbase + 32 * c + 16, pl);
         }
-        uint32_t ph[16], pl[16];
-#pragma unroll
-        for (int e = 0; e < 16; ++e) {
-          ph[e] = pack2<false>(v[2 * e], v[2 * e + 1]);
-          if constexpr (PSPLIT) {
-            const float2 hv = unpack2<false>(ph[e]);
-            pl[e] = pack2<false>(v[2 * e] - hv.x, v[2 * e + 1] - hv.y);
-          }
-        }
-        tmem_st16u(sbase + 32 * c, ph);
-        if constexpr (PSPLIT) tmem_st16u(sbase + 32 * c + 16, pl);
+        l += rs;
+        tmem_wait_st();
       }
-      l += rs;
-      tmem_wait_st();
       tc_fence_before();
       __syncwarp();
       if (lane == 0) {
@@ -576,17 +607,20 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const TcArgs a,
     // final P V is awaited through the one-phase drain barrier: o_done may be
     // two phases behind here, since it is only awaited to rescale O, and a
     // parity wait tells phases apart only one phase ahead.)
-    if (ok) ok = __all_sync(kAll, wait_or_abort(&ctl->drain, 0, abort_flag, a.err));
+    float l0, l1;
+    exchange(l, l0, l1);
+    const float L = l0 + l1;
+    ok = __all_sync(kAll, ok && wait_or_abort(&ctl->drain, 0, abort_flag, a.err));
     if (ok) {
       tc_fence_after();
-      const float s = l > 0.f ? (BLK ? vref : a.v_scale) / l : 0.f;
-      const size_t orow = ((size_t)(q0 + tok_lo + tl) * a.Hq + (size_t)h * kG + hh) * kD;
-#pragma unroll
-      for (int c = 0; c < 4; ++c) {
+      const float sc = L > 0.f ? (BLK ? vref : a.v_scale) / L : 0.f;
+      const size_t orow = ((size_t)(q0 + tok_lo + tl) * a.Hq + (size_t)h * kG + hh) * kD + 64 * hf;
+#pragma unroll 1
+      for (int cc = 0; cc < 2; ++cc) {
         float o[32];
-        tmem_ld32(trow + kOCol + 32 * c, o);
+        tmem_ld32(trow + kOCol + 64 * hf + 32 * cc, o);
         tmem_wait_ld();
-        if (row_valid) store_row32<OUT>(a.out, orow + 32 * c, o, s);
+        if (row_valid) store_row32<OUT>(a.out, orow + 32 * cc, o, sc);
       }
     }
   }
