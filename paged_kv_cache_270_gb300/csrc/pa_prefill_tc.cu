@@ -326,36 +326,52 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const TcArgs a,
   } else if (warp == 1) {
     // ---------------------------------------------------------- MMA issue
     if (lane == 0 && wait_or_abort(&ctl->q_ready, 0, abort_flag, a.err)) {
-      for (int j = 0; j <= nblk; ++j) {
-        if (j < nblk) {  // S(j) = Q K(j)^T, once P V(j - 2) has read P(j - 2) from this buffer
-          const int sb = j & 1, u = j >> 1;
-          if (!wait_or_abort(&ctl->kv_full[sb], u & 1, abort_flag, a.err)) break;
-          if (j >= 2 && !wait_or_abort(&ctl->o_done, (j - 2) & 1, abort_flag, a.err)) break;
+      // S(j) = Q K(j)^T into S buffer j % 2
+      auto issue_qk = [&](int j) {
+        const int sb = j & 1;
+        const uint32_t kb = smem_addr(sm + kKRing + sb * 16384);
+#pragma unroll
+        for (int t = 0; t < 2; ++t)
+#pragma unroll
+          for (int k = 0; k < 4; ++k)
+            mma_f8_ts(tmem + sb * 128, tmem + (t ? kQLoCol : kQHiCol) + 8 * k, kmajor(kb + 32 * k), kIdescQK,
+                      (uint32_t)(t | k));
+        mma_commit(&ctl->s_full[sb]);
+        mma_commit(&ctl->kv_empty[sb]);
+      };
+      // Order: S(0), S(1), then per block i: O += P(i) V(i), and once that is
+      // done (its P lives in S buffer i % 2), S(i + 2).  The tensor pipe thus
+      // runs P V and the next Q K^T back to back while the softmax works on
+      // block i + 1, whose S was computed one step earlier.
+      bool run = true;
+      for (int j = 0; j < 2 && j < nblk && run; ++j) {
+        run = wait_or_abort(&ctl->kv_full[j], 0, abort_flag, a.err);
+        if (run) {
           tc_fence_after();
-          const uint32_t kb = smem_addr(sm + kKRing + sb * 16384);
-#pragma unroll
-          for (int t = 0; t < 2; ++t)
-#pragma unroll
-            for (int k = 0; k < 4; ++k)
-              mma_f8_ts(tmem + sb * 128, tmem + (t ? kQLoCol : kQHiCol) + 8 * k, kmajor(kb + 32 * k), kIdescQK,
-                        (uint32_t)(t | k));
-          mma_commit(&ctl->s_full[sb]);
-          mma_commit(&ctl->kv_empty[sb]);
+          issue_qk(j);
         }
-        if (j >= 1) {  // O += P(i) V(i), i = j - 1, once P is written and V converted
-          const int i = j - 1, vb = i & 1;
-          if (!wait_or_abort(&ctl->p_full, i & 1, abort_flag, a.err)) break;
-          if (!wait_or_abort(&ctl->vt_full[vb], (i >> 1) & 1, abort_flag, a.err)) break;
+      }
+      for (int i = 0; i < nblk && run; ++i) {
+        const int vb = i & 1;
+        if (!wait_or_abort(&ctl->p_full, i & 1, abort_flag, a.err)) break;
+        if (!wait_or_abort(&ctl->vt_full[vb], (i >> 1) & 1, abort_flag, a.err)) break;
+        tc_fence_after();
+        const uint32_t vt = smem_addr(sm + kVT + vb * 32768);
+#pragma unroll
+        for (int part = 0; part < (PSPLIT ? 2 : 1); ++part)
+#pragma unroll
+          for (int k = 0; k < 8; ++k)
+            mma_f16_ts(tmem + kOCol, tmem + vb * 128 + 32 * (k >> 1) + 16 * part + 8 * (k & 1),
+                       mnmajor(vt + k * 2048), kIdescPV, (uint32_t)(i | k | part));
+        mma_commit(&ctl->o_done);
+        mma_commit(&ctl->vt_empty[vb]);
+        if (i + 2 < nblk) {
+          // Phase distance: o_done(i - 1) was awaited one step earlier and only
+          // P V(i) is outstanding, so o_done has completed i or i + 1 phases.
+          if (!wait_or_abort(&ctl->kv_full[vb], ((i + 2) >> 1) & 1, abort_flag, a.err)) break;
+          if (!wait_or_abort(&ctl->o_done, i & 1, abort_flag, a.err)) break;
           tc_fence_after();
-          const uint32_t vt = smem_addr(sm + kVT + vb * 32768);
-#pragma unroll
-          for (int part = 0; part < (PSPLIT ? 2 : 1); ++part)
-#pragma unroll
-            for (int k = 0; k < 8; ++k)
-              mma_f16_ts(tmem + kOCol, tmem + vb * 128 + 32 * (k >> 1) + 16 * part + 8 * (k & 1),
-                         mnmajor(vt + k * 2048), kIdescPV, (uint32_t)(i | k | part));
-          mma_commit(&ctl->o_done);
-          mma_commit(&ctl->vt_empty[vb]);
+          issue_qk(i + 2);
         }
       }
       // every MMA issued above has finished before O is read and TMEM released
