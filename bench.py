@@ -87,10 +87,12 @@ DESCRIPTION = {
 # DRAM traffic per decode launch from one ncu capture, valid only while the
 # decode source is byte-identical to the one measured.
 NCU_TRAFFIC = {
-    "source_sha256": "9667eabbeac7d0b38166dbc16e345e9c5318380efe509de57f0c437f9f696056",
+    "source_sha256": "833f28eca0c083e906d556a083e4b1bebc7e1dd5c8ed7021091df9e8a8fd9f66",
     # dram__bytes_read.sum + dram__bytes_write.sum of one decode launch
-    "bytes_per_launch": {"llama3_70b_fp8_a": 1074140000 + 5422336,
-                         "llama3_70b_fp8_b": 2152005000 + 7624448},
+    "bytes_per_launch": {"llama3_70b_fp8_a": 1073991936 + 5629696,
+                         "llama3_70b_fp8_b": 2152029696 + 6951680,
+                         "llama3_70b_fp8_block_a": 1076107008 + 4295168,
+                         "llama3_70b_fp8_block_b": 2156209408 + 5888000},
 }
 
 
