@@ -639,9 +639,20 @@ __global__ void __launch_bounds__(128) reduce_wide_kernel(const float* __restric
     __syncthreads();
     const int cnt = min(128, n - base);
     if (tid < D) {
+      // 16 independent loads per round into four partial sums: the merge is
+      // bound by load latency, not bandwidth
       const float* po = ws_o + ((size_t)row * splits + base) * D + tid;
-#pragma unroll 8
-      for (int j = 0; j < cnt; ++j) O += wsh[j] * po[(size_t)j * D];
+      float acc[4] = {0.f, 0.f, 0.f, 0.f};
+      int j = 0;
+      for (; j + 16 <= cnt; j += 16) {
+        float v[16];
+#pragma unroll
+        for (int e = 0; e < 16; ++e) v[e] = po[(size_t)(j + e) * D];
+#pragma unroll
+        for (int e = 0; e < 16; ++e) acc[e & 3] += wsh[j + e] * v[e];
+      }
+      for (; j < cnt; ++j) acc[0] += wsh[j] * po[(size_t)j * D];
+      O += (acc[0] + acc[1]) + (acc[2] + acc[3]);
     }
     __syncthreads();
   }
