@@ -341,3 +341,77 @@ def test_llama70b_block_b_full_size_sampled():
             assert np.array_equal(dev.cpu().numpy().ravel(), o[:len(ids) * 8 * 16 * 128])
             dsc = pool.scale_view(which)[torch.from_numpy(ids.astype(np.int64)).cuda()]
             assert np.array_equal(dsc.cpu().numpy(), oracle.tile_scales(DT, len(ids), 16, 8, 128, o))
+
+
+def test_no_alloc_entry_point_on_block_scaled_pools():
+    """pa_decode_no_alloc on a block-scaled pool gives exactly pa_decode's
+    result for the same split count (same kernels, partials in the fixed array)."""
+    w = W.make("llama3_70b_fp8_block_a", scale_down=32)
+    pool = new_pool(w, 0)
+    fill_both(w, pool, None)
+    q = bits_to_torch(w.q_bits(), "bf16")
+    t = torch.from_numpy(np.ascontiguousarray(w.block_tables)).cuda()
+    c = torch.from_numpy(np.ascontiguousarray(w.ctx_lens)).cuda()
+    S, Hq, D = q.shape
+    stream = torch.cuda.current_stream().cuda_stream
+    for ns in (1, 6):
+        ws_bytes = N.pa_decode_workspace_bytes(pool.handle, S, Hq, t.shape[1], ns)
+        ws = torch.empty(max(ws_bytes, 16), dtype=torch.uint8, device="cuda")
+        ref = torch.empty((S, Hq, D), dtype=torch.float32, device="cuda")
+        got = torch.full((S, Hq, D), float("nan"), dtype=torch.float32, device="cuda")
+        N.pa_decode(pool.handle, 0, ref.data_ptr(), N.PA_FP32, q.data_ptr(), t.data_ptr(),
+                    t.shape[1], c.data_ptr(), S, Hq, w.softmax_scale, ns, ws.data_ptr(), ws_bytes,
+                    stream)
+        N.pa_decode_no_alloc(pool.handle, 0, got.data_ptr(), N.PA_FP32, q.data_ptr(),
+                             t.data_ptr(), t.shape[1], c.data_ptr(), S, Hq, w.softmax_scale, ns,
+                             stream)
+        torch.cuda.synchronize()
+        assert torch.equal(got, ref)
+    assert pool.device_error() == N.PA_OK
+
+
+@pytest.mark.parametrize("H", [1, 2])
+def test_swap_records_across_layers_carry_each_layers_scales(H):
+    """3 layers: a swap record is the tiles of every layer then the scales
+    [layer][K|V][head] and zero padding to 16 bytes (8 bytes of it with one kv
+    head); swapping back into other blocks restores tiles and scales of every layer."""
+    L, nb, d = 3, 10, 64
+    pool = KVPool(L, nb, H, d, DT)
+    pool.k_cache.fill_(0)
+    pool.v_cache.fill_(0)
+    rng = np.random.default_rng(11)
+    for layer in range(L):
+        k = W.f32_to_bf16_bits(rng.standard_normal((48, H, d)).astype(np.float32) * (layer + 1))
+        v = W.f32_to_bf16_bits(rng.standard_normal((48, H, d)).astype(np.float32) * (layer + 3))
+        pool.reshape_and_cache(bits_to_torch(k, "bf16"), bits_to_torch(v, "bf16"),
+                               torch.arange(48, dtype=torch.int64, device="cuda"), layer=layer)
+    ids = torch.tensor([2, 0], dtype=torch.int32, device="cuda")
+    rec = pool.swap_block_bytes()
+    tile = H * 16 * d
+    scale_bytes = 2 * L * H * 4
+    assert rec == 2 * L * tile + -(-scale_bytes // 16) * 16
+    host = torch.empty(rec * 2, dtype=torch.uint8).pin_memory()
+    host.fill_(0x77)
+    pool.swap_out(ids, host)
+    torch.cuda.synchronize()
+    hb = host.numpy()
+    for i, b in enumerate((2, 0)):
+        r = hb[i * rec:(i + 1) * rec]
+        sc = r[2 * L * tile:2 * L * tile + scale_bytes].view(np.float32).reshape(L, 2, H)
+        for layer in range(L):
+            base = 2 * layer * tile
+            assert np.array_equal(r[base:base + tile],
+                                  pool.layer_view("k", layer)[b].cpu().numpy().ravel())
+            assert np.array_equal(r[base + tile:base + 2 * tile],
+                                  pool.layer_view("v", layer)[b].cpu().numpy().ravel())
+            assert np.array_equal(sc[layer, 0], pool.scale_view("k", layer)[b].cpu().numpy())
+            assert np.array_equal(sc[layer, 1], pool.scale_view("v", layer)[b].cpu().numpy())
+        assert np.all(r[2 * L * tile + scale_bytes:] == 0)   # padding is written as zeros
+    dst = torch.tensor([7, 9], dtype=torch.int32, device="cuda")
+    pool.swap_in(dst, host)
+    torch.cuda.synchronize()
+    for layer in range(L):
+        for which in ("k", "v"):
+            assert torch.equal(pool.layer_view(which, layer)[[7, 9]], pool.layer_view(which, layer)[[2, 0]])
+            assert torch.equal(pool.scale_view(which, layer)[[7, 9]], pool.scale_view(which, layer)[[2, 0]])
+    assert pool.device_error() == N.PA_OK
