@@ -781,6 +781,37 @@ int layer_maps(pa_pool* pool, int layer, const CUtensorMap** tk, const CUtensorM
   return PA_OK;
 }
 
+int layer_half_maps(pa_pool* pool, int layer, const CUtensorMap** tk, const CUtensorMap** tv) {
+  const pa_pool_desc& d = pool->desc;
+  const int row_bytes = d.head_dim * pool->elem_bytes;
+  if (row_bytes != 256) return fail(PA_ERR_UNSUPPORTED, "half-row maps need 256-byte rows");
+  if (pool->tmaps_half.size() != 2u * d.n_layers) {
+    pool->tmaps_half.assign(2u * d.n_layers, pa_tmap_blob{});
+    pool->tmap_half_ready.assign(d.n_layers, 0);
+  }
+  CUtensorMap* maps = reinterpret_cast<CUtensorMap*>(pool->tmaps_half.data());
+  if (!pool->tmap_half_ready[layer]) {
+    EncodeTiledFn f = encode_tiled();
+    if (!f) return fail(PA_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
+    const cuuint64_t rows = (cuuint64_t)d.num_blocks * d.n_kv_heads * d.block_size;
+    const cuuint64_t dims[2] = {256, rows};
+    const cuuint64_t strides[1] = {256};
+    const cuuint32_t box[2] = {128, 16};
+    const cuuint32_t es[2] = {1, 1};
+    for (int which = 0; which < 2; ++which) {
+      uint8_t* base = (which ? pool->v : pool->k) + (size_t)layer * pool->layer_bytes;
+      CUresult r = f(&maps[2 * layer + which], CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, base, dims, strides, box, es,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+      if (r != CUDA_SUCCESS) return fail(PA_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d)", (int)r);
+    }
+    pool->tmap_half_ready[layer] = 1;
+  }
+  *tk = &maps[2 * layer];
+  *tv = &maps[2 * layer + 1];
+  return PA_OK;
+}
+
 template <int KV, int D, int OUT>
 Dispatch make_dispatch() {
   return {&Launcher<KV, D, OUT>::info(), &Launcher<KV, D, OUT>::launch};

@@ -32,6 +32,10 @@ struct pa_pool {
   // encoded on first use by pa_decode.
   std::vector<pa_tmap_blob> tmaps;
   std::vector<char> tmap_ready;  // per layer
+  // 16-bit pools: maps whose box is one 64-element half of each row (the
+  // tensor-core prefill), encoded on first use the same way
+  std::vector<pa_tmap_blob> tmaps_half;
+  std::vector<char> tmap_half_ready;
   // Prefix cache: chain hash of a full block -> the block holding its K/V.
   // The cache owns one reference to each block it maps.
   struct prefix_entry {
@@ -69,10 +73,14 @@ namespace pa {
 // first use and kept in the pool; rows of one token of one kv head, a box is
 // one 16-token tile, 128-byte swizzled when a row is 128 or 256 bytes.
 int layer_maps(pa_pool* pool, int layer, const CUtensorMap_st** tk, const CUtensorMap_st** tv);
+// The same regions for 16-bit pools as rows of 256 bytes with a 128-byte box,
+// so one page is loaded as two 64-element halves (x = 0 and x = 128 bytes).
+int layer_half_maps(pa_pool* pool, int layer, const CUtensorMap_st** tk, const CUtensorMap_st** tv);
 
-// Chunked prefill on the tcgen05 tensor cores, for the shapes it covers (FP8
-// pools, head_dim 128, 8 query heads per KV head, bf16 or fp32 output); the
-// arguments are those of pa_prefill, already validated.
+// Chunked prefill on the tcgen05 tensor cores, for the shapes it covers
+// (head_dim 128, 8 query heads per KV head; FP8 or bfloat16 pools with bf16 or
+// fp32 output, binary16 pools with fp16 or fp32 output); the arguments are
+// those of pa_prefill, already validated.
 bool prefill_tc_supported(const pa_pool* pool, int n_q_heads, int out_dtype);
 int prefill_tc(pa_pool* pool, int layer, void* out, int out_dtype, const void* q, const int32_t* q_start,
                const int32_t* tables, int max_blocks, const int32_t* ctx, int S, int n_q_heads,

@@ -1,4 +1,4 @@
-// pa_prefill_tc.cu -- chunked prefill over an FP8 paged KV cache on the
+// pa_prefill_tc.cu -- chunked prefill over a paged KV cache on the
 // fifth-generation tensor cores (tcgen05 MMA, accumulators in tensor memory).
 //
 // Same operation as pa_prefill.cu: a chunk of new tokens per sequence, already
@@ -8,7 +8,8 @@
 // -- Gestión de caché KV de nueva generación", section 8.1: pages gathered
 // through the block table).  This kernel takes the shapes where a CTA's rows
 // fill a 128-row MMA: head_dim 128 and 8 query heads per KV head (16 query
-// tokens x 8 heads), FP8 E4M3 pages with a per-tensor or per-tile scale.
+// tokens x 8 heads), FP8 E4M3 pages with a per-tensor or per-tile scale, or
+// bfloat16 / binary16 pages.
 //
 // Design (the pages give none):
 //  * grid = (16-token query tile, kv head, sequence), longest tiles first; one
@@ -29,6 +30,13 @@
 //    of every key block and of the row's O): S comes out of TMEM, the max moves
 //    only when it grows by more than 2^8 (so P <= 2^8), and then the threads
 //    rescale their halves of the O row in TMEM before the next P V.
+//  * 16-bit pools take the same pipeline without the conversion: a page
+//    arrives as two 64-dim halves (two TMA boxes of 128-byte rows), which is
+//    at once the K-major layout of K and the MN-major layout of V, so both
+//    MMAs read the ring in place (Q in TMEM unsplit; P in the pool's type, with
+//    its low part whenever P in bfloat16 would be too coarse).  The ring has
+//    three slots, as a V slot stays busy until its P V is done; the converter
+//    warps only zero the last block's V rows past the tile.
 //  * warp 1 allocates TMEM and one lane issues every MMA; completion is
 //    signalled through mbarriers (tcgen05.commit).  Every wait is bounded: a
 //    timeout records PA_ERR_TIMEOUT, raises a CTA-wide abort flag that ends
@@ -52,29 +60,48 @@ constexpr int kThreads = 448;   // 14 warps: producer, MMA, 4 converters, 8 soft
 constexpr unsigned kAll = 0xffffffffu;
 constexpr uint32_t kTmemCols = 512;
 // TMEM columns (one lane per row): S(j) in buffer j % 2 at 0 / 128, overwritten
-// by P(j) in binary16: keys 32c .. 32c+31 in columns 32c .. 32c+15 of the
-// buffer (P's low part, fp32-output mode, in 32c+16 .. 32c+31); O at 256; the
-// two E4M3 terms of Q at 384 and 416.
+// by P(j) in 16 bits: keys 32c .. 32c+31 in columns 32c .. 32c+15 of the buffer
+// (P's low part, where used, in 32c+16 .. 32c+31); O at 256; Q at 384 .. 447
+// (FP8 pools: its two E4M3 terms at 384 and 416; 16-bit pools: Q itself).
 constexpr uint32_t kOCol = 256;
 constexpr uint32_t kQHiCol = 384;
 constexpr uint32_t kQLoCol = 416;
 
-// shared memory, from a 1024-byte aligned base
-constexpr int kKRing = 0;             // [2][8 pages][16 keys][128 B] E4M3 (TMA, swizzled)
-constexpr int kVRing = kKRing + 32768;
-constexpr int kVT = kVRing + 32768;   // [2][2 dim blocks][128 keys][128 B] binary16, swizzled
-__host__ __device__ constexpr int data_bytes(bool) { return kVT + 65536; }
+// Cache types this kernel takes
+enum Kind { K_E4M3 = 0, K_E4M3B = 1, K_BF16 = 2, K_F16 = 3 };
 
 struct Ctrl {
-  uint64_t kv_full[2], kv_empty[2], s_full[2], vt_full[2], vt_empty[2];
+  uint64_t kv_full[3], kv_empty[3], s_full[2], vt_full[2], vt_empty[2];
   uint64_t sc_full[2], sc_empty[2], q_ready, p_full, o_done, drain, xchg;
+  uint64_t tail_ready, tail_done;  // 16-bit pools: the last block's V rows past the tile are zeroed
   float2 sc[2][8];  // block-scaled pools: (K scale, V scale) of each page of a ring block
   float xbuf[2][128][2];  // the two half-row threads' partials (Q amax, block max, row sum)
   uint32_t tmem;
   int abort;
 };
-constexpr int smem_bytes(bool psplit) { return 1024 + data_bytes(psplit) + (int)sizeof(Ctrl); }
-static_assert(smem_bytes(true) <= 232448, "shared memory budget");
+
+// Shared memory, from a 1024-byte aligned base.  A ring slot holds one
+// 128-key block (8 pages) of K and of V as the TMA wrote them, 128-byte
+// swizzled.  FP8: K and V slots of 16 KiB ([8 pages][16 keys][128 B]), two
+// slots, plus two binary16 V blocks converted for the MMA ([2 dim blocks][128
+// keys][128 B]).  16-bit pools: each page arrives as two 64-dim halves, so a
+// slot is [2 dim halves][128 keys][128 B] (32 KiB) -- the K-major layout for
+// K and the MN-major layout for V, both read in place; three slots, as a V
+// slot is held until its P V is done.
+template <int KIND>
+struct Lay {
+  static constexpr bool kF8 = KIND == K_E4M3 || KIND == K_E4M3B;
+  static constexpr bool kBlk = KIND == K_E4M3B;
+  static constexpr bool kBf = KIND == K_BF16;
+  static constexpr int kRing = kF8 ? 2 : 3;
+  static constexpr int kSlot = kF8 ? 16384 : 32768;
+  static constexpr int kKRing = 0;
+  static constexpr int kVRing = kRing * kSlot;
+  static constexpr int kVT = kVRing + kRing * kSlot;
+  static constexpr int kData = kF8 ? kVT + 65536 : kVT;
+  static constexpr int kSmem = 1024 + kData + (int)sizeof(Ctrl);
+  static_assert(kSmem <= 232448, "shared memory budget");
+};
 
 struct TcArgs {
   const uint16_t* q;
@@ -102,10 +129,12 @@ __device__ __forceinline__ uint64_t kmajor(uint32_t saddr) { return sw128_desc(s
 // MN-major operand: 64-element blocks of the MN dim 16 KiB apart, 8 K-rows 1024 bytes apart.
 __device__ __forceinline__ uint64_t mnmajor(uint32_t saddr) { return sw128_desc(saddr, 16384, 1024); }
 
-// Instruction descriptors: fp32 accumulate, M = N = 128; S = E4M3 x E4M3 with
-// both operands K-major; O = binary16 x binary16 with B MN-major.
+// Instruction descriptors: fp32 accumulate, M = N = 128; operand type field
+// 0 = binary16 (kind::f16) / E4M3 (kind::f8f6f4), 1 = bfloat16; Q K^T with both
+// operands K-major; P V with B MN-major.
 constexpr uint32_t kIdescQK = (1u << 4) | ((128u >> 3) << 17) | ((128u >> 4) << 24);
 constexpr uint32_t kIdescPV = (1u << 4) | (1u << 16) | ((128u >> 3) << 17) | ((128u >> 4) << 24);
+constexpr uint32_t kBf16Types = (1u << 7) | (1u << 10);
 
 // D (TMEM) = A x B (+ D): A in tensor memory (row i in lane i, consecutive K
 // elements packed little-endian into 32-bit columns), B in shared memory.
@@ -208,6 +237,12 @@ __device__ __forceinline__ void store_row32(void* out, size_t idx, const float* 
     float4* o = reinterpret_cast<float4*>(static_cast<float*>(out) + idx);
 #pragma unroll
     for (int i = 0; i < 8; ++i) o[i] = make_float4(v[4 * i] * s, v[4 * i + 1] * s, v[4 * i + 2] * s, v[4 * i + 3] * s);
+  } else if constexpr (OUT == PA_FP16) {
+    uint4* o = reinterpret_cast<uint4*>(static_cast<__half*>(out) + idx);
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+      o[i] = make_uint4(pack2<false>(v[8 * i] * s, v[8 * i + 1] * s), pack2<false>(v[8 * i + 2] * s, v[8 * i + 3] * s),
+                        pack2<false>(v[8 * i + 4] * s, v[8 * i + 5] * s), pack2<false>(v[8 * i + 6] * s, v[8 * i + 7] * s));
   } else {
     uint4* o = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(out) + idx);
 #pragma unroll
@@ -217,13 +252,16 @@ __device__ __forceinline__ void store_row32(void* out, size_t idx, const float* 
   }
 }
 
-template <bool BLK, int OUT, bool PSPLIT>
+template <int KIND, int OUT, bool PSPLIT>
 __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const TcArgs a,
                                                                   const __grid_constant__ CUtensorMap tmk,
                                                                   const __grid_constant__ CUtensorMap tmv) {
+  using L = Lay<KIND>;
+  constexpr bool F8 = L::kF8, BLK = L::kBlk, BF = L::kBf;
+  constexpr int R = L::kRing;
   extern __shared__ __align__(16) uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  Ctrl* ctl = reinterpret_cast<Ctrl*>(sm + data_bytes(PSPLIT));
+  Ctrl* ctl = reinterpret_cast<Ctrl*>(sm + L::kData);
   volatile int* abort_flag = &ctl->abort;
 
   const int qt = gridDim.x - 1 - blockIdx.x, h = blockIdx.y, seq = blockIdx.z;
@@ -244,9 +282,12 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const TcArgs a,
   const int nblk = (npages + 7) / 8;
 
   if (threadIdx.x == 0) {
-    for (int i = 0; i < 2; ++i) {
+    for (int i = 0; i < R; ++i) {
       mbar_init(&ctl->kv_full[i], 1);
-      mbar_init(&ctl->kv_empty[i], 5);  // the QK MMAs' commit + the four converter warps
+      // FP8: the QK MMAs' commit + the four converter warps; 16-bit: the P V MMAs' commit
+      mbar_init(&ctl->kv_empty[i], F8 ? 5 : 1);
+    }
+    for (int i = 0; i < 2; ++i) {
       mbar_init(&ctl->s_full[i], 1);
       mbar_init(&ctl->vt_full[i], 4);
       mbar_init(&ctl->vt_empty[i], 1);
@@ -258,6 +299,8 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const TcArgs a,
     mbar_init(&ctl->o_done, 1);
     mbar_init(&ctl->drain, 1);
     mbar_init(&ctl->xchg, 8);
+    mbar_init(&ctl->tail_ready, 1);
+    mbar_init(&ctl->tail_done, 4);
     ctl->abort = 0;
     fence_barrier_init();
   }
@@ -281,8 +324,8 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const TcArgs a,
     const uint64_t policy = l2_evict_first_policy();
     int issued = 0;
     for (int j = 0; j < nblk; ++j) {
-      const int half = j & 1, u = j >> 1;
-      if (j >= 2 && !__all_sync(kAll, wait_or_abort(&ctl->kv_empty[half], (u - 1) & 1, abort_flag, a.err))) break;
+      const int half = j % R, u = j / R;
+      if (j >= R && !__all_sync(kAll, wait_or_abort(&ctl->kv_empty[half], (u - 1) & 1, abort_flag, a.err))) break;
       const int cnt = min(8, npages - 8 * j);
       int phys = 0;
       float sk = 1.f, sv = 0.f;
@@ -308,36 +351,55 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const TcArgs a,
           mbar_arrive(&ctl->sc_full[half]);
         }
       }
-      if (lane == 0) mbar_arrive_expect_tx(&ctl->kv_full[half], (uint32_t)cnt * 4096u);
+      if (lane == 0) mbar_arrive_expect_tx(&ctl->kv_full[half], (uint32_t)cnt * (F8 ? 4096u : 8192u));
       for (int i = 0; i < cnt; ++i) {
         const int ph = __shfl_sync(kAll, phys, i);
         if (lane == 0) {
           const int row0 = (ph * a.Hkv + h) * 16;
-          tma_load_2d(sm + kKRing + half * 16384 + i * 2048, &tmk, 0, row0, &ctl->kv_full[half], policy);
-          tma_load_2d(sm + kVRing + half * 16384 + i * 2048, &tmv, 0, row0, &ctl->kv_full[half], policy);
+          uint8_t* kd = sm + L::kKRing + half * L::kSlot + i * 2048;
+          uint8_t* vd = sm + L::kVRing + half * L::kSlot + i * 2048;
+          if constexpr (F8) {
+            tma_load_2d(kd, &tmk, 0, row0, &ctl->kv_full[half], policy);
+            tma_load_2d(vd, &tmv, 0, row0, &ctl->kv_full[half], policy);
+          } else {  // the two 64-dim (128-byte) halves of each 256-byte row
+#pragma unroll
+            for (int hh = 0; hh < 2; ++hh) {
+              tma_load_2d(kd + hh * 16384, &tmk, 128 * hh, row0, &ctl->kv_full[half], policy);
+              tma_load_2d(vd + hh * 16384, &tmv, 128 * hh, row0, &ctl->kv_full[half], policy);
+            }
+          }
         }
       }
       ++issued;
     }
     // no copy may still target shared memory when the CTA exits
     if (lane == 0)
-      for (int j = max(0, issued - 2); j < issued; ++j)
-        if (!mbar_wait(&ctl->kv_full[j & 1], (j >> 1) & 1)) record_error(a.err, PA_ERR_TIMEOUT);
+      for (int j = max(0, issued - R); j < issued; ++j)
+        if (!mbar_wait(&ctl->kv_full[j % R], (j / R) & 1)) record_error(a.err, PA_ERR_TIMEOUT);
   } else if (warp == 1) {
     // ---------------------------------------------------------- MMA issue
     if (lane == 0 && wait_or_abort(&ctl->q_ready, 0, abort_flag, a.err)) {
       // S(j) = Q K(j)^T into S buffer j % 2
       auto issue_qk = [&](int j) {
         const int sb = j & 1;
-        const uint32_t kb = smem_addr(sm + kKRing + sb * 16384);
+        if constexpr (!F8)
+          if (j == nblk - 1) mbar_arrive(&ctl->tail_ready);  // its pages have landed
+        const uint32_t kb = smem_addr(sm + L::kKRing + (j % R) * L::kSlot);
+        if constexpr (F8) {
 #pragma unroll
-        for (int t = 0; t < 2; ++t)
+          for (int t = 0; t < 2; ++t)
 #pragma unroll
-          for (int k = 0; k < 4; ++k)
-            mma_f8_ts(tmem + sb * 128, tmem + (t ? kQLoCol : kQHiCol) + 8 * k, kmajor(kb + 32 * k), kIdescQK,
-                      (uint32_t)(t | k));
+            for (int k = 0; k < 4; ++k)
+              mma_f8_ts(tmem + sb * 128, tmem + (t ? kQLoCol : kQHiCol) + 8 * k, kmajor(kb + 32 * k), kIdescQK,
+                        (uint32_t)(t | k));
+        } else {  // 16 dims per MMA: dim half k / 4, 32 bytes into its rows
+#pragma unroll
+          for (int k = 0; k < 8; ++k)
+            mma_f16_ts(tmem + sb * 128, tmem + kQHiCol + 8 * k, kmajor(kb + (k >> 2) * 16384 + (k & 3) * 32),
+                       kIdescQK | (BF ? kBf16Types : 0u), (uint32_t)k);
+        }
         mma_commit(&ctl->s_full[sb]);
-        mma_commit(&ctl->kv_empty[sb]);
+        if constexpr (F8) mma_commit(&ctl->kv_empty[j % R]);  // K is read; V was converted
       };
       // Order: S(0), S(1), then per block i: O += P(i) V(i), and once that is
       // done (its P lives in S buffer i % 2), S(i + 2).  The tensor pipe thus
@@ -345,7 +407,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const TcArgs a,
       // block i + 1, whose S was computed one step earlier.
       bool run = true;
       for (int j = 0; j < 2 && j < nblk && run; ++j) {
-        run = wait_or_abort(&ctl->kv_full[j], 0, abort_flag, a.err);
+        run = wait_or_abort(&ctl->kv_full[j % R], (j / R) & 1, abort_flag, a.err);
         if (run) {
           tc_fence_after();
           issue_qk(j);
@@ -354,21 +416,27 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const TcArgs a,
       for (int i = 0; i < nblk && run; ++i) {
         const int vb = i & 1;
         if (!wait_or_abort(&ctl->p_full, i & 1, abort_flag, a.err)) break;
-        if (!wait_or_abort(&ctl->vt_full[vb], (i >> 1) & 1, abort_flag, a.err)) break;
+        if constexpr (F8) {
+          if (!wait_or_abort(&ctl->vt_full[vb], (i >> 1) & 1, abort_flag, a.err)) break;
+        } else {
+          if (i == nblk - 1 && !wait_or_abort(&ctl->tail_done, 0, abort_flag, a.err)) break;
+        }
         tc_fence_after();
-        const uint32_t vt = smem_addr(sm + kVT + vb * 32768);
+        // B: the binary16 V block (FP8 pools) or the V ring slot itself (16-bit pools)
+        const uint32_t vt = F8 ? smem_addr(sm + L::kVT + vb * 32768) : smem_addr(sm + L::kVRing + (i % R) * L::kSlot);
 #pragma unroll
         for (int part = 0; part < (PSPLIT ? 2 : 1); ++part)
 #pragma unroll
           for (int k = 0; k < 8; ++k)
             mma_f16_ts(tmem + kOCol, tmem + vb * 128 + 32 * (k >> 1) + 16 * part + 8 * (k & 1),
-                       mnmajor(vt + k * 2048), kIdescPV, (uint32_t)(i | k | part));
+                       mnmajor(vt + k * 2048), kIdescPV | (BF ? kBf16Types : 0u), (uint32_t)(i | k | part));
         mma_commit(&ctl->o_done);
-        mma_commit(&ctl->vt_empty[vb]);
+        if constexpr (F8) mma_commit(&ctl->vt_empty[vb]);
+        else mma_commit(&ctl->kv_empty[i % R]);  // K and V of block i are read
         if (i + 2 < nblk) {
           // Phase distance: o_done(i - 1) was awaited one step earlier and only
           // P V(i) is outstanding, so o_done has completed i or i + 1 phases.
-          if (!wait_or_abort(&ctl->kv_full[vb], ((i + 2) >> 1) & 1, abort_flag, a.err)) break;
+          if (!wait_or_abort(&ctl->kv_full[(i + 2) % R], ((i + 2) / R) & 1, abort_flag, a.err)) break;
           if (!wait_or_abort(&ctl->o_done, i & 1, abort_flag, a.err)) break;
           tc_fence_after();
           issue_qk(i + 2);
@@ -385,13 +453,34 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const TcArgs a,
     // one 16-byte chunk, so each 8-lane phase of a 16-byte access covers 8
     // distinct (swizzled) chunks
     const int ct = 32 * (warp < 4 ? warp - 2 : warp - 10) + lane;  // 0 .. 127
-    for (int j = 0; j < nblk; ++j) {
+    if constexpr (!F8) {
+      // 16-bit pools: nothing to convert, but V is read in place, so the rows
+      // of the last block past the tile's last query (stale slots of its last
+      // page, pages not loaded) are zeroed: P is 0 there, and 0 x NaN is not.
+      // The MMA warp signals once that block's copies have landed (its ring
+      // slot is used for nothing else afterwards, so kv_full stays complete).
+      const int j = nblk - 1;
+      bool go = __all_sync(kAll, wait_or_abort(&ctl->tail_ready, 0, abort_flag, a.err));
+      go = go && __all_sync(kAll, wait_or_abort(&ctl->kv_full[j % R], (j / R) & 1, abort_flag, a.err));
+      if (go) {
+        const int nvalid = pos_last + 1 - 128 * j;  // 1 .. 128
+        uint8_t* vr = sm + L::kVRing + (j % R) * L::kSlot;
+        for (int idx = ct; idx < (128 - nvalid) * 16; idx += 128) {  // 16 chunks of 16 B per key
+          const int key = nvalid + (idx >> 4), c = idx & 15;
+          *reinterpret_cast<uint4*>(vr + (c >> 3) * 16384 + key * 128 + (c & 7) * 16) = make_uint4(0, 0, 0, 0);
+        }
+        fence_proxy_async();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&ctl->tail_done);
+      }
+    }
+    for (int j = 0; j < (F8 ? nblk : 0); ++j) {
       const int half = j & 1, u = j >> 1;
       if (!__all_sync(kAll, wait_or_abort(&ctl->kv_full[half], u & 1, abort_flag, a.err))) break;
       if (j >= 2 && !__all_sync(kAll, wait_or_abort(&ctl->vt_empty[half], (u - 1) & 1, abort_flag, a.err))) break;
       const int nvalid = min(128, pos_last + 1 - 128 * j);  // keys past the last query: zero
-      const uint8_t* vr = sm + kVRing + half * 16384;
-      uint8_t* vt = sm + kVT + half * 32768;
+      const uint8_t* vr = sm + L::kVRing + half * L::kSlot;
+      uint8_t* vt = sm + L::kVT + half * 32768;
 #pragma unroll 4
       for (int it = 0; it < 8; ++it) {
         const int idx = ct + 128 * it, key = idx & 127, ch = idx >> 7;
@@ -446,7 +535,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const TcArgs a,
     // into two E4M3 terms, stored in TMEM as the A operand of S = Q K^T
     float row_scale = a.qk_scale_log2;
     {
-      uint32_t qw[32];  // this half's 64 bfloat16 values, two per word
+      uint32_t qw[32];  // this half's 64 16-bit values, two per word
       const uint4* src = reinterpret_cast<const uint4*>(
           a.q + ((size_t)(q0 + tok_lo + tl) * a.Hq + (size_t)h * kG + hh) * kD + 64 * hf);
 #pragma unroll
@@ -458,11 +547,23 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const TcArgs a,
         qw[4 * c + 3] = v.w;
       }
       float am = 0.f;
+      if constexpr (F8) {
 #pragma unroll
-      for (int w = 0; w < 32; ++w)
-        am = fmaxf(am, fmaxf(fabsf(bf16_bits_to_float(qw[w] & 0xFFFFu)), fabsf(bf16_bits_to_float(qw[w] >> 16))));
+        for (int w = 0; w < 32; ++w)
+          am = fmaxf(am, fmaxf(fabsf(bf16_bits_to_float(qw[w] & 0xFFFFu)), fabsf(bf16_bits_to_float(qw[w] >> 16))));
+      }
       float a0, a1;
-      exchange(am, a0, a1);
+      exchange(am, a0, a1);  // (16-bit pools exchange nothing useful; the phase keeps step)
+      if constexpr (!F8) {
+        // 16-bit pools: Q itself is the A operand, exact; a negative score scale
+        // flips its signs so the per-row factor is positive
+        row_scale = fabsf(a.qk_scale_log2);
+        if (a.qk_scale_log2 < 0.f) {
+#pragma unroll
+          for (int w = 0; w < 32; ++w) qw[w] ^= 0x80008000u;
+        }
+        tmem_st32u(trow + kQHiCol + 32 * hf, qw);
+      } else {
       const float amax = fmaxf(a0, a1);
       int ex = 0;
       if (amax > 0.f) frexpf(amax, &ex);
@@ -487,6 +588,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const TcArgs a,
       }
       tmem_st16u(trow + kQHiCol + 16 * hf, qhi);
       tmem_st16u(trow + kQLoCol + 16 * hf, qlo);
+      }
       tmem_wait_st();
       tc_fence_before();
       __syncwarp();
@@ -597,13 +699,13 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const TcArgs a,
             }
             rs += (t[0] + t[1]) + (t[2] + t[3]);
           }
-          uint32_t ph[16], pl[16];
+          uint32_t ph[16], pl[16];  // in V's type: bfloat16 for bfloat16 pools, else binary16
 #pragma unroll
           for (int e = 0; e < 16; ++e) {
-            ph[e] = pack2<false>(v[2 * e], v[2 * e + 1]);
+            ph[e] = pack2<BF>(v[2 * e], v[2 * e + 1]);
             if constexpr (PSPLIT) {
-              const float2 hv = unpack2<false>(ph[e]);
-              pl[e] = pack2<false>(v[2 * e] - hv.x, v[2 * e + 1] - hv.y);
+              const float2 hv = unpack2<BF>(ph[e]);
+              pl[e] = pack2<BF>(v[2 * e] - hv.x, v[2 * e + 1] - hv.y);
             }
           }
           tmem_st16u(sbase + 32 * c, ph);
@@ -655,20 +757,20 @@ struct TcInfo {
   bool configured[128];
 };
 
-template <bool BLK, int OUT, bool PSPLIT>
+template <int KIND, int OUT, bool PSPLIT>
 TcInfo& tc_info() {
-  static TcInfo ti = {reinterpret_cast<const void*>(&prefill_tc_kernel<BLK, OUT, PSPLIT>), smem_bytes(PSPLIT), {}};
+  static TcInfo ti = {reinterpret_cast<const void*>(&prefill_tc_kernel<KIND, OUT, PSPLIT>), Lay<KIND>::kSmem, {}};
   return ti;
 }
 
-template <bool BLK, int OUT, bool PSPLIT>
+template <int KIND, int OUT, bool PSPLIT>
 cudaError_t tc_launch(const TcArgs& a, const CUtensorMap* tk, const CUtensorMap* tv, int tiles, int S,
                       cudaStream_t st) {
   static std::mutex mu;
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
-  TcInfo& ti = tc_info<BLK, OUT, PSPLIT>();
+  TcInfo& ti = tc_info<KIND, OUT, PSPLIT>();
   {
     std::lock_guard<std::mutex> lock(mu);
     if (dev < 0 || dev >= 128) return cudaErrorInvalidDevice;
@@ -678,7 +780,7 @@ cudaError_t tc_launch(const TcArgs& a, const CUtensorMap* tk, const CUtensorMap*
       ti.configured[dev] = true;
     }
   }
-  prefill_tc_kernel<BLK, OUT, PSPLIT><<<dim3(tiles, a.Hkv, S), kThreads, ti.smem, st>>>(a, *tk, *tv);
+  prefill_tc_kernel<KIND, OUT, PSPLIT><<<dim3(tiles, a.Hkv, S), kThreads, ti.smem, st>>>(a, *tk, *tv);
   return cudaGetLastError();
 }
 
@@ -686,16 +788,26 @@ cudaError_t tc_launch(const TcArgs& a, const CUtensorMap* tk, const CUtensorMap*
 
 bool prefill_tc_supported(const pa_pool* pool, int n_q_heads, int out_dtype) {
   const pa_pool_desc& d = pool->desc;
-  return (d.kv_dtype == PA_FP8_E4M3 || d.kv_dtype == PA_FP8_E4M3_BLOCK) && d.head_dim == kD &&
-         n_q_heads == kG * d.n_kv_heads && (out_dtype == PA_BF16 || out_dtype == PA_FP32);
+  if (d.head_dim != kD || n_q_heads != kG * d.n_kv_heads) return false;
+  switch (d.kv_dtype) {
+    case PA_FP8_E4M3:
+    case PA_FP8_E4M3_BLOCK:
+    case PA_BF16:
+      return out_dtype == PA_BF16 || out_dtype == PA_FP32;
+    case PA_FP16:
+      return out_dtype == PA_FP16 || out_dtype == PA_FP32;
+    default:
+      return false;
+  }
 }
 
 int prefill_tc(pa_pool* pool, int layer, void* out, int out_dtype, const void* q, const int32_t* q_start,
                const int32_t* tables, int max_blocks, const int32_t* ctx, int S, int n_q_heads,
                int max_chunk, float softmax_scale, unsigned int* err, cudaStream_t st) {
   const pa_pool_desc& d = pool->desc;
+  const bool f8 = d.kv_dtype == PA_FP8_E4M3 || d.kv_dtype == PA_FP8_E4M3_BLOCK;
   const CUtensorMap_st *tk = nullptr, *tv = nullptr;
-  int rc = layer_maps(pool, layer, &tk, &tv);
+  int rc = f8 ? layer_maps(pool, layer, &tk, &tv) : layer_half_maps(pool, layer, &tk, &tv);
   if (rc) return rc;
   TcArgs a;
   a.q = static_cast<const uint16_t*>(q);
@@ -709,18 +821,31 @@ int prefill_tc(pa_pool* pool, int layer, void* out, int out_dtype, const void* q
   a.Hq = n_q_heads;
   a.Hkv = d.n_kv_heads;
   a.num_blocks = d.num_blocks;
-  a.qk_scale_log2 = softmax_scale * 1.4426950408889634f * (pool->block_scaled ? 1.f : d.k_scale);
-  a.v_scale = pool->block_scaled ? 1.f : d.v_scale;
+  const bool static_fp8 = d.kv_dtype == PA_FP8_E4M3;
+  a.qk_scale_log2 = softmax_scale * 1.4426950408889634f * (static_fp8 ? d.k_scale : 1.f);
+  a.v_scale = static_fp8 ? d.v_scale : 1.f;
   a.err = err;
   const int tiles = (max_chunk + 15) / 16;
-  cudaError_t e;
   const bool f32 = out_dtype == PA_FP32;
-  if (pool->block_scaled)
-    e = f32 ? tc_launch<true, PA_FP32, true>(a, tk, tv, tiles, S, st)
-            : tc_launch<true, PA_BF16, false>(a, tk, tv, tiles, S, st);
-  else
-    e = f32 ? tc_launch<false, PA_FP32, true>(a, tk, tv, tiles, S, st)
-            : tc_launch<false, PA_BF16, false>(a, tk, tv, tiles, S, st);
+  cudaError_t e;
+  switch (d.kv_dtype) {
+    case PA_FP8_E4M3:
+      e = f32 ? tc_launch<K_E4M3, PA_FP32, true>(a, tk, tv, tiles, S, st)
+              : tc_launch<K_E4M3, PA_BF16, false>(a, tk, tv, tiles, S, st);
+      break;
+    case PA_FP8_E4M3_BLOCK:
+      e = f32 ? tc_launch<K_E4M3B, PA_FP32, true>(a, tk, tv, tiles, S, st)
+              : tc_launch<K_E4M3B, PA_BF16, false>(a, tk, tv, tiles, S, st);
+      break;
+    case PA_BF16:  // P in bfloat16 carries 8 bits: always split into two parts
+      e = f32 ? tc_launch<K_BF16, PA_FP32, true>(a, tk, tv, tiles, S, st)
+              : tc_launch<K_BF16, PA_BF16, true>(a, tk, tv, tiles, S, st);
+      break;
+    default:
+      e = f32 ? tc_launch<K_F16, PA_FP32, true>(a, tk, tv, tiles, S, st)
+              : tc_launch<K_F16, PA_FP16, false>(a, tk, tv, tiles, S, st);
+      break;
+  }
   if (e != cudaSuccess) return fail(PA_ERR_CUDA, "prefill (tcgen05) launch: %s", cudaGetErrorString(e));
   return PA_OK;
 }

@@ -1,7 +1,8 @@
 """GPU parity of the tensor-core (tcgen05) chunked prefill against the fp64
-oracle.  pa_prefill takes that path for FP8 pools with head_dim 128 and 8 query
-heads per KV head; these cases make it run many 128-key blocks (the two-block
-ring wraps many times), ragged query tiles, causal diagonals at every offset,
+oracle.  pa_prefill takes that path for pools with head_dim 128 and 8 query
+heads per KV head (FP8 static or block-scaled, bfloat16, binary16); these cases
+make it run many 128-key blocks (the ring
+wraps many times), ragged query tiles, causal diagonals at every offset,
 both FP8 scalings and both output types, and scores that grow block after
 block so the running max moves by more than 2^8 and O is rescaled in tensor
 memory."""
@@ -47,18 +48,18 @@ def _setup(kv_dtype, pairs, seed, Hkv=2, k_gain_per_block=1.0, q_away_from_zero=
         k, v = w.kv_bits(s, 0, int(n))
         if k_gain_per_block != 1.0:
             g = np.power(k_gain_per_block, np.arange(int(n)) // 128).astype(np.float32)
-            k = W.f32_to_bf16_bits(W.bits_to_f32(k, "bf16") * g[:, None, None])
+            k = _cast(w, W.bits_to_f32(k, w.in_dtype) * g[:, None, None])
         kv.append((k, v))
     if kv_dtype == "fp8_e4m3":
-        ka = max(float(np.abs(W.bits_to_f32(k, "bf16")).max()) for k, _ in kv)
-        va = max(float(np.abs(W.bits_to_f32(v, "bf16")).max()) for _, v in kv)
+        ka = max(float(np.abs(W.bits_to_f32(k, w.in_dtype)).max()) for k, _ in kv)
+        va = max(float(np.abs(W.bits_to_f32(v, w.in_dtype)).max()) for _, v in kv)
         w.k_scale = float(np.float32(ka) / np.float32(448))
         w.v_scale = float(np.float32(va) / np.float32(448))
     pool = new_pool(w, 0xFF)
     op = oracle_pools(w, 0xFF)
     for s, (k, v) in enumerate(kv):
         slots = w.slots(s, 0, int(ctx[s]))
-        pool.reshape_and_cache(bits_to_torch(k, "bf16"), bits_to_torch(v, "bf16"),
+        pool.reshape_and_cache(bits_to_torch(k, w.in_dtype), bits_to_torch(v, w.in_dtype),
                                torch.from_numpy(slots).cuda())
         assert oracle.reshape_and_cache(kv_dtype, nb, 16, Hkv, 128, k, v, slots, w.k_scale,
                                         w.v_scale, *op) == 0
@@ -66,16 +67,20 @@ def _setup(kv_dtype, pairs, seed, Hkv=2, k_gain_per_block=1.0, q_away_from_zero=
     qf = rng.standard_normal((T, 8 * Hkv, 128)).astype(np.float32)
     if q_away_from_zero:  # |q| in [0.5, 2): the two-term E4M3 split of q is exact
         qf = (np.sign(qf) * rng.uniform(0.5, 2.0, qf.shape)).astype(np.float32)
-    q = W.f32_to_bf16_bits(qf)
+    q = _cast(w, qf)
     q_start = np.concatenate([[0], np.cumsum(chunks)]).astype(np.int32)
     return w, pool, op, q, q_start, chunks
 
 
+def _cast(w, x):
+    return W.f32_to_f16_bits(x) if w.in_dtype == "fp16" else W.f32_to_bf16_bits(x)
+
+
 def _run(w, pool, op, q, q_start, chunks):
-    ref = oracle.paged_prefill(w.kv_dtype, "bf16", w.num_blocks, 16, w.n_kv_heads, 128, op[0],
+    ref = oracle.paged_prefill(w.kv_dtype, w.in_dtype, w.num_blocks, 16, w.n_kv_heads, 128, op[0],
                                op[1], w.k_scale, w.v_scale, q, q_start, w.block_tables, w.ctx_lens,
                                w.softmax_scale)
-    args = (bits_to_torch(q, "bf16"), torch.from_numpy(q_start).cuda(),
+    args = (bits_to_torch(q, w.in_dtype), torch.from_numpy(q_start).cuda(),
             torch.from_numpy(w.block_tables).cuda(), torch.from_numpy(w.ctx_lens).cuda())
     out = pool.prefill(*args, max_chunk=max(chunks), softmax_scale=w.softmax_scale)
     out32 = pool.prefill(*args, max_chunk=max(chunks), softmax_scale=w.softmax_scale,
@@ -87,7 +92,7 @@ def _run(w, pool, op, q, q_start, chunks):
     return out32, ref
 
 
-@pytest.mark.parametrize("kv_dtype", ["fp8_e4m3", "fp8_e4m3_block"])
+@pytest.mark.parametrize("kv_dtype", ["fp8_e4m3", "fp8_e4m3_block", "bf16", "fp16"])
 def test_long_histories_ragged_tiles(kv_dtype):
     # (history, chunk): 1-token chunks, chunks ending inside a page, a chunk
     # whose diagonal crosses a 128-key block, 3000 keys of history (24 blocks)
@@ -96,7 +101,7 @@ def test_long_histories_ragged_tiles(kv_dtype):
     _run(w, pool, op, q, q_start, chunks)
 
 
-@pytest.mark.parametrize("kv_dtype", ["fp8_e4m3", "fp8_e4m3_block"])
+@pytest.mark.parametrize("kv_dtype", ["fp8_e4m3", "fp8_e4m3_block", "bf16", "fp16"])
 def test_scores_growing_block_after_block(kv_dtype):
     """K doubles every 128 tokens: each block's scores exceed the previous
     max by far more than 2^8 in the exponent, so every block rescales O.
