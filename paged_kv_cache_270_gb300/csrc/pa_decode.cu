@@ -146,6 +146,8 @@ __global__ void __launch_bounds__(kThreads, (Cfg<KV, D>::kMinBlocks)) decode_ker
   constexpr bool F8 = C::kFp8;
   constexpr bool BLK = C::kBlockScaled;
   constexpr int NT = D / 16;  // MMA steps along the head dim (QK) / m-tiles (PV)
+  // FP8 pools with swizzled rows read V through transposed 8-bit ldmatrix
+  constexpr bool LDT = F8 && SWZ;
   extern __shared__ __align__(16) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + C::kAlign - 1) & ~uintptr_t(C::kAlign - 1));
@@ -330,17 +332,29 @@ __global__ void __launch_bounds__(kThreads, (Cfg<KV, D>::kMinBlocks)) decode_ker
       if constexpr (BLK) psc = stage_scale[stage];
 
       // ---- issue every shared-memory read of the page up front
+      // The page's 16 tokens are taken in a fixed order lambda = 0..15 (the rows
+      // of S^T and the K index of P V).  The transposed-ldmatrix path hands each
+      // thread tokens 4t .. 4t+3 of a V column, so there lambda = 2t, 2t+1,
+      // 2t+8, 2t+9 are the tokens 4t .. 4t+3, and the accumulator rows g, g+8
+      // read K rows 2g - (g & 1) and that + 2; otherwise lambda is the token.
       constexpr int VW = VB / 4;  // V words per row per thread
       const int rows[4] = {2 * t, 2 * t + 1, 2 * t + 8, 2 * t + 9};
+      const int kg0 = LDT ? 2 * g - (g & 1) : g, kg1 = LDT ? kg0 + 2 : g + 8;
       uint4 kr[2][KB / 16];
       uint32_t vw[4][VW];
+      uint32_t vt[NT][2];  // LDT: V codes, tokens 4t .. 4t+3 of dims 16i + g and 16i + g + 8
       {
-        const uint32_t kr0 = g * RB + t * KB;
 #pragma unroll
         for (int c = 0; c < KB / 16; ++c) {
-          kr[0][c] = lds128(Ks + tile_off<SWZ>(kr0 + 16 * c));
-          kr[1][c] = lds128(Ks + tile_off<SWZ>(kr0 + 8 * RB + 16 * c));
+          kr[0][c] = lds128(Ks + tile_off<SWZ>(kg0 * RB + t * KB + 16 * c));
+          kr[1][c] = lds128(Ks + tile_off<SWZ>(kg1 * RB + t * KB + 16 * c));
         }
+        if constexpr (LDT) {
+#pragma unroll
+          for (int i = 0; i < NT; i += 2)
+            ldsm_x2_trans_b8(Vs + tile_off<SWZ>((lane & 15) * RB + 16 * (i + (lane >> 4))), vt[i][0], vt[i][1],
+                             vt[i + 1][0], vt[i + 1][1]);
+        } else {
 #pragma unroll
         for (int r = 0; r < 4; ++r) {
           const uint32_t vo = rows[r] * RB + g * VB;
@@ -358,6 +372,7 @@ __global__ void __launch_bounds__(kThreads, (Cfg<KV, D>::kMinBlocks)) decode_ker
               vw[r][4 * c + 3] = u.w;
             }
           }
+        }
         }
       }
 
@@ -390,14 +405,24 @@ __global__ void __launch_bounds__(kThreads, (Cfg<KV, D>::kMinBlocks)) decode_ker
       float x0 = s[0] * qks, x1 = s[1] * qks;
       float x2 = s[2] * qks, x3 = s[3] * qks;
       if (tok0 + 16 > ctx) {  // last, partial page (warp-uniform): slots past ctx hold anything
-        if (tok0 + g >= ctx) x0 = x1 = -INFINITY;
-        if (tok0 + g + 8 >= ctx) x2 = x3 = -INFINITY;
+        if (tok0 + kg0 >= ctx) x0 = x1 = -INFINITY;
+        if (tok0 + kg1 >= ctx) x2 = x3 = -INFINITY;
+        if constexpr (LDT) {
+          const int nv = ctx - tok0 - 4 * t;  // valid tokens among this thread's 4
+          const uint32_t keep = nv >= 4 ? 0xFFFFFFFFu : (nv <= 0 ? 0u : (1u << (8 * nv)) - 1u);
 #pragma unroll
-        for (int r = 0; r < 4; ++r)
-          if (tok0 + rows[r] >= ctx) {
-#pragma unroll
-            for (int w = 0; w < VW; ++w) vw[r][w] = 0u;
+          for (int i = 0; i < NT; ++i) {
+            vt[i][0] &= keep;
+            vt[i][1] &= keep;
           }
+        } else {
+#pragma unroll
+          for (int r = 0; r < 4; ++r)
+            if (tok0 + rows[r] >= ctx) {
+#pragma unroll
+              for (int w = 0; w < VW; ++w) vw[r][w] = 0u;
+            }
+        }
       }
       float pm0 = fmaxf(x0, x2), pm1 = fmaxf(x1, x3);
 #pragma unroll
@@ -459,7 +484,12 @@ __global__ void __launch_bounds__(kThreads, (Cfg<KV, D>::kMinBlocks)) decode_ker
 #pragma unroll
         for (int i = 0; i < NT; ++i) {
           uint32_t af[4];
-          if constexpr (F8) {
+          if constexpr (LDT) {
+            af[0] = e4m3x2_to_f16x2(vt[i][0]);
+            af[1] = e4m3x2_to_f16x2(vt[i][1]);
+            af[2] = e4m3x2_to_f16x2(vt[i][0] >> 16);
+            af[3] = e4m3x2_to_f16x2(vt[i][1] >> 16);
+          } else if constexpr (F8) {
             const uint32_t sel = (i & 1) ? 0x7362u : 0x5140u;
             const uint32_t x01 = __byte_perm(vw[0][i >> 1], vw[1][i >> 1], sel);
             const uint32_t x23 = __byte_perm(vw[2][i >> 1], vw[3][i >> 1], sel);
@@ -505,11 +535,12 @@ __global__ void __launch_bounds__(kThreads, (Cfg<KV, D>::kMinBlocks)) decode_ker
     float* mw = mo + warp * 8 * D;
 #pragma unroll
     for (int i = 0; i < NT; ++i) {
-      const int d0 = g * (D / 8) + 2 * i;  // output dims held by this thread
+      // output dims held by this thread (accumulator rows g and g + 8 of m-tile i)
+      const int d0 = LDT ? 16 * i + g : g * (D / 8) + 2 * i, d1 = LDT ? d0 + 8 : d0 + 1;
       mw[(2 * t) * D + d0] = o[i][0];
       mw[(2 * t + 1) * D + d0] = o[i][1];
-      mw[(2 * t) * D + d0 + 1] = o[i][2];
-      mw[(2 * t + 1) * D + d0 + 1] = o[i][3];
+      mw[(2 * t) * D + d1] = o[i][2];
+      mw[(2 * t + 1) * D + d1] = o[i][3];
     }
     if (g == 0) {
       float* ml = mml + warp * 16;

@@ -172,6 +172,18 @@ __device__ __forceinline__ void mma16816(float (&c)[4], const uint32_t (&a)[4], 
   }
 }
 
+// Two 16 x 16 byte matrices from shared memory, transposed: lanes 0-15 give the
+// addresses of the first matrix's 16 rows (16 bytes each), lanes 16-31 those of
+// the second.  Lane 4g + t receives rows 4t .. 4t+3 of column g (r0) and of
+// column g + 8 (r1) of the first matrix, low byte = row 4t, and the same of
+// the second in (r2, r3).
+__device__ __forceinline__ void ldsm_x2_trans_b8(const void* row, uint32_t& r0, uint32_t& r1, uint32_t& r2,
+                                                 uint32_t& r3) {
+  asm volatile("ldmatrix.sync.aligned.m16n16.x2.trans.shared.b8 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+               : "r"(smem_addr(row)));
+}
+
 // Transpose of an 8x8 matrix of 16-bit elements held one row-pair per lane
 // (lane 4r + c holds row r, columns 2c and 2c+1).
 __device__ __forceinline__ uint32_t movmatrix_trans(uint32_t x) {
