@@ -146,8 +146,10 @@ __global__ void __launch_bounds__(kThreads, (Cfg<KV, D>::kMinBlocks)) decode_ker
   constexpr bool F8 = C::kFp8;
   constexpr bool BLK = C::kBlockScaled;
   constexpr int NT = D / 16;  // MMA steps along the head dim (QK) / m-tiles (PV)
-  // FP8 pools with swizzled rows read V through transposed 8-bit ldmatrix
+  // Pools with swizzled rows read V through transposed ldmatrix: 8-bit for
+  // FP8 pools (LDT), 16-bit otherwise (LD16)
   constexpr bool LDT = F8 && SWZ;
+  constexpr bool LD16 = !F8 && SWZ;
   extern __shared__ __align__(16) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + C::kAlign - 1) & ~uintptr_t(C::kAlign - 1));
@@ -343,6 +345,8 @@ __global__ void __launch_bounds__(kThreads, (Cfg<KV, D>::kMinBlocks)) decode_ker
       uint4 kr[2][KB / 16];
       uint32_t vw[4][VW];
       uint32_t vt[NT][2];  // LDT: V codes, tokens 4t .. 4t+3 of dims 16i + g and 16i + g + 8
+      // LD16: V pairs, tokens (2t, 2t+1) of dims 16i + g, 16i + g + 8, then tokens (2t+8, 2t+9)
+      uint32_t vh[NT][4];
       {
 #pragma unroll
         for (int c = 0; c < KB / 16; ++c) {
@@ -354,6 +358,12 @@ __global__ void __launch_bounds__(kThreads, (Cfg<KV, D>::kMinBlocks)) decode_ker
           for (int i = 0; i < NT; i += 2)
             ldsm_x2_trans_b8(Vs + tile_off<SWZ>((lane & 15) * RB + 16 * (i + (lane >> 4))), vt[i][0], vt[i][1],
                              vt[i + 1][0], vt[i + 1][1]);
+        } else if constexpr (LD16) {
+          // matrix m of m-tile i: tokens 8 (m >> 1) .. +7, dims 16i + 8 (m & 1) .. +7
+          const uint32_t vrow = ((lane & 7) + ((lane >> 4) << 3)) * RB + ((lane >> 3) & 1) * 16;
+#pragma unroll
+          for (int i = 0; i < NT; ++i)
+            ldsm_x4_trans_b16(Vs + tile_off<SWZ>(vrow + 32 * i), vh[i][0], vh[i][1], vh[i][2], vh[i][3]);
         } else {
 #pragma unroll
         for (int r = 0; r < 4; ++r) {
@@ -387,8 +397,9 @@ __global__ void __launch_bounds__(kThreads, (Cfg<KV, D>::kMinBlocks)) decode_ker
 #pragma unroll
           for (int jj = 0; jj < 4; ++jj) {
             const int j = 4 * c + jj;
-            const uint32_t af[4] = {e4m3x2_to_f16x2(w0[jj]), e4m3x2_to_f16x2(w1[jj]),
-                                    e4m3x2_to_f16x2(w0[jj] >> 16), e4m3x2_to_f16x2(w1[jj] >> 16)};
+            uint32_t af[4];
+            e4m3x4_to_f16x2x2(w0[jj], af[0], af[2]);
+            e4m3x4_to_f16x2x2(w1[jj], af[1], af[3]);
             const uint2 qj = qsm[j * 32 + lane];
             mma16816<false>(s, af, qj.x, qj.y);
           }
@@ -414,6 +425,17 @@ __global__ void __launch_bounds__(kThreads, (Cfg<KV, D>::kMinBlocks)) decode_ker
           for (int i = 0; i < NT; ++i) {
             vt[i][0] &= keep;
             vt[i][1] &= keep;
+          }
+        } else if constexpr (LD16) {
+          const int r0 = ctx - tok0 - 2 * t;  // tokens 2t, 2t+1 valid when r0 > 0, r0 > 1
+          const uint32_t klo = (r0 > 0 ? 0x0000FFFFu : 0u) | (r0 > 1 ? 0xFFFF0000u : 0u);
+          const uint32_t khi = (r0 > 8 ? 0x0000FFFFu : 0u) | (r0 > 9 ? 0xFFFF0000u : 0u);
+#pragma unroll
+          for (int i = 0; i < NT; ++i) {
+            vh[i][0] &= klo;
+            vh[i][1] &= klo;
+            vh[i][2] &= khi;
+            vh[i][3] &= khi;
           }
         } else {
 #pragma unroll
@@ -485,18 +507,19 @@ __global__ void __launch_bounds__(kThreads, (Cfg<KV, D>::kMinBlocks)) decode_ker
         for (int i = 0; i < NT; ++i) {
           uint32_t af[4];
           if constexpr (LDT) {
-            af[0] = e4m3x2_to_f16x2(vt[i][0]);
-            af[1] = e4m3x2_to_f16x2(vt[i][1]);
-            af[2] = e4m3x2_to_f16x2(vt[i][0] >> 16);
-            af[3] = e4m3x2_to_f16x2(vt[i][1] >> 16);
+            e4m3x4_to_f16x2x2(vt[i][0], af[0], af[2]);
+            e4m3x4_to_f16x2x2(vt[i][1], af[1], af[3]);
+          } else if constexpr (LD16) {
+            af[0] = vh[i][0];
+            af[1] = vh[i][1];
+            af[2] = vh[i][2];
+            af[3] = vh[i][3];
           } else if constexpr (F8) {
             const uint32_t sel = (i & 1) ? 0x7362u : 0x5140u;
             const uint32_t x01 = __byte_perm(vw[0][i >> 1], vw[1][i >> 1], sel);
             const uint32_t x23 = __byte_perm(vw[2][i >> 1], vw[3][i >> 1], sel);
-            af[0] = e4m3x2_to_f16x2(x01);
-            af[1] = e4m3x2_to_f16x2(x01 >> 16);
-            af[2] = e4m3x2_to_f16x2(x23);
-            af[3] = e4m3x2_to_f16x2(x23 >> 16);
+            e4m3x4_to_f16x2x2(x01, af[0], af[1]);
+            e4m3x4_to_f16x2x2(x23, af[2], af[3]);
           } else {
             af[0] = __byte_perm(vw[0][i], vw[1][i], 0x5410u);
             af[1] = __byte_perm(vw[0][i], vw[1][i], 0x7632u);
@@ -536,7 +559,7 @@ __global__ void __launch_bounds__(kThreads, (Cfg<KV, D>::kMinBlocks)) decode_ker
 #pragma unroll
     for (int i = 0; i < NT; ++i) {
       // output dims held by this thread (accumulator rows g and g + 8 of m-tile i)
-      const int d0 = LDT ? 16 * i + g : g * (D / 8) + 2 * i, d1 = LDT ? d0 + 8 : d0 + 1;
+      const int d0 = (LDT || LD16) ? 16 * i + g : g * (D / 8) + 2 * i, d1 = (LDT || LD16) ? d0 + 8 : d0 + 1;
       mw[(2 * t) * D + d0] = o[i][0];
       mw[(2 * t + 1) * D + d0] = o[i][1];
       mw[(2 * t) * D + d1] = o[i][2];

@@ -306,7 +306,9 @@ __global__ void __launch_bounds__((kMaxGroup + 1) * 32) prefill_kernel(
           for (int jj = 0; jj < 4; ++jj) {
             const int j = 4 * c + jj;  // dims t*D/4 + 4j .. 4j+3
             const uint32_t af[4] = {qa0[2 * j], qa1[2 * j], qa0[2 * j + 1], qa1[2 * j + 1]};
-            mma16816<false>(s[nt], af, e4m3x2_to_f16x2(w[jj]), e4m3x2_to_f16x2(w[jj] >> 16));
+            uint32_t b0, b1;
+            e4m3x4_to_f16x2x2(w[jj], b0, b1);
+            mma16816<false>(s[nt], af, b0, b1);
           }
         } else {
 #pragma unroll
@@ -439,8 +441,11 @@ __global__ void __launch_bounds__((kMaxGroup + 1) * 32) prefill_kernel(
           const uint32_t sel = (e < 2) ? 0x5140u : 0x7362u;
           const uint32_t x01 = __byte_perm(vw[0][w], vw[1][w], sel);
           const uint32_t x23 = __byte_perm(vw[2][w], vw[3][w], sel);
-          b0 = e4m3x2_to_f16x2((e & 1) ? (x01 >> 16) : x01);
-          b1 = e4m3x2_to_f16x2((e & 1) ? (x23 >> 16) : x23);
+          uint32_t l0, h0, l1, h1;
+          e4m3x4_to_f16x2x2(x01, l0, h0);
+          e4m3x4_to_f16x2x2(x23, l1, h1);
+          b0 = (e & 1) ? h0 : l0;
+          b1 = (e & 1) ? h1 : l1;
         } else {
           const int w = nt >> 1;
           const uint32_t sel = (nt & 1) ? 0x7632u : 0x5410u;

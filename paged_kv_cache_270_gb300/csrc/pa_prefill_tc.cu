@@ -490,8 +490,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const TcArgs a,
         uint32_t hv[8];
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
-          hv[2 * q] = e4m3x2_to_f16x2(cw[q]);
-          hv[2 * q + 1] = e4m3x2_to_f16x2(cw[q] >> 16);
+          e4m3x4_to_f16x2x2(cw[q], hv[2 * q], hv[2 * q + 1]);
         }
         uint8_t* row = vt + (ch >> 2) * 16384 + key * 128;
         const int c0 = (ch & 3) * 2;
