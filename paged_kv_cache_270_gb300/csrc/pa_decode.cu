@@ -74,6 +74,11 @@ struct Cfg {
   static constexpr bool kSwizzle = (kRowBytes % 128) == 0;
   static constexpr int kTmaRank = kRowBytes == 256 ? 3 : 2;
   static constexpr int kStages = 8;
+  // Consumer warp w takes pages w, w + 4, ...; with a stage count that is a
+  // multiple of the warp count, the previous page of a stage is the same
+  // warp's, so a warp waits on a full barrier at most one phase behind (the
+  // parity wait cannot tell phases further apart).
+  static_assert(kStages % kConsumerWarps == 0, "stages must be a multiple of the consumer warps");
   static constexpr int kStageBytes = 2 * kTile;  // K tile + V tile
   static constexpr int kRingBytes = kStages * kStageBytes;
   static constexpr int kMergeBytes = kConsumerWarps * 8 * (D + 2) * 4;
