@@ -87,14 +87,13 @@ DESCRIPTION = {
 # DRAM traffic per decode launch from one ncu capture, valid only while the
 # decode source is byte-identical to the one measured.
 NCU_TRAFFIC = {
-    "source_sha256": "833f28eca0c083e906d556a083e4b1bebc7e1dd5c8ed7021091df9e8a8fd9f66",
+    "source_sha256": "3cb887c2bca179ac3f99734d0ddcab3a0f880be525af31f589fc4f33dabab5b4",
     # dram__bytes_read.sum + dram__bytes_write.sum of one decode launch
-    "bytes_per_launch": {"llama3_70b_fp8_a": 1073991936 + 5629696,
-                         "llama3_70b_fp8_b": 2152029696 + 6951680,
-                         "llama3_70b_fp8_block_a": 1076107008 + 4295168,
-                         "llama3_70b_fp8_block_b": 2156209408 + 5888000},
+    "bytes_per_launch": {"llama3_70b_fp8_a": 1074093056 + 5023744,
+                         "llama3_70b_fp8_b": 2151996672 + 7354880,
+                         "llama3_70b_fp8_block_a": 1076084736 + 4217600,
+                         "llama3_70b_fp8_block_b": 2156343040 + 5719808},
 }
-
 
 # --------------------------------------------------------------------- workers
 def _gen_amax(args):
