@@ -187,6 +187,14 @@ def _measured_peak():
         return FALLBACK_HBM_GBS, "fallback"
 
 
+def _p10_p90(xs):
+    """10th and 90th percentiles (nearest rank) of per-launch times, ms."""
+    v = sorted(xs)
+    if not v:
+        return None
+    return [round(v[int(0.1 * (len(v) - 1))], 4), round(v[int(0.9 * (len(v) - 1))], 4)]
+
+
 def _source_sha():
     h = hashlib.sha256()
     for f in ("pa_decode.cu", "pa_device.cuh"):
@@ -507,6 +515,7 @@ def run_gb300(args, rank, world, local_rank):
         per_batch[b.w.name] = {
             "sequences": b.S, "tokens_per_seq": int(b.w.ctx_lens.max()), "kv_bytes": b.kv_bytes,
             "splits": b.splits, "decode_ms_median": statistics.median(d),
+            "decode_ms_p10_p90": _p10_p90(d),
             "decode_kv_gbs": b.kv_bytes / (statistics.median(d) / 1e3) / 1e9}
     launches = K * sum(b.launches for b in batches)
     line = {
@@ -677,6 +686,7 @@ def run_prefill(args, rank, world, local_rank):
                    "flops_per_step": flops, "parallelism": "1 GPU" if world == 1 else
                    f"replicas x{world}"},
         "prefill_ms_median": round(statistics.median(pre_ms), 4),
+        "prefill_ms_p10_p90": _p10_p90(pre_ms),
         "tokens_per_s": round(world * T * K / t_max, 1),
         "roofline": {"kernel": "prefill_tc_kernel (tcgen05)", "bound": "tensor", "achieved": round(achieved, 1),
                      "peak": peak, "peak_kind": peak_kind, "unit": "TFLOP/s",

@@ -934,13 +934,19 @@ int check_shape(const pa_pool* pool, int S, int n_q_heads, int max_blocks) {
   return PA_OK;
 }
 
-// Splits along the pages.  With r resident CTAs, u = S * Hkv units and at
-// most B pages per unit, a split count s gives CTAs of P = ceil(B / s) pages;
-// if a fraction f of the units' pages is really there, the kernel takes about
-// ceil(f * u * s / r) waves of (P + c) page-times.  The contexts live on the
-// device, so the choice averages the full (f = 1) and the half-full (f = 1/2)
-// batch: the first favours whole waves for uniform batches, the second keeps
-// the longest sequences of a ragged batch from setting the kernel time.
+// Splits along the pages.  With u = S * Hkv units of at most B pages, s splits
+// give u * s CTAs of P = ceil(B / s) pages, launched in waves of r = occ * sms
+// resident CTAs.  Once an SM holds about k_sat CTAs the kernel is bound by its
+// share of HBM bandwidth, so a wave whose busiest SM holds k CTAs lasts about
+// (P + c) * max(k, k_sat) page-times: k CTAs share the SM's bandwidth, and fewer
+// than k_sat cannot fill it (each is then bound by its own load latency).  The
+// cost of s is the sum over its waves; c is the fixed cost of a CTA (pipeline
+// fill, query load) plus, with splits, its partial and merge.  Measured on the
+// 70B-shaped FP8 batches this ranks the split counts as the kernel does (4 x
+// 131072 tokens: 19 splits, exactly 4 CTAs per SM, best; 256 x 4096: 1 split).
+// The contexts live on the device, so every unit is taken as full: a batch with
+// a few sequences much longer than the rest is better served by an explicit
+// split count.
 int auto_splits(const pa_pool* pool, int S, int max_blocks, int* out) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
@@ -952,6 +958,7 @@ int auto_splits(const pa_pool* pool, int S, int max_blocks, int* out) {
   int occ = configure(*d.info, dev);
   if (occ <= 0) return fail(PA_ERR_CUDA, "decode kernel occupancy query failed");
   const double slots = (double)sms * occ;
+  const double k_sat = std::min(4, occ);
   const double units = (double)std::max(S, 1) * pool->desc.n_kv_heads;
   const int max_s = std::min(max_blocks, 256);
   int best = 1;
@@ -959,11 +966,13 @@ int auto_splits(const pa_pool* pool, int S, int max_blocks, int* out) {
   for (int s = 1; s <= max_s; ++s) {
     const int pps = (max_blocks + s - 1) / s;
     if (s > 1 && (max_blocks + pps - 1) / pps != s) continue;  // same as a smaller s
-    const double per = pps + 4.0 + (s > 1 ? 2.0 : 0.0);
-    const double full = std::ceil(units * s / slots) * per;
-    const double half = std::ceil(0.5 * units * s / slots) * per;
-    const double cost = 0.5 * (full + half);
-    if (cost < best_cost * 0.98) {
+    const double ctas = units * s;
+    const double full_waves = std::floor(ctas / slots);
+    const double rest = ctas - full_waves * slots;
+    double per_sm = full_waves * std::max((double)occ, k_sat);
+    if (rest > 0) per_sm += std::max(std::ceil(rest / sms), k_sat);
+    const double cost = per_sm * (pps + 4.0 + (s > 1 ? 2.0 : 0.0));
+    if (cost < best_cost * 0.97) {  // more splits only for a clear gain
       best_cost = cost;
       best = s;
     }
