@@ -334,7 +334,6 @@ class Batch:
         self.d_tables = self.h_tables.cuda()
         self.d_ctx = self.h_ctx.cuda()
         self.d_out = torch.empty((S, Hq, D), dtype=in_t, device="cuda")
-        self.h_out = torch.empty((S, Hq, D), dtype=in_t).pin_memory()
         self.splits = self.pool.num_splits(S, Hq, self.max_blocks)
         self.ws_bytes = self.pool.workspace_bytes(S, Hq, self.max_blocks, 0)
         self.ws = torch.empty(max(self.ws_bytes, 16), dtype=torch.uint8, device="cuda")
@@ -342,7 +341,7 @@ class Batch:
         self.h2d_bytes = sum(t.numel() * t.element_size() for t in
                              (self.h_q, self.h_k, self.h_v, self.h_slots, self.h_tables,
                               self.h_ctx))
-        self.d2h_bytes = self.h_out.numel() * self.h_out.element_size()
+        self.d2h_bytes = self.d_out.numel() * self.d_out.element_size()
         self.launches = 2 + (1 if self.splits > 1 else 0)
         self.softmax_scale = w.softmax_scale
         self.out_code = N.PA_FP16 if w.in_dtype == "fp16" else N.PA_BF16
@@ -357,13 +356,55 @@ class Batch:
                          self.d_ctx.data_ptr(), self.S, self.Hq, self.softmax_scale, 0,
                          self.ws.data_ptr(), self.ws_bytes, stream)
 
-    def upload(self):
-        for d, h in ((self.d_q, self.h_q), (self.d_k, self.h_k), (self.d_v, self.h_v),
-                     (self.d_slots, self.h_slots), (self.d_tables, self.h_tables),
-                     (self.d_ctx, self.h_ctx)):
-            d.copy_(h, non_blocking=True)
 
-    def download(self):
+class Staging:
+    """The step's host<->device traffic for the end-to-end run, packed: every
+    batch's per-step inputs sit in one pinned host buffer whose device twin the
+    kernels read (the batches' device tensors become views into it), and the
+    outputs of all batches in one device buffer with a pinned host twin.  A step
+    then moves its inputs with one host-to-device copy and its results with one
+    device-to-host copy.  (Overlapping the second batch's copies with the first
+    batch's decode on a copy stream measured slower: the step moves ~10 MB, and
+    the cross-stream waits cost more than they hide.)"""
+    FIELDS = ("q", "k", "v", "slots", "tables", "ctx")
+
+    def __init__(self, batches):
+        import torch
+        align = lambda n: (n + 255) // 256 * 256  # noqa: E731
+        nbytes = lambda t: t.numel() * t.element_size()  # noqa: E731
+        self.in_rng, self.out_rng = [], []
+        off_in = off_out = 0
+        for b in batches:
+            n = sum(align(nbytes(getattr(b, "h_" + f))) for f in self.FIELDS)
+            self.in_rng.append((off_in, off_in + n))
+            off_in += n
+            n = align(nbytes(b.d_out))
+            self.out_rng.append((off_out, off_out + n))
+            off_out += n
+        self.h_in = torch.empty(off_in, dtype=torch.uint8).pin_memory()
+        self.d_in = torch.empty(off_in, dtype=torch.uint8, device="cuda")
+        self.h_out = torch.empty(off_out, dtype=torch.uint8).pin_memory()
+        self.d_out = torch.empty(off_out, dtype=torch.uint8, device="cuda")
+        for b, (off, _) in zip(batches, self.in_rng):
+            for f in self.FIELDS:
+                h = getattr(b, "h_" + f)
+                n = nbytes(h)
+                self.h_in[off:off + n].copy_(h.contiguous().view(-1).view(torch.uint8))
+                setattr(b, "d_" + f, self.d_in[off:off + n].view(h.dtype).view(h.shape))
+                off += align(n)
+        self.d_in.copy_(self.h_in)
+        for b, (off, _) in zip(batches, self.out_rng):
+            n = nbytes(b.d_out)
+            b.d_out = self.d_out[off:off + n].view(b.d_out.dtype).view(b.d_out.shape)
+        self.h2d_bytes = sum(b.h2d_bytes for b in batches)
+        self.d2h_bytes = sum(b.d2h_bytes for b in batches)
+
+    def step(self, batches, sh):
+        """One end-to-end step: inputs in, reshape + decode per batch, results out."""
+        self.d_in.copy_(self.h_in, non_blocking=True)
+        for b in batches:
+            b.reshape(sh)
+            b.decode(sh)
         self.h_out.copy_(self.d_out, non_blocking=True)
 
 
@@ -422,6 +463,7 @@ def run_gb300(args, rank, world, local_rank):
     procs = max(1, min(os.cpu_count() or 1, 16))
     with ctx_mp.Pool(procs) as pool_procs:
         batches = [Batch(n, pool_procs) for n in names]
+        staging = Staging(batches)
         scales = {b.w.name: (b.w.k_scale, b.w.v_scale) for b in batches}
         stream = torch.cuda.current_stream()
         sh = int(stream.cuda_stream)
@@ -465,29 +507,21 @@ def run_gb300(args, rank, world, local_rank):
         e2e = None
         if not args.no_e2e:
             for _ in range(max(1, args.warmup // 2)):
-                for b in batches:
-                    b.upload()
-                step()
-                for b in batches:
-                    b.download()
+                staging.step(batches, sh)
                 torch.cuda.synchronize()
             _barrier(world)
             e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             e0.record(stream)
             for _ in range(K):
-                for b in batches:
-                    b.upload()
-                step()
-                for b in batches:
-                    b.download()
-                stream.synchronize()
+                staging.step(batches, sh)
+                stream.synchronize()  # the step's results are in host memory
             e1.record(stream)
             torch.cuda.synchronize()
             te = _max_over_ranks(e0.elapsed_time(e1) / 1e3, world)
             kv = sum(b.kv_bytes for b in batches)
             e2e = {"value": world * kv * K / te / 1e9, "unit": "GB/s",
-                   "h2d_bytes_per_step": sum(b.h2d_bytes for b in batches),
-                   "d2h_bytes_per_step": sum(b.d2h_bytes for b in batches),
+                   "h2d_bytes_per_step": staging.h2d_bytes,
+                   "d2h_bytes_per_step": staging.d2h_bytes,
                    "ms_per_step": te / K * 1e3}
         for b in batches:
             err = b.pool.device_error()
@@ -647,12 +681,48 @@ def run_prefill(args, rank, world, local_rank):
     pre_ms = [ev[0].elapsed_time(ev[1]) for ev in evs]
     e2e = None
     if not args.no_e2e:
+        # End to end, per sequence on the public API: a sequence's q, K/V and slots
+        # go up on a copy stream while the previous sequence computes, and its
+        # output comes back while the next one computes.
+        cs = torch.cuda.Stream()
+        C, Hq = w.chunk, w.n_q_heads
+        h_qs1 = pin(np.array([0, C], np.int32))
+        d_qs1 = h_qs1.cuda()
+        small = [(d_tab, h_tab), (d_ctx, h_ctx), (d_qs1, h_qs1)]
+        per_seq = [[(d_[s * C:(s + 1) * C], h_[s * C:(s + 1) * C]) for d_, h_ in
+                    ((d_q, h_q), (d_k, h_k), (d_v, h_v), (d_slots, h_slots))] for s in range(w.S)]
+        e2e_h2d = sum(h_.numel() * h_.element_size() for _, h_ in small) + sum(
+            h_.numel() * h_.element_size() for seq in per_seq for _, h_ in seq)
+
         def e2e_step():
-            for d_, h_ in zip(ds, hs):
-                d_.copy_(h_, non_blocking=True)
-            step()
-            h_out.copy_(d_out, non_blocking=True)
-            stream.synchronize()
+            cs.wait_stream(stream)
+            ready = []
+            with torch.cuda.stream(cs):
+                for d_, h_ in small:
+                    d_.copy_(h_, non_blocking=True)
+                for seq in per_seq:
+                    for d_, h_ in seq:
+                        d_.copy_(h_, non_blocking=True)
+                    ev_ = torch.cuda.Event()
+                    ev_.record(cs)
+                    ready.append(ev_)
+            done = []
+            for s_, ev_ in enumerate(ready):
+                stream.wait_event(ev_)
+                N.pa_reshape_and_cache(pool.handle, 0, d_k[s_ * C].data_ptr(), d_v[s_ * C].data_ptr(),
+                                       d_slots[s_ * C:].data_ptr(), C, sh)
+                N.pa_prefill(pool.handle, 0, d_out[s_ * C].data_ptr(), N.PA_BF16, d_q[s_ * C].data_ptr(),
+                             d_qs1.data_ptr(), d_tab[s_].data_ptr(), w.max_blocks, d_ctx[s_:].data_ptr(), 1,
+                             Hq, C, w.softmax_scale, sh)
+                ev_ = torch.cuda.Event()
+                ev_.record(stream)
+                done.append(ev_)
+            with torch.cuda.stream(cs):
+                for s_, ev_ in enumerate(done):
+                    cs.wait_event(ev_)
+                    h_out[s_ * C:(s_ + 1) * C].copy_(d_out[s_ * C:(s_ + 1) * C], non_blocking=True)
+            stream.wait_stream(cs)
+            stream.synchronize()  # the step's results are in host memory
         for _ in range(2):
             e2e_step()
         _barrier(world)
@@ -664,9 +734,15 @@ def run_prefill(args, rank, world, local_rank):
         torch.cuda.synchronize()
         te = _max_over_ranks(f0.elapsed_time(f1) / 1e3, world)
         e2e = {"value": round(world * w.prefill_flops() * K / te / 1e12, 2), "unit": "TFLOP/s",
-               "h2d_bytes_per_step": sum(t_.numel() * t_.element_size() for t_ in hs),
+               "h2d_bytes_per_step": e2e_h2d,
                "d2h_bytes_per_step": h_out.numel() * h_out.element_size(),
                "ms_per_step": round(te / K * 1e3, 4)}
+        # the per-sequence calls give the same result as the packet call
+        ref_out = d_out.clone()
+        step()
+        torch.cuda.synchronize()
+        if not torch.equal(ref_out, d_out) or not torch.equal(h_out, d_out.cpu()):
+            raise RuntimeError("per-sequence prefill differs from the packet call")
     if pool.device_error():
         raise RuntimeError("device error in prefill")
     if rank != 0:
