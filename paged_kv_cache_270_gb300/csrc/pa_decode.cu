@@ -81,7 +81,10 @@ struct Cfg {
   static_assert(kStages % kConsumerWarps == 0, "stages must be a multiple of the consumer warps");
   static constexpr int kStageBytes = 2 * kTile;  // K tile + V tile
   static constexpr int kRingBytes = kStages * kStageBytes;
-  static constexpr int kMergeBytes = kConsumerWarps * 8 * (D + 2) * 4;
+  // merge area: per warp, 8 heads x (D + 4) floats (the pad spreads a warp's
+  // stores over all banks) plus (m, l) per head
+  static constexpr int kMergeStride = D + 4;
+  static constexpr int kMergeBytes = kConsumerWarps * 8 * (kMergeStride + 2) * 4;
   static constexpr int kDataBytes = kRingBytes > kMergeBytes ? kRingBytes : kMergeBytes;
   static constexpr int kAlign = 1024;  // a 128-byte-swizzled TMA destination is 1 KiB aligned
   // FP8 pools keep the query fragments in shared memory instead of 16 registers
@@ -556,19 +559,20 @@ __global__ void __launch_bounds__(kThreads, (Cfg<KV, D>::kMinBlocks)) decode_ker
 
   __syncthreads();  // the ring is idle from here on: reuse it for the merge
 
-  float* mo = reinterpret_cast<float*>(smem);          // [warp][8 heads][D]
-  float* mml = mo + kConsumerWarps * 8 * D;            // [warp][8 heads][2]
+  float* mo = reinterpret_cast<float*>(smem);          // [warp][8 heads][MS]
+  constexpr int MS = C::kMergeStride;
+  float* mml = mo + kConsumerWarps * 8 * MS;           // [warp][8 heads][2]
   if (warp < kConsumerWarps) {
     const int g = lane >> 2, t = lane & 3;
-    float* mw = mo + warp * 8 * D;
+    float* mw = mo + warp * 8 * MS;
 #pragma unroll
     for (int i = 0; i < NT; ++i) {
       // output dims held by this thread (accumulator rows g and g + 8 of m-tile i)
       const int d0 = (LDT || LD16) ? 16 * i + g : g * (D / 8) + 2 * i, d1 = (LDT || LD16) ? d0 + 8 : d0 + 1;
-      mw[(2 * t) * D + d0] = o[i][0];
-      mw[(2 * t + 1) * D + d0] = o[i][1];
-      mw[(2 * t) * D + d1] = o[i][2];
-      mw[(2 * t + 1) * D + d1] = o[i][3];
+      mw[(2 * t) * MS + d0] = o[i][0];
+      mw[(2 * t + 1) * MS + d0] = o[i][1];
+      mw[(2 * t) * MS + d1] = o[i][2];
+      mw[(2 * t + 1) * MS + d1] = o[i][3];
     }
     if (g == 0) {
       float* ml = mml + warp * 16;
@@ -593,7 +597,7 @@ __global__ void __launch_bounds__(kThreads, (Cfg<KV, D>::kMinBlocks)) decode_ker
         const float mw = mml[w * 16 + 2 * head];
         const float f = (mw == -INFINITY) ? 0.f : fast_exp2(mw - M);
         L += f * mml[w * 16 + 2 * head + 1];
-        O += f * mo[(w * 8 + head) * D + dim];
+        O += f * mo[(w * 8 + head) * MS + dim];
       }
     }
     if (direct) {
