@@ -78,7 +78,7 @@ int layer_maps(pa_pool* pool, int layer, const CUtensorMap_st** tk, const CUtens
 int layer_half_maps(pa_pool* pool, int layer, const CUtensorMap_st** tk, const CUtensorMap_st** tv);
 
 // Chunked prefill on the tcgen05 tensor cores, for the shapes it covers
-// (head_dim 128, 8 query heads per KV head; FP8 or bfloat16 pools with bf16 or
+// (head_dim 128, 1, 2, 4 or 8 query heads per KV head; FP8 or bfloat16 pools with bf16 or
 // fp32 output, binary16 pools with fp16 or fp32 output); the arguments are
 // those of pa_prefill, already validated.
 bool prefill_tc_supported(const pa_pool* pool, int n_q_heads, int out_dtype);

@@ -7,13 +7,14 @@
 // sections 5 and 6.3: prefill in packets interleaved with decode; "Capítulo 8
 // -- Gestión de caché KV de nueva generación", section 8.1: pages gathered
 // through the block table).  This kernel takes the shapes where a CTA's rows
-// fill a 128-row MMA: head_dim 128 and 8 query heads per KV head (16 query
-// tokens x 8 heads), FP8 E4M3 pages with a per-tensor or per-tile scale, or
-// bfloat16 / binary16 pages.
+// fill a 128-row MMA: head_dim 128 and G = 1, 2, 4 or 8 query heads per KV
+// head (a tile of 128 / G query tokens x G heads), FP8 E4M3 pages with a
+// per-tensor or per-tile scale, or bfloat16 / binary16 pages.
 //
 // Design (the pages give none):
-//  * grid = (16-token query tile, kv head, sequence), longest tiles first; one
-//    CTA per SM (about 200 KB of shared memory, 384 of the 512 TMEM columns).
+//  * grid = (query tile, kv head, sequence), longest tiles first; one CTA per
+//    SM (131 KB of shared memory for FP8 pools, 197 KB for 16-bit pools; 448 of
+//    the 512 TMEM columns: S twice, O, Q).
 //  * warp 0 streams the K and V pages of 128-key blocks (8 pages) with TMA into
 //    a two-block ring; the K pages land 128-byte swizzled, back to back, which
 //    is exactly the K-major operand layout of the MMA, so S = Q K^T reads them
@@ -55,7 +56,7 @@ namespace pa {
 namespace {
 
 constexpr int kD = 128;         // head dim
-constexpr int kG = 8;           // query heads per kv head
+constexpr int kRows = 128;      // MMA rows of a tile: query tokens x the G heads of a kv head
 constexpr int kThreads = 448;   // 14 warps: producer, MMA, 4 converters, 8 softmax
 constexpr unsigned kAll = 0xffffffffu;
 constexpr uint32_t kTmemCols = 512;
@@ -112,6 +113,7 @@ struct TcArgs {
   const float* ksc;  // block-scaled pools: this layer's scales [num_blocks][Hkv]
   const float* vsc;
   int max_blocks, Hq, Hkv, num_blocks;
+  int lg;               // log2 G: row r of a tile is token r >> lg, head r & (G - 1)
   float qk_scale_log2;  // softmax_scale * log2(e) (* k_scale for a static FP8 pool)
   float v_scale;        // static FP8 pool's V scale (1 for block-scaled pools)
   unsigned int* err;
@@ -268,14 +270,14 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const TcArgs a,
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int q0 = a.q_start[seq];
   const int Cn = a.q_start[seq + 1] - q0;
-  const int tok_lo = 16 * qt;
+  const int tok_lo = qt << (7 - a.lg);  // a tile holds 128 / G query tokens
   if (tok_lo >= Cn) return;
   const int ctx = a.ctx[seq];
   if (Cn < 0 || ctx < Cn || ctx > a.max_blocks * 16) {
     if (threadIdx.x == 0) record_error(a.err, PA_ERR_BOUNDS);
     return;
   }
-  const int n_tok = min(16, Cn - tok_lo);
+  const int n_tok = min(kRows >> a.lg, Cn - tok_lo);
   const int pos0 = ctx - Cn + tok_lo;  // position of the tile's first query
   const int pos_last = pos0 + n_tok - 1;
   const int npages = pos_last / 16 + 1;
@@ -506,7 +508,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const TcArgs a,
     }
   } else {
     // ---------------------------------------------------------- softmax rows
-    // Two threads per row: row r (= 8 * query token + head) in TMEM lane r; the
+    // Two threads per row: row r (= G * query token + head) in TMEM lane r; the
     // thread of half hf takes keys 64 hf .. 64 hf + 63 of every block (two
     // 32-column chunks), O columns 64 hf .. 64 hf + 63, and Q dims 64 hf ...
     // The halves exchange partials through shared memory, one xchg phase each
@@ -515,7 +517,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const TcArgs a,
     // waits then return at once), so the phases of xchg stay in step.
     const int sw = warp - 4, hf = sw >> 2;
     const int r = (sw & 3) * 32 + lane;
-    const int tl = r >> 3, hh = r & 7;
+    const int tl = r >> a.lg, hh = r & ((1 << a.lg) - 1);
     const bool row_valid = tl < n_tok;
     const uint32_t trow = tmem + ((uint32_t)((warp & 3) * 32) << 16);
     int xk = 0;  // next xchg phase
@@ -536,7 +538,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const TcArgs a,
     {
       uint32_t qw[32];  // this half's 64 16-bit values, two per word
       const uint4* src = reinterpret_cast<const uint4*>(
-          a.q + ((size_t)(q0 + tok_lo + tl) * a.Hq + (size_t)h * kG + hh) * kD + 64 * hf);
+          a.q + ((size_t)(q0 + tok_lo + tl) * a.Hq + ((size_t)h << a.lg) + hh) * kD + 64 * hf);
 #pragma unroll
       for (int c = 0; c < 8; ++c) {
         const uint4 v = row_valid ? src[c] : make_uint4(0, 0, 0, 0);
@@ -731,7 +733,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const TcArgs a,
     if (ok) {
       tc_fence_after();
       const float sc = L > 0.f ? (BLK ? vref : a.v_scale) / L : 0.f;
-      const size_t orow = ((size_t)(q0 + tok_lo + tl) * a.Hq + (size_t)h * kG + hh) * kD + 64 * hf;
+      const size_t orow = ((size_t)(q0 + tok_lo + tl) * a.Hq + ((size_t)h << a.lg) + hh) * kD + 64 * hf;
 #pragma unroll 1
       for (int cc = 0; cc < 2; ++cc) {
         float o[32];
@@ -787,7 +789,9 @@ cudaError_t tc_launch(const TcArgs& a, const CUtensorMap* tk, const CUtensorMap*
 
 bool prefill_tc_supported(const pa_pool* pool, int n_q_heads, int out_dtype) {
   const pa_pool_desc& d = pool->desc;
-  if (d.head_dim != kD || n_q_heads != kG * d.n_kv_heads) return false;
+  if (d.head_dim != kD || n_q_heads % d.n_kv_heads != 0) return false;
+  const int G = n_q_heads / d.n_kv_heads;
+  if (G != 1 && G != 2 && G != 4 && G != 8) return false;
   switch (d.kv_dtype) {
     case PA_FP8_E4M3:
     case PA_FP8_E4M3_BLOCK:
@@ -824,7 +828,10 @@ int prefill_tc(pa_pool* pool, int layer, void* out, int out_dtype, const void* q
   a.qk_scale_log2 = softmax_scale * 1.4426950408889634f * (static_fp8 ? d.k_scale : 1.f);
   a.v_scale = static_fp8 ? d.v_scale : 1.f;
   a.err = err;
-  const int tiles = (max_chunk + 15) / 16;
+  const int G = n_q_heads / d.n_kv_heads;
+  a.lg = G == 8 ? 3 : G == 4 ? 2 : G == 2 ? 1 : 0;
+  const int tok = kRows >> a.lg;
+  const int tiles = (max_chunk + tok - 1) / tok;
   const bool f32 = out_dtype == PA_FP32;
   cudaError_t e;
   switch (d.kv_dtype) {

@@ -6,8 +6,8 @@ import pytest
 import torch
 
 import oracle
-from gpu_harness import (bits_to_torch, check_fp32, check_half, fill_both, gpu_decode, new_pool,
-                         oracle_pools, vmax_of)
+from gpu_harness import (FP32_ROW_TOL, bits_to_torch, check_fp32, check_half, fill_both, gpu_decode,
+                         new_pool, oracle_decode, oracle_pools, vmax_of)
 from paged_kv_cache_270_gb300 import _native as N
 from paged_kv_cache_270_gb300 import workloads as W
 
@@ -90,15 +90,26 @@ def test_prefill_shapes_and_ragged_chunks(kv_dtype, d, G):
 
 
 def test_one_token_chunks_match_decode():
+    """A chunk of one token is a decode: both calls meet the fp32-mode bound
+    against the oracle's decode, so they agree per row within twice it.  (The
+    two kernels differ in how they carry P -- at these shapes the prefill runs
+    on the tensor-core kernel, whose running max moves in steps of 2^8 -- so
+    they are not compared element by element at a tighter tolerance.)"""
     w = W.make("llama3_8b_bf16", scale_down=8)
     pool = new_pool(w, 0)
-    fill_both(w, pool, None)
+    op = oracle_pools(w, 0)
+    fill_both(w, pool, op)
     q_bits = w.q_bits()
+    ref = oracle_decode(w, op, q_bits)
     q_start = np.arange(w.S + 1, dtype=np.int32)
     pre = _gpu_prefill(w, pool, q_bits.reshape(w.S, w.n_q_heads, w.head_dim), q_start,
                        out_dtype=torch.float32)
     dec = gpu_decode(w, pool, q_bits, out_dtype=torch.float32)
-    assert torch.allclose(pre, dec, rtol=1e-5, atol=1e-6)
+    check_fp32(pre, ref)
+    check_fp32(dec, ref)
+    diff = (pre - dec).abs().amax(dim=-1).double().cpu().numpy()
+    scale = np.abs(ref).max(axis=-1)
+    assert np.all(diff <= 2 * FP32_ROW_TOL * scale + 1e-30)
 
 
 def test_prefill_in_two_chunks_matches_one_chunk():

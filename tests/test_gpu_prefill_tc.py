@@ -1,6 +1,6 @@
 """GPU parity of the tensor-core (tcgen05) chunked prefill against the fp64
 oracle.  pa_prefill takes that path for pools with head_dim 128 and 8 query
-heads per KV head (FP8 static or block-scaled, bfloat16, binary16); these cases
+heads per KV head (1, 2, 4 or 8; FP8 static or block-scaled, bfloat16, binary16); these cases
 make it run many 128-key blocks (the ring
 wraps many times), ragged query tiles, causal diagonals at every offset,
 both FP8 scalings and both output types, and scores that grow block after
@@ -26,7 +26,7 @@ def _built():
     oracle.build()
 
 
-def _setup(kv_dtype, pairs, seed, Hkv=2, k_gain_per_block=1.0, q_away_from_zero=False):
+def _setup(kv_dtype, pairs, seed, Hkv=2, k_gain_per_block=1.0, q_away_from_zero=False, G=8):
     ctx = np.array([h + c for h, c in pairs], np.int32)
     chunks = [c for _, c in pairs]
     max_blocks = int(-(-ctx.max() // 16))
@@ -40,7 +40,7 @@ def _setup(kv_dtype, pairs, seed, Hkv=2, k_gain_per_block=1.0, q_away_from_zero=
         tables[s, :k] = perm[used:used + k]
         tables[s, k:] = rng.integers(-5, 10**6, max_blocks - k)  # never read
         used += k
-    w = W.Workload(name="tc", index=12, kv_dtype=kv_dtype, n_q_heads=8 * Hkv, n_kv_heads=Hkv,
+    w = W.Workload(name="tc", index=12, kv_dtype=kv_dtype, n_q_heads=G * Hkv, n_kv_heads=Hkv,
                    head_dim=128, ctx_lens=ctx, num_blocks=nb, block_tables=tables, kv_seed=seed)
     # K/V values: N(0,1); optionally K grows by a factor per 128-token block
     kv = []
@@ -64,7 +64,7 @@ def _setup(kv_dtype, pairs, seed, Hkv=2, k_gain_per_block=1.0, q_away_from_zero=
         assert oracle.reshape_and_cache(kv_dtype, nb, 16, Hkv, 128, k, v, slots, w.k_scale,
                                         w.v_scale, *op) == 0
     T = sum(chunks)
-    qf = rng.standard_normal((T, 8 * Hkv, 128)).astype(np.float32)
+    qf = rng.standard_normal((T, G * Hkv, 128)).astype(np.float32)
     if q_away_from_zero:  # |q| in [0.5, 2): the two-term E4M3 split of q is exact
         qf = (np.sign(qf) * rng.uniform(0.5, 2.0, qf.shape)).astype(np.float32)
     q = _cast(w, qf)
@@ -111,6 +111,17 @@ def test_scores_growing_block_after_block(kv_dtype):
     pairs = [(900, 100), (500, 33)]
     w, pool, op, q, q_start, chunks = _setup(kv_dtype, pairs, seed=43, k_gain_per_block=2.0,
                                              q_away_from_zero=True)
+    _run(w, pool, op, q, q_start, chunks)
+
+
+@pytest.mark.parametrize("kv_dtype", ["fp8_e4m3", "fp8_e4m3_block", "bf16"])
+@pytest.mark.parametrize("G", [1, 2, 4])
+def test_fewer_heads_per_group_longer_tiles(kv_dtype, G):
+    """G query heads per KV head: a tile is 128 / G tokens (128 for G = 1), so
+    chunks span several tiles with a ragged last one and diagonals cross
+    128-key blocks at every offset."""
+    pairs = [(0, 1), (3000, 200), (129, 130), (700, 64), (0, 257)]
+    w, pool, op, q, q_start, chunks = _setup(kv_dtype, pairs, seed=53 + G, G=G)
     _run(w, pool, op, q, q_start, chunks)
 
 
