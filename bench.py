@@ -26,6 +26,7 @@ import json
 import math
 import multiprocessing as mp
 import os
+import re
 import statistics
 import sys
 import threading
@@ -85,15 +86,198 @@ DESCRIPTION = {
 }
 
 # DRAM traffic per decode launch from one ncu capture, valid only while the
-# decode source is byte-identical to the one measured.
+# decode source (its code: comments and blank lines do not count) is the one
+# measured.
 NCU_TRAFFIC = {
-    "source_sha256": "5048944d5dc3f95299af35bf014960ba91041c91da1c227798e67de12080b0f9",
+    # hash of the decode source with comments and blank lines removed (see _source_sha)
+    "source_sha256": "aed15271eb2b8d6c9483d181188d24ca11ef4219303159a2cb7b4711304dfe41",
     # dram__bytes_read.sum + dram__bytes_write.sum of one decode launch
     "bytes_per_launch": {"llama3_70b_fp8_a": 1073976832 + 3423232,
                          "llama3_70b_fp8_b": 2151986944 + 4409344,
                          "llama3_70b_fp8_block_a": 1076086272 + 2972416,
                          "llama3_70b_fp8_block_b": 2156226560 + 5916672},
 }
+
+# --------------------------------------------------------------------- workers
+def _gen_amax(args):
+    name, s, lo, hi = args
+    from paged_kv_cache_270_gb300 import workloads as W
+    w = W.make(name)
+    k, v = w.kv_bits(s, lo, hi)
+    return (float(np.abs(W.bits_to_f32(k, w.in_dtype)).max(initial=0)),
+            float(np.abs(W.bits_to_f32(v, w.in_dtype)).max(initial=0)))
+
+
+def _gen_bits(args):
+    name, s, lo, hi = args
+    from paged_kv_cache_270_gb300 import workloads as W
+    w = W.make(name)
+    k, v = w.kv_bits(s, lo, hi)
+    return s, lo, hi, k, v
+
+
+def _oracle_prefill_worker(args):
+    """Times the fp64 oracle's chunked prefill on the last `rows` queries of one
+    sequence; returns (flops, t_start, t_end)."""
+    name, s, rows, k_scale, v_scale = args
+    import oracle
+    from paged_kv_cache_270_gb300 import workloads as W
+    w = W.make(name)
+    n = int(w.ctx_lens[s])
+    nb = -(-n // 16)
+    nbytes = oracle.pool_bytes(w.kv_dtype, nb, 16, w.n_kv_heads, w.head_dim)
+    kp, vp = np.zeros(nbytes, np.uint8), np.zeros(nbytes, np.uint8)
+    k, v = w.kv_bits(s, 0, n)
+    oracle.reshape_and_cache(w.kv_dtype, nb, 16, w.n_kv_heads, w.head_dim, k, v,
+                             np.arange(n, dtype=np.int64), k_scale, v_scale, kp, vp)
+    q = w.prefill_q_bits()[s * w.chunk + w.chunk - rows: (s + 1) * w.chunk]
+    t0 = time.time()
+    oracle.paged_prefill(w.kv_dtype, w.in_dtype, nb, 16, w.n_kv_heads, w.head_dim, kp, vp,
+                         k_scale, v_scale, q, np.array([0, rows], np.int32),
+                         np.arange(nb, dtype=np.int32)[None, :], np.array([n], np.int32),
+                         w.softmax_scale)
+    t1 = time.time()
+    keys = rows * n - rows * (rows - 1) // 2
+    return 4 * w.head_dim * w.n_q_heads * keys, t0, t1
+
+
+def _oracle_worker(args):
+    """Times the fp64 oracle (gather + textbook attention) on some sequences of
+    a workload; returns (kv bytes, t_start, t_end)."""
+    name, seqs, k_scale, v_scale = args
+    import oracle
+    from paged_kv_cache_270_gb300 import workloads as W
+    w = W.make(name)
+    w.k_scale, w.v_scale = k_scale, v_scale
+    ids = []
+    for s in seqs:
+        ids += list(w.block_tables[s, : -(-int(w.ctx_lens[s]) // 16)])
+    remap = {b: i for i, b in enumerate(ids)}
+    tables = np.zeros((len(seqs), w.max_blocks), np.int32)
+    nbytes = oracle.pool_bytes(w.kv_dtype, len(ids), 16, w.n_kv_heads, w.head_dim)
+    kp, vp = np.zeros(nbytes, np.uint8), np.zeros(nbytes, np.uint8)
+    for r, s in enumerate(seqs):
+        n = int(w.ctx_lens[s])
+        nb = -(-n // 16)
+        tables[r, :nb] = [remap[b] for b in w.block_tables[s, :nb]]
+        k, v = w.kv_bits(s, 0, n)
+        pos = np.arange(n, dtype=np.int64)
+        slots = tables[r, pos // 16].astype(np.int64) * 16 + pos % 16
+        oracle.reshape_and_cache(w.kv_dtype, len(ids), 16, w.n_kv_heads, w.head_dim, k, v, slots,
+                                 w.k_scale, w.v_scale, kp, vp)
+    q = w.q_bits()[list(seqs)]
+    ctx = w.ctx_lens[list(seqs)]
+    t0 = time.time()
+    oracle.paged_attention(w.kv_dtype, w.in_dtype, len(ids), 16, w.n_kv_heads, w.head_dim, kp, vp,
+                           w.k_scale, w.v_scale, q, tables, ctx, w.softmax_scale)
+    t1 = time.time()
+    return w.kv_bytes(ctx), t0, t1
+
+
+# ------------------------------------------------------------------- helpers
+def _env_rank():
+    return (int(os.environ.get("RANK", 0)), int(os.environ.get("WORLD_SIZE", 1)),
+            int(os.environ.get("LOCAL_RANK", 0)))
+
+
+def _measured_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def _p10_p90(xs):
+    """10th and 90th percentiles (nearest rank) of per-launch times, ms."""
+    v = sorted(xs)
+    if not v:
+        return None
+    return [round(v[int(0.1 * (len(v) - 1))], 4), round(v[int(0.9 * (len(v) - 1))], 4)]
+
+
+def _source_sha():
+    """sha256 of the decode kernel's code: pa_decode.cu and pa_device.cuh with
+    // comments, trailing blanks and empty lines removed, so that editing a
+    comment keeps the recorded traffic valid and any code change voids it."""
+    h = hashlib.sha256()
+    for f in ("pa_decode.cu", "pa_device.cuh"):
+        with open(os.path.join(ROOT, "paged_kv_cache_270_gb300", "csrc", f)) as fh:
+            lines = (re.sub(r"//.*$", "", ln).rstrip() for ln in fh.read().splitlines())
+            h.update(("\n".join(ln for ln in lines if ln.strip()) + "\n").encode())
+    return h.hexdigest()
+
+
+class ClockSampler:
+    """Samples SM clock, power and clock-event reasons through NVML while the
+    timed region runs (read-only queries)."""
+    REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown",
+               0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown",
+               0x2: "applications_clocks_setting", 0x1: "gpu_idle"}
+
+    def __init__(self, device_index: int):
+        self.samples = []
+        self.ok = False
+        self.max_mhz = None
+        try:
+            import torch
+            self.nvml = ctypes.CDLL("libnvidia-ml.so.1")
+            if self.nvml.nvmlInit_v2() != 0:
+                return
+            props = torch.cuda.get_device_properties(device_index)
+            bus = f"{props.pci_domain_id:08x}:{props.pci_bus_id:02x}:{props.pci_device_id:02x}.0"
+            self.h = ctypes.c_void_p()
+            if self.nvml.nvmlDeviceGetHandleByPciBusId_v2(bus.encode(), ctypes.byref(self.h)) != 0:
+                return
+            mx = ctypes.c_uint()
+            if self.nvml.nvmlDeviceGetMaxClockInfo(self.h, 1, ctypes.byref(mx)) == 0:
+                self.max_mhz = mx.value
+            self._reasons = getattr(self.nvml, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+                getattr(self.nvml, "nvmlDeviceGetCurrentClocksThrottleReasons")
+            self.ok = True
+        except Exception:
+            self.ok = False
+
+    def _sample(self):
+        c, p, r = ctypes.c_uint(), ctypes.c_uint(), ctypes.c_ulonglong()
+        self.nvml.nvmlDeviceGetClockInfo(self.h, 1, ctypes.byref(c))
+        self.nvml.nvmlDeviceGetPowerUsage(self.h, ctypes.byref(p))
+        self._reasons(self.h, ctypes.byref(r))
+        self.samples.append((c.value, p.value / 1000.0, r.value))
+
+    def __enter__(self):
+        self._stop = threading.Event()
+        if self.ok:
+            self._sample()
+
+            def loop():
+                while not self._stop.is_set():
+                    self._sample()
+                    time.sleep(0.002)
+            self._t = threading.Thread(target=loop, daemon=True)
+            self._t.start()
+        return self
+
+    def __exit__(self, *exc):
+        self._stop.set()
+        if self.ok:
+            self._t.join()
+            self._sample()
+
+    def summary(self):
+        if not self.ok or not self.samples:
+            return {"sm_mhz": None, "sm_max_mhz": self.max_mhz, "reasons": ["nvml unavailable"]}
+        reasons = set()
+        for _, _, r in self.samples:
+            for bit, name in self.REASONS.items():
+                if r & bit and name != "gpu_idle":
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(s[0] for s in self.samples),
+                "sm_max_mhz": self.max_mhz, "reasons": sorted(reasons),
+                "power_w_max": max(s[1] for s in self.samples), "samples": len(self.samples)}
+
 
 # --------------------------------------------------------------- GPU batches
 class Batch:

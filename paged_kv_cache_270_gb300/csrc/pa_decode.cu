@@ -30,9 +30,14 @@
 //    O^T += V_page^T * P^T (M = 16 dims per MMA, K = the 16 tokens).
 //    Any permutation of the head dimension that Q and K share leaves q.k
 //    unchanged, so each thread loads a contiguous 16-byte run of a K row and
-//    the matching Q run; for V each thread owns a contiguous run of output
-//    dims and byte-permutes token pairs into the A operand.
-//  * FP8 codes convert exactly to binary16; q (bfloat16) is rescaled by a power
+//    the matching Q run.  V comes through a transposed ldmatrix, which hands
+//    each thread consecutive tokens of one V column: token pairs for 16-bit
+//    pools, four tokens for FP8 pools, whose tokens are then taken in an order
+//    that makes those four the A operand's two pairs (K rows follow the same
+//    order).  Rows narrower than 128 bytes (d = 64 FP8) keep byte permutes.
+//  * FP8 codes convert exactly to binary16, two at a time from the 16-bit
+//    halves of a register (reaching the upper pair by shifting the word would
+//    cost an instruction per conversion); q (bfloat16) is rescaled by a power
 //    of two so the group's largest |q| lands in [2^14, 2^15) before rounding to
 //    binary16, and the scale is folded back into the softmax exponent.  For
 //    bfloat16 pools (and in fp32-output mode) P is split into a high and a low
