@@ -90,12 +90,12 @@ DESCRIPTION = {
 # measured.
 NCU_TRAFFIC = {
     # hash of the decode source with comments and blank lines removed (see _source_sha)
-    "source_sha256": "aed15271eb2b8d6c9483d181188d24ca11ef4219303159a2cb7b4711304dfe41",
+    "source_sha256": "ddd9c083844ce652cb229e6c12bab56f32b4426afb1b743ea3f7b54c2d9a5c12",
     # dram__bytes_read.sum + dram__bytes_write.sum of one decode launch
-    "bytes_per_launch": {"llama3_70b_fp8_a": 1073976832 + 3423232,
-                         "llama3_70b_fp8_b": 2151986944 + 4409344,
-                         "llama3_70b_fp8_block_a": 1076086272 + 2972416,
-                         "llama3_70b_fp8_block_b": 2156226560 + 5916672},
+    "bytes_per_launch": {"llama3_70b_fp8_a": 1074000128 + 3104768,
+                         "llama3_70b_fp8_b": 2151987712 + 4451840,
+                         "llama3_70b_fp8_block_a": 1076084736 + 2918144,
+                         "llama3_70b_fp8_block_b": 2156249344 + 5932032},
 }
 
 # --------------------------------------------------------------------- workers

@@ -174,6 +174,7 @@ __global__ void __launch_bounds__(kThreads, (Cfg<KV, D>::kMinBlocks)) decode_ker
 
   const int split = blockIdx.x, h = blockIdx.y, seq = blockIdx.z;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  grid_dependency_wait();  // the kernel before may still write q, tables, pages
 
   int ctx = a.ctx[seq];
   if (ctx < 0 || ctx > a.max_blocks * 16) {
@@ -562,6 +563,7 @@ __global__ void __launch_bounds__(kThreads, (Cfg<KV, D>::kMinBlocks)) decode_ker
     }
   }
 
+  grid_dependents_launch();  // the split merge may be scheduled (it waits for this grid)
   __syncthreads();  // the ring is idle from here on: reuse it for the merge
 
   float* mo = reinterpret_cast<float*>(smem);          // [warp][8 heads][MS]
@@ -634,6 +636,7 @@ __global__ void __launch_bounds__(128) reduce_rows_kernel(const float* __restric
                                                           const int32_t* __restrict__ ctx,
                                                           void* out, int rows, int Hq, int splits,
                                                           int max_blocks, int pps, float v_scale) {
+  grid_dependency_wait();  // the partials come from the decode kernel just before
   const int row = blockIdx.x * 4 + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
   if (row >= rows) return;
@@ -680,6 +683,7 @@ __global__ void __launch_bounds__(128) reduce_wide_kernel(const float* __restric
                                                           const int32_t* __restrict__ ctx,
                                                           void* out, int Hq, int splits,
                                                           int max_blocks, int pps, float v_scale) {
+  grid_dependency_wait();
   __shared__ float wsh[128];
   __shared__ float red[4];
   const int row = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -748,22 +752,38 @@ struct Launcher {
                             {}};
     return ki;
   }
+  // Both kernels are launched with programmatic stream serialization: each may
+  // be scheduled while the kernel before it in the stream finishes, and waits
+  // for it before its first global access, so its launch overlaps that
+  // kernel's tail (decode + merge of a 4 x 131072 batch 1.2% faster, behind
+  // its cache write; 0.6% with the merge alone launched so).
   static cudaError_t launch(const DecodeArgs& a, const CUtensorMap* tk, const CUtensorMap* tv,
                             int S, cudaStream_t st) {
-    dim3 grid(a.splits, a.Hkv, S);
-    decode_kernel<KV, D, OUT, kPsplit><<<grid, kThreads, Cfg<KV, D>::kSmem, st>>>(a, *tk, *tv);
-    cudaError_t e = cudaGetLastError();
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(a.splits, a.Hkv, S);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = Cfg<KV, D>::kSmem;
+    cfg.stream = st;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    cudaError_t e = cudaLaunchKernelEx(&cfg, decode_kernel<KV, D, OUT, kPsplit>, a, *tk, *tv);
     if (e != cudaSuccess || a.splits == 1) return e;
     const int rows = S * a.Hq;
-    if (a.splits <= 8)
-      reduce_rows_kernel<D, OUT><<<(rows + 3) / 4, 128, 0, st>>>(
-          a.ws_o, a.ws_ml, a.ctx, a.out, rows, a.Hq, a.splits, a.max_blocks, a.pages_per_split,
-          a.v_scale);
-    else
-      reduce_wide_kernel<D, OUT><<<rows, 128, 0, st>>>(a.ws_o, a.ws_ml, a.ctx, a.out, a.Hq,
-                                                      a.splits, a.max_blocks, a.pages_per_split,
-                                                      a.v_scale);
-    return cudaGetLastError();
+    cfg.blockDim = dim3(128);
+    cfg.dynamicSmemBytes = 0;
+    if (a.splits <= 8) {
+      cfg.gridDim = dim3((rows + 3) / 4);
+      e = cudaLaunchKernelEx(&cfg, reduce_rows_kernel<D, OUT>, (const float*)a.ws_o, (const float*)a.ws_ml,
+                             a.ctx, a.out, rows, a.Hq, a.splits, a.max_blocks, a.pages_per_split, a.v_scale);
+    } else {
+      cfg.gridDim = dim3(rows);
+      e = cudaLaunchKernelEx(&cfg, reduce_wide_kernel<D, OUT>, (const float*)a.ws_o, (const float*)a.ws_ml,
+                             a.ctx, a.out, a.Hq, a.splits, a.max_blocks, a.pages_per_split, a.v_scale);
+    }
+    return e;
   }
 };
 

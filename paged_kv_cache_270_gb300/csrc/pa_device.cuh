@@ -147,6 +147,17 @@ __device__ __forceinline__ uint2 lds64(const void* p) {
   return v;
 }
 
+// ---------------------------------------------------------------- dependent launch
+// A kernel launched with programmatic stream serialization may start while the
+// kernel before it in the stream is still running.  It must wait here, before
+// touching global memory that kernel may write or read; the wait returns once
+// that grid has completed and its writes are visible (at once for an ordinary
+// launch).
+__device__ __forceinline__ void grid_dependency_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+// Lets the next kernel in the stream, if launched that way, be scheduled once
+// every CTA of this grid has called this or exited.
+__device__ __forceinline__ void grid_dependents_launch() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
 // ---------------------------------------------------------------- MMA
 // D(16x8, fp32) += A(16x16, row) * B(16x8, col), warp-wide.
 // Fragment ownership (g = lane / 4, t = lane % 4):
