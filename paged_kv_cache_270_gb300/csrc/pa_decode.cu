@@ -100,9 +100,11 @@ struct Cfg {
   // block-scaled pools: the (K, V) scales of the page in each stage
   static constexpr int kScaleBytes = kBlockScaled ? kStages * 8 : 0;
   static constexpr int kSmem = kDataBytes + 2 * kStages * 8 + kQBytes + kScaleBytes + kAlign;
-  // register budget, in CTAs per SM (16-bit pools: what their ring size allows;
-  // block-scaled FP8 spills at five, so it keeps four)
-  static constexpr int kMinBlocks = kBlockScaled ? 4 : (kQInSmem ? 5 : (D == 128 ? 3 : 4));
+  // register budget, in CTAs per SM (16-bit pools: what their ring size allows).
+  // Block-scaled FP8 spills a little at five, so it has a second build for four
+  // (kMinBlocksLow), taken by launches that put at most four CTAs on an SM.
+  static constexpr int kMinBlocks = kQInSmem ? 5 : (D == 128 ? 3 : 4);
+  static constexpr int kMinBlocksLow = kBlockScaled ? 4 : kMinBlocks;
   static constexpr bool kMmaBf16 = (KV == KV_BF16);
   static_assert(kStageBytes % kAlign == 0 || !kSwizzle, "tiles must stay 1 KiB aligned");
 };
@@ -149,8 +151,8 @@ __device__ __forceinline__ uint32_t tile_off(uint32_t off) {
   else return off;
 }
 
-template <int KV, int D, int OUT, bool PSPLIT>
-__global__ void __launch_bounds__(kThreads, (Cfg<KV, D>::kMinBlocks)) decode_kernel(const DecodeArgs a,
+template <int KV, int D, int OUT, bool PSPLIT, int MINB>
+__global__ void __launch_bounds__(kThreads, MINB) decode_kernel(const DecodeArgs a,
                                                           const __grid_constant__ CUtensorMap tmk,
                                                           const __grid_constant__ CUtensorMap tmv) {
   using C = Cfg<KV, D>;
@@ -332,7 +334,7 @@ __global__ void __launch_bounds__(kThreads, (Cfg<KV, D>::kMinBlocks)) decode_ker
     // block-scaled pools: V weights are taken relative to the largest V scale
     // this warp has seen (vref), so P * sv / vref stays <= 1 in 16 bits; the
     // accumulator is rescaled when vref grows and multiplied by it at the end
-    float vref = 0.f, vref_inv = 0.f;
+    float vinv = INFINITY;  // 1 / vref; vref starts at 0
 
     for (int k = warp; k < n_local; k += kConsumerWarps) {
       const int stage = k % C::kStages;
@@ -344,8 +346,8 @@ __global__ void __launch_bounds__(kThreads, (Cfg<KV, D>::kMinBlocks)) decode_ker
       const uint8_t* Ks = ring + stage * C::kStageBytes;
       const uint8_t* Vs = Ks + C::kTile;
       const int tok0 = (p_begin + k) * 16;
-      float2 psc = make_float2(1.f, 1.f);
-      if constexpr (BLK) psc = stage_scale[stage];
+      // block-scaled pools: the page's (K, V) scales are read from the stage's
+      // slot where they are used (it stays valid until the page is released)
 
       // ---- issue every shared-memory read of the page up front
       // The page's 16 tokens are taken in a fixed order lambda = 0..15 (the rows
@@ -426,7 +428,7 @@ __global__ void __launch_bounds__(kThreads, (Cfg<KV, D>::kMinBlocks)) decode_ker
       }
 
       // ---- online softmax over this page (tokens g and g+8; heads 2t, 2t+1)
-      const float qks = BLK ? qk_scale * psc.x : qk_scale;
+      const float qks = BLK ? qk_scale * stage_scale[stage].x : qk_scale;
       float x0 = s[0] * qks, x1 = s[1] * qks;
       float x2 = s[2] * qks, x3 = s[3] * qks;
       if (tok0 + 16 > ctx) {  // last, partial page (warp-uniform): slots past ctx hold anything
@@ -468,7 +470,9 @@ __global__ void __launch_bounds__(kThreads, (Cfg<KV, D>::kMinBlocks)) decode_ker
       }
       // token 0 of every page is valid, so the new maxima are finite
       const float mn0 = fmaxf(m0, pm0), mn1 = fmaxf(m1, pm1);
-      const bool vgrow = BLK && psc.y > vref;  // warp-uniform: one scale per page
+      // warp-uniform: one scale per page; sv * (1 / vref) > 1 is sv > vref, also
+      // for vref = 0 (inf > 1, and 0 * inf is NaN, not > 1)
+      const bool vgrow = BLK && stage_scale[stage].y * vinv > 1.f;
       if (__any_sync(kFull, (mn0 != m0) | (mn1 != m1)) || vgrow) {  // rescale only when needed
         const float al0 = fast_exp2(m0 - mn0), al1 = fast_exp2(m1 - mn1);
         l0 *= al0;
@@ -476,11 +480,11 @@ __global__ void __launch_bounds__(kThreads, (Cfg<KV, D>::kMinBlocks)) decode_ker
         float ov0 = al0, ov1 = al1;
         if constexpr (BLK) {
           if (vgrow) {
-            const float r = vref / psc.y;  // 0 on the first page with a nonzero scale
+            const float sv = stage_scale[stage].y;
+            const float r = 1.f / (vinv * sv);  // vref / sv: 0 on the first page with a nonzero scale
             ov0 *= r;
             ov1 *= r;
-            vref = psc.y;
-            vref_inv = 1.f / psc.y;
+            vinv = 1.f / sv;
           }
         }
 #pragma unroll
@@ -498,7 +502,7 @@ __global__ void __launch_bounds__(kThreads, (Cfg<KV, D>::kMinBlocks)) decode_ker
       l0 += p0 + p2;
       l1 += p1 + p3;
       if constexpr (BLK) {  // weights of this page's V codes: P * sv / vref
-        const float f = psc.y * vref_inv;
+        const float f = stage_scale[stage].y * vinv;
         p0 *= f;
         p1 *= f;
         p2 *= f;
@@ -555,10 +559,10 @@ __global__ void __launch_bounds__(kThreads, (Cfg<KV, D>::kMinBlocks)) decode_ker
     if constexpr (BLK) {  // back to value units (vref = 0 only if every V here is 0)
 #pragma unroll
       for (int i = 0; i < NT; ++i) {
-        o[i][0] *= vref;
-        o[i][1] *= vref;
-        o[i][2] *= vref;
-        o[i][3] *= vref;
+        o[i][0] *= 1.f / vinv;
+        o[i][1] *= 1.f / vinv;
+        o[i][2] *= 1.f / vinv;
+        o[i][3] *= 1.f / vinv;
       }
     }
   }
@@ -746,11 +750,24 @@ struct KernelInfo {
 template <int KV, int D, int OUT>
 struct Launcher {
   static constexpr bool kPsplit = (KV == KV_BF16) || (OUT == OUT_F32);
+  static constexpr int kMinB = Cfg<KV, D>::kMinBlocks, kMinBLow = Cfg<KV, D>::kMinBlocksLow;
   static KernelInfo& info() {
-    static KernelInfo ki = {reinterpret_cast<const void*>(&decode_kernel<KV, D, OUT, kPsplit>),
+    static KernelInfo ki = {reinterpret_cast<const void*>(&decode_kernel<KV, D, OUT, kPsplit, kMinB>),
                             Cfg<KV, D>::kSmem,
                             {}};
     return ki;
+  }
+  // the build for launches with at most kMinBLow CTAs per SM (the same kernel
+  // unless the pool type has a second build)
+  static KernelInfo& info_low() {
+    if constexpr (kMinBLow == kMinB) {
+      return info();
+    } else {
+      static KernelInfo ki = {reinterpret_cast<const void*>(&decode_kernel<KV, D, OUT, kPsplit, kMinBLow>),
+                              Cfg<KV, D>::kSmem,
+                              {}};
+      return ki;
+    }
   }
   // Both kernels are launched with programmatic stream serialization: each may
   // be scheduled while the kernel before it in the stream finishes, and waits
@@ -758,7 +775,7 @@ struct Launcher {
   // kernel's tail (decode + merge of a 4 x 131072 batch 1.2% faster, behind
   // its cache write; 0.6% with the merge alone launched so).
   static cudaError_t launch(const DecodeArgs& a, const CUtensorMap* tk, const CUtensorMap* tv,
-                            int S, cudaStream_t st) {
+                            int S, cudaStream_t st, bool low) {
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
@@ -769,7 +786,8 @@ struct Launcher {
     cfg.stream = st;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    cudaError_t e = cudaLaunchKernelEx(&cfg, decode_kernel<KV, D, OUT, kPsplit>, a, *tk, *tv);
+    cudaError_t e = low ? cudaLaunchKernelEx(&cfg, decode_kernel<KV, D, OUT, kPsplit, kMinBLow>, a, *tk, *tv)
+                        : cudaLaunchKernelEx(&cfg, decode_kernel<KV, D, OUT, kPsplit, kMinB>, a, *tk, *tv);
     if (e != cudaSuccess || a.splits == 1) return e;
     const int rows = S * a.Hq;
     cfg.blockDim = dim3(128);
@@ -788,9 +806,10 @@ struct Launcher {
 };
 
 struct Dispatch {
-  KernelInfo* info;
+  KernelInfo* info;      // the default build (its occupancy sizes the splits)
+  KernelInfo* info_low;  // the build for launches of one wave at its own occupancy
   cudaError_t (*launch)(const DecodeArgs&, const CUtensorMap*, const CUtensorMap*, int,
-                        cudaStream_t);
+                        cudaStream_t, bool);
 };
 
 // ---- TMA descriptors of the pool regions
@@ -902,7 +921,7 @@ int layer_half_maps(pa_pool* pool, int layer, const CUtensorMap** tk, const CUte
 
 template <int KV, int D, int OUT>
 Dispatch make_dispatch() {
-  return {&Launcher<KV, D, OUT>::info(), &Launcher<KV, D, OUT>::launch};
+  return {&Launcher<KV, D, OUT>::info(), &Launcher<KV, D, OUT>::info_low(), &Launcher<KV, D, OUT>::launch};
 }
 
 template <int KV, int D>
@@ -1084,6 +1103,17 @@ int pa_decode(pa_pool* pool, int layer, void* out, int out_dtype, const void* q,
   cudaGetDevice(&dev);
   Dispatch disp = pick(d.kv_dtype, d.head_dim, out_dtype);
   if (configure(*disp.info, dev) <= 0) return fail(PA_ERR_CUDA, "decode kernel configuration failed");
+  // A launch that fits one wave of the second build's occupancy takes that
+  // build (block-scaled pools: four CTAs per SM without spills, against five).
+  bool low = false;
+  if (disp.info_low != disp.info) {
+    const int occ_low = configure(*disp.info_low, dev);
+    if (occ_low <= 0) return fail(PA_ERR_CUDA, "decode kernel configuration failed");
+    int sms = 0;
+    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+      return fail(PA_ERR_CUDA, "SM count query failed");
+    low = (long long)S * d.n_kv_heads * splits <= (long long)occ_low * sms;
+  }
 
   const CUtensorMap *tk = nullptr, *tv = nullptr;
   st = layer_maps(pool, layer, &tk, &tv);
@@ -1109,7 +1139,7 @@ int pa_decode(pa_pool* pool, int layer, void* out, int out_dtype, const void* q,
   a.ksc = pool->block_scaled ? layer_scales(pool, pool->k, layer) : nullptr;
   a.vsc = pool->block_scaled ? layer_scales(pool, pool->v, layer) : nullptr;
   a.err = err;
-  cudaError_t e = disp.launch(a, tk, tv, S, static_cast<cudaStream_t>(stream));
+  cudaError_t e = disp.launch(a, tk, tv, S, static_cast<cudaStream_t>(stream), low);
   if (e != cudaSuccess) return fail(PA_ERR_CUDA, "decode launch: %s", cudaGetErrorString(e));
   return PA_OK;
 }

@@ -197,6 +197,9 @@ def test_decode_steps_8b_shapes():
 
 @pytest.mark.parametrize("name", ["llama3_70b_fp8_block_a", "llama3_70b_fp8_block_b"])
 def test_llama70b_block_reduced(name):
+    """Both register builds of the block-scaled kernel: launches of at most four
+    CTAs per SM (152 SMs) take the spill-free one, 32 forced splits (1024 and
+    2048 CTAs here) the five-per-SM one."""
     w = W.make(name, scale_down=16)
     pool = new_pool(w, 0)
     op = oracle_pools(w, 0)
@@ -204,7 +207,8 @@ def test_llama70b_block_reduced(name):
     q = w.q_bits()
     ref = oracle_decode(w, op, q)
     vmax = vmax_of(w, op)
-    for ns in (0, 1, 3):
+    assert w.S * w.n_kv_heads * min(32, w.max_blocks) > 4 * 152
+    for ns in (0, 1, 3, 32):
         check_half(gpu_decode(w, pool, q, num_splits=ns), ref, vmax)
         check_fp32(gpu_decode(w, pool, q, out_dtype=torch.float32, num_splits=ns), ref)
     torch.cuda.synchronize()
