@@ -90,12 +90,12 @@ DESCRIPTION = {
 # measured.
 NCU_TRAFFIC = {
     # hash of the decode source with comments and blank lines removed (see _source_sha)
-    "source_sha256": "ddd9c083844ce652cb229e6c12bab56f32b4426afb1b743ea3f7b54c2d9a5c12",
+    "source_sha256": "d6b7fd0ca4115ea4ec99e80f0a4cdbb1e920f223cf536e76419cf92fbe376762",
     # dram__bytes_read.sum + dram__bytes_write.sum of one decode launch
-    "bytes_per_launch": {"llama3_70b_fp8_a": 1074000128 + 3104768,
-                         "llama3_70b_fp8_b": 2151987712 + 4451840,
-                         "llama3_70b_fp8_block_a": 1076084736 + 2918144,
-                         "llama3_70b_fp8_block_b": 2156249344 + 5932032},
+    "bytes_per_launch": {"llama3_70b_fp8_a": 1073976576 + 3272960,
+                         "llama3_70b_fp8_b": 2151992320 + 4573184,
+                         "llama3_70b_fp8_block_a": 1076082944 + 3091968,
+                         "llama3_70b_fp8_block_b": 2156268288 + 5209088},
 }
 
 # --------------------------------------------------------------------- workers
