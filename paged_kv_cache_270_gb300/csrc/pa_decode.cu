@@ -346,8 +346,8 @@ __global__ void __launch_bounds__(kThreads, MINB) decode_kernel(const DecodeArgs
       const uint8_t* Ks = ring + stage * C::kStageBytes;
       const uint8_t* Vs = Ks + C::kTile;
       const int tok0 = (p_begin + k) * 16;
-      // block-scaled pools: the page's (K, V) scales are read from the stage's
-      // slot where they are used (it stays valid until the page is released)
+      // (block-scaled pools read the page's (K, V) scales from the stage's slot
+      // where they are used: it stays valid until the page is released)
 
       // ---- issue every shared-memory read of the page up front
       // The page's 16 tokens are taken in a fixed order lambda = 0..15 (the rows
