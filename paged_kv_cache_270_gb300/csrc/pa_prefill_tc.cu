@@ -324,29 +324,43 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const TcArgs a,
     // ---------------------------------------------------------- TMA producer
     const int32_t* trow = a.tables + (size_t)seq * a.max_blocks;
     const uint64_t policy = l2_evict_first_policy();
-    int issued = 0;
-    for (int j = 0; j < nblk; ++j) {
-      const int half = j % R, u = j / R;
-      if (j >= R && !__all_sync(kAll, wait_or_abort(&ctl->kv_empty[half], (u - 1) & 1, abort_flag, a.err))) break;
-      const int cnt = min(8, npages - 8 * j);
-      int phys = 0;
-      float sk = 1.f, sv = 0.f;
-      if (lane < cnt) {
-        phys = trow[8 * j + lane];
-        if (phys < 0 || phys >= a.num_blocks) {
-          record_error(a.err, PA_ERR_BOUNDS);
-          phys = 0;
-        }
-        if constexpr (BLK) {
+    // Lane i holds the table entry (block-scaled: and the tile scales) of page
+    // 32 b + i of the current batch of four blocks; the next batch's entries
+    // are loaded one batch ahead, so no table load sits between two blocks.
+    auto entry = [&](int page) { return page < npages ? trow[page] : 0; };
+    int phys = 0, nxt = entry(32 + lane);
+    float sk = 1.f, sv = 0.f;
+    auto take = [&](int raw, int page) {  // checks the batch's entries and reads their scales
+      phys = raw;
+      if (page < npages && (raw < 0 || raw >= a.num_blocks)) {
+        record_error(a.err, PA_ERR_BOUNDS);
+        phys = 0;
+      }
+      if constexpr (BLK) {
+        sk = 1.f;
+        sv = 0.f;
+        if (page < npages) {
           sk = a.ksc[(size_t)phys * a.Hkv + h];
           sv = a.vsc[(size_t)phys * a.Hkv + h];
         }
       }
+    };
+    take(entry(lane), lane);
+    int issued = 0;
+    for (int j = 0; j < nblk; ++j) {
+      const int half = j % R, u = j / R;
+      const int pb = 8 * (j & 3);  // the block's first page within the batch
+      if (j > 0 && pb == 0) {
+        take(nxt, 8 * j + lane);
+        nxt = entry(8 * j + 32 + lane);
+      }
+      if (j >= R && !__all_sync(kAll, wait_or_abort(&ctl->kv_empty[half], (u - 1) & 1, abort_flag, a.err))) break;
+      const int cnt = min(8, npages - 8 * j);
       if constexpr (BLK) {
         if (j >= 2 && !__all_sync(kAll, wait_or_abort(&ctl->sc_empty[half], (u - 1) & 1, abort_flag, a.err))) break;
         float2 v[8];
 #pragma unroll
-        for (int i = 0; i < 8; ++i) v[i] = make_float2(__shfl_sync(kAll, sk, i), __shfl_sync(kAll, sv, i));
+        for (int i = 0; i < 8; ++i) v[i] = make_float2(__shfl_sync(kAll, sk, pb + i), __shfl_sync(kAll, sv, pb + i));
         if (lane == 0) {
 #pragma unroll
           for (int i = 0; i < 8; ++i) ctl->sc[half][i] = v[i];
@@ -355,7 +369,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const TcArgs a,
       }
       if (lane == 0) mbar_arrive_expect_tx(&ctl->kv_full[half], (uint32_t)cnt * (F8 ? 4096u : 8192u));
       for (int i = 0; i < cnt; ++i) {
-        const int ph = __shfl_sync(kAll, phys, i);
+        const int ph = __shfl_sync(kAll, phys, pb + i);
         if (lane == 0) {
           const int row0 = (ph * a.Hkv + h) * 16;
           uint8_t* kd = sm + L::kKRing + half * L::kSlot + i * 2048;
