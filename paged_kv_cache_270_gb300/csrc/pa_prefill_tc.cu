@@ -369,10 +369,15 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const TcArgs a,
         }
       }
       if (lane == 0) mbar_arrive_expect_tx(&ctl->kv_full[half], (uint32_t)cnt * (F8 ? 4096u : 8192u));
-      for (int i = 0; i < cnt; ++i) {
-        const int ph = __shfl_sync(kAll, phys, pb + i);
-        if (lane == 0) {
-          const int row0 = (ph * a.Hkv + h) * 16;
+      // each page's copies are issued by the lane that holds its entry, so the
+      // block's copies leave in one warp instruction per tile instead of one
+      // thread issuing them in turn (a copy landing before lane 0's expect-tx
+      // only makes the byte count transiently negative; the phase still waits
+      // for that arrival)
+      {
+        const int i = lane - pb;  // this lane's page within the block
+        if (i >= 0 && i < cnt) {
+          const int row0 = (phys * a.Hkv + h) * 16;
           uint8_t* kd = sm + L::kKRing + half * L::kSlot + i * 2048;
           uint8_t* vd = sm + L::kVRing + half * L::kSlot + i * 2048;
           if constexpr (F8) {
