@@ -423,10 +423,10 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const TcArgs a,
         mma_commit(&ctl->s_full[sb]);
         if constexpr (F8) mma_commit(&ctl->kv_empty[j % R]);  // K is read; V was converted
       };
-      // Order: S(0), S(1), then per block i: O += P(i) V(i), and once that is
-      // done (its P lives in S buffer i % 2), S(i + 2).  The tensor pipe thus
-      // runs P V and the next Q K^T back to back while the softmax works on
-      // block i + 1, whose S was computed one step earlier.
+      // Order: S(0), S(1), then per block i: O += P(i) V(i) and S(i + 2) right
+      // behind it (its P lives in S buffer i % 2; the MMAs run in issue order).
+      // The tensor pipe thus runs P V and the next Q K^T back to back while the
+      // softmax works on block i + 1, whose S was computed one step earlier.
       bool run = true;
       for (int j = 0; j < 2 && j < nblk && run; ++j) {
         run = wait_or_abort(&ctl->kv_full[j % R], (j / R) & 1, abort_flag, a.err);
@@ -456,10 +456,10 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const TcArgs a,
         if constexpr (F8) mma_commit(&ctl->vt_empty[vb]);
         else mma_commit(&ctl->kv_empty[i % R]);  // K and V of block i are read
         if (i + 2 < nblk) {
-          // Phase distance: o_done(i - 1) was awaited one step earlier and only
-          // P V(i) is outstanding, so o_done has completed i or i + 1 phases.
+          // S(i + 2) goes into the TMEM columns P V(i) reads P(i) from.  The
+          // MMAs of one thread run in issue order, so Q K^T(i + 2) is issued
+          // right behind P V(i) without waiting for it to finish.
           if (!wait_or_abort(&ctl->kv_full[(i + 2) % R], ((i + 2) / R) & 1, abort_flag, a.err)) break;
-          if (!wait_or_abort(&ctl->o_done, i & 1, abort_flag, a.err)) break;
           tc_fence_after();
           issue_qk(i + 2);
         }
@@ -673,8 +673,10 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const TcArgs a,
         m = mx;
       }
       // O is rescaled once the previous block's P V is done (rarely needed).
-      // Phase distance: QK(j) waited for P V(j - 2), and P V(j) needs this
-      // block's P, so o_done has completed j - 1 or j phases here.
+      // Phase distance: s_full(j) was committed after Q K^T(j), issued after
+      // P V(j - 2), and a commit tracks every earlier MMA of the thread, so
+      // P V(j - 2) is done; P V(j) needs this block's P.  So o_done has
+      // completed j - 1 or j phases here.
       if (ok && j > 0 && __any_sync(kAll, ov != 1.f)) {
         ok = __all_sync(kAll, wait_or_abort(&ctl->o_done, (j - 1) & 1, abort_flag, a.err));
         if (ok) {
