@@ -210,6 +210,13 @@ __device__ __forceinline__ void tmem_st16u(uint32_t taddr, const uint32_t* w) {
         "r"(w[8]), "r"(w[9]), "r"(w[10]), "r"(w[11]), "r"(w[12]), "r"(w[13]), "r"(w[14]), "r"(w[15])
       : "memory");
 }
+__device__ __forceinline__ void tmem_ld16u(uint32_t taddr, uint32_t* w) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+      : "=r"(w[0]), "=r"(w[1]), "=r"(w[2]), "=r"(w[3]), "=r"(w[4]), "=r"(w[5]), "=r"(w[6]), "=r"(w[7]),
+        "=r"(w[8]), "=r"(w[9]), "=r"(w[10]), "=r"(w[11]), "=r"(w[12]), "=r"(w[13]), "=r"(w[14]), "=r"(w[15])
+      : "r"(taddr));
+}
 __device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 __device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
@@ -632,21 +639,24 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const TcArgs a,
         vinv = vref > 0.f ? 1.f / vref : 0.f;
       }
       ok = __all_sync(kAll, ok && wait_or_abort(&ctl->s_full[sb], u & 1, abort_flag, a.err));
-      // Scores in log2 units are s * f_page, f_page > 0.  S is read 32 columns
-      // at a time, twice: the block max first, then the exponentials; the causal
-      // mask runs only on blocks that reach the tile's first query.
+      // Scores in log2 units are s * f_page, f_page > 0.  The thread's 64 scores
+      // are read from TMEM once and kept in registers through the max exchange
+      // (the block max first, then the exponentials); the causal mask runs only
+      // on blocks that reach the tile's first query.
       const int key0 = 128 * j;
       const bool diag = key0 + 127 > pos0;
       const uint32_t sbase = trow + sb * 128;
       float mh = -INFINITY;
+      float sv[2][32];  // this thread's 64 scores of the block, read from TMEM once
       if (ok) {
         tc_fence_after();
-#pragma unroll 1
+        tmem_ld32(sbase + 32 * (2 * hf), sv[0]);
+        tmem_ld32(sbase + 32 * (2 * hf + 1), sv[1]);
+        tmem_wait_ld();
+#pragma unroll
         for (int cc = 0; cc < 2; ++cc) {
           const int c = 2 * hf + cc;
-          float v[32];
-          tmem_ld32(sbase + 32 * c, v);
-          tmem_wait_ld();
+          float* v = sv[cc];
           if (diag) {
 #pragma unroll
             for (int e = 0; e < 32; ++e)
@@ -682,14 +692,14 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const TcArgs a,
         if (ok) {
           tc_fence_after();
 #pragma unroll 1
-          for (int cc = 0; cc < 2; ++cc) {
-            float o[32];
-            const uint32_t oc = trow + kOCol + 64 * hf + 32 * cc;
-            tmem_ld32(oc, o);
+          for (int cc = 0; cc < 4; ++cc) {  // 16 columns at a time (the scores are live)
+            uint32_t o[16];
+            const uint32_t oc = trow + kOCol + 64 * hf + 16 * cc;
+            tmem_ld16u(oc, o);
             tmem_wait_ld();
 #pragma unroll
-            for (int e = 0; e < 32; ++e) o[e] *= ov;
-            tmem_st32(oc, o);
+            for (int e = 0; e < 16; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * ov);
+            tmem_st16u(oc, o);
           }
           tmem_wait_st();
         }
@@ -698,17 +708,10 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const TcArgs a,
       // columns 32c .. 32c+15 (the low part, fp32 mode, to 32c+16 .. 32c+31)
       if (ok) {
         float rs = 0.f;
-#pragma unroll 1
+#pragma unroll
         for (int cc = 0; cc < 2; ++cc) {
           const int c = 2 * hf + cc;
-          float v[32];
-          tmem_ld32(sbase + 32 * c, v);
-          tmem_wait_ld();
-          if (diag) {
-#pragma unroll
-            for (int e = 0; e < 32; ++e)
-              if (key0 + 32 * c + e > qp_of(pos0, tl, n_tok)) v[e] = -INFINITY;
-          }
+          float* v = sv[cc];  // masked in the first pass
 #pragma unroll
           for (int hp = 0; hp < 2; ++hp) {
             const float f = BLK ? row_scale * fmaxf(ctl->sc[sb][2 * c + hp].x, 1.17549435e-38f) : row_scale;
