@@ -622,6 +622,13 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const TcArgs a,
       __syncwarp();
       if (lane == 0) mbar_arrive(&ctl->q_ready);
     }
+    // Masked keys hold -inf and meet the score factor in the exponent's
+    // multiply, where a zero factor (softmax_scale 0, or a page of zero K
+    // scale) would give -inf * 0 = NaN.  Every factor is kept at or above the
+    // smallest normal float: scores then round to ~0 in log2 units and the
+    // visible keys weigh the same, which is what a zero scale asks for.
+    constexpr float kMinFactor = 1.17549435e-38f;
+    row_scale = fmaxf(row_scale, kMinFactor);
 
     float m = -INFINITY, l = 0.f, vref = 0.f;
     for (int j = 0; j < nblk; ++j) {
@@ -646,6 +653,12 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const TcArgs a,
       const int key0 = 128 * j;
       const bool diag = key0 + 127 > pos0;
       const uint32_t sbase = trow + sb * 128;
+      float pf[2][2];  // the score factor of each of the thread's four pages
+#pragma unroll
+      for (int cc = 0; cc < 2; ++cc)
+#pragma unroll
+        for (int hp = 0; hp < 2; ++hp)
+          pf[cc][hp] = BLK ? fmaxf(row_scale * ctl->sc[sb][2 * (2 * hf + cc) + hp].x, kMinFactor) : row_scale;
       float mh = -INFINITY;
       float sv[2][32];  // this thread's 64 scores of the block, read from TMEM once
       if (ok) {
@@ -653,25 +666,22 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const TcArgs a,
         tmem_ld32(sbase + 32 * (2 * hf), sv[0]);
         tmem_ld32(sbase + 32 * (2 * hf + 1), sv[1]);
         tmem_wait_ld();
+        float pm[2][2];  // each page's largest raw score
 #pragma unroll
         for (int cc = 0; cc < 2; ++cc) {
-          const int c = 2 * hf + cc;
           float* v = sv[cc];
           if (diag) {
 #pragma unroll
             for (int e = 0; e < 32; ++e)
-              if (key0 + 32 * c + e > qp_of(pos0, tl, n_tok)) v[e] = -INFINITY;
+              if (key0 + 32 * (2 * hf + cc) + e > qp_of(pos0, tl, n_tok)) v[e] = -INFINITY;
           }
-#pragma unroll
-          for (int hp = 0; hp < 2; ++hp) {  // the chunk's two pages
-            const float f = BLK ? row_scale * fmaxf(ctl->sc[sb][2 * c + hp].x, 1.17549435e-38f) : row_scale;
-            float t[4];
-#pragma unroll
-            for (int e = 0; e < 4; ++e)
-              t[e] = fmaxf(fmaxf(v[16 * hp + e], v[16 * hp + 4 + e]), fmaxf(v[16 * hp + 8 + e], v[16 * hp + 12 + e]));
-            mh = fmaxf(mh, fmaxf(fmaxf(t[0], t[1]), fmaxf(t[2], t[3])) * f);
-          }
+          pm[cc][0] = max16(v);
+          pm[cc][1] = max16(v + 16);
         }
+        if constexpr (BLK)
+          mh = fmaxf(fmax3f(pm[0][0] * pf[0][0], pm[0][1] * pf[0][1], pm[1][0] * pf[1][0]), pm[1][1] * pf[1][1]);
+        else  // one positive factor: the largest product is the largest score times it
+          mh = fmaxf(fmax3f(pm[0][0], pm[0][1], pm[1][0]), pm[1][1]) * row_scale;
       }
       float m0, m1;
       exchange(mh, m0, m1);
@@ -714,16 +724,31 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const TcArgs a,
           float* v = sv[cc];  // masked in the first pass
 #pragma unroll
           for (int hp = 0; hp < 2; ++hp) {
-            const float f = BLK ? row_scale * fmaxf(ctl->sc[sb][2 * c + hp].x, 1.17549435e-38f) : row_scale;
+            // two keys per packed multiply-add and add; the sums keep the
+            // order of four running sums over keys e = 0, 1, 2, 3 (mod 4)
+            const float2 f2 = make_float2(pf[cc][hp], pf[cc][hp]), nm = make_float2(-m, -m);
             const float vm = BLK ? ctl->sc[sb][2 * c + hp].y * vinv : 1.f;
-            float t[4] = {0.f, 0.f, 0.f, 0.f};
+            const float2 vm2 = make_float2(vm, vm);
+            float2 t01 = make_float2(0.f, 0.f), t23 = t01;
+            float* x = v + 16 * hp;
 #pragma unroll
-            for (int e = 0; e < 16; ++e) {
-              const float pe = fast_exp2(fmaf(v[16 * hp + e], f, -m));
-              t[e & 3] += pe;
-              v[16 * hp + e] = BLK ? pe * vm : pe;
+            for (int e = 0; e < 16; e += 4) {
+              const float2 za = __ffma2_rn(make_float2(x[e], x[e + 1]), f2, nm);
+              const float2 zb = __ffma2_rn(make_float2(x[e + 2], x[e + 3]), f2, nm);
+              float2 pa = make_float2(fast_exp2(za.x), fast_exp2(za.y));
+              float2 pb = make_float2(fast_exp2(zb.x), fast_exp2(zb.y));
+              t01 = __fadd2_rn(t01, pa);
+              t23 = __fadd2_rn(t23, pb);
+              if constexpr (BLK) {
+                pa = __fmul2_rn(pa, vm2);
+                pb = __fmul2_rn(pb, vm2);
+              }
+              x[e] = pa.x;
+              x[e + 1] = pa.y;
+              x[e + 2] = pb.x;
+              x[e + 3] = pb.y;
             }
-            rs += (t[0] + t[1]) + (t[2] + t[3]);
+            rs += (t01.x + t01.y) + (t23.x + t23.y);
           }
           uint32_t ph[16], pl[16];  // in V's type: bfloat16 for bfloat16 pools, else binary16
 #pragma unroll
