@@ -125,22 +125,6 @@ __device__ __forceinline__ float fast_exp2(float x) {
   return y;
 }
 
-// max(a, b, c) in one instruction (the three-input max.f32 of sm_100 and
-// later); like fmaxf, a NaN input is ignored.
-__device__ __forceinline__ float fmax3f(float a, float b, float c) {
-  float d;
-  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
-  return d;
-}
-
-// Largest of v[0 .. 15]: eight maxima, three deep.
-__device__ __forceinline__ float max16(const float* v) {
-  const float a = fmax3f(v[0], v[1], v[2]), b = fmax3f(v[3], v[4], v[5]);
-  const float c = fmax3f(v[6], v[7], v[8]), d = fmax3f(v[9], v[10], v[11]);
-  const float e = fmax3f(v[12], v[13], v[14]);
-  return fmaxf(fmax3f(a, b, c), fmax3f(d, e, v[15]));
-}
-
 // L2 policy for data streamed exactly once (the KV tiles of a decode pass).
 __device__ __forceinline__ uint64_t l2_evict_first_policy() {
   uint64_t p;

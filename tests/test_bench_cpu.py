@@ -55,3 +55,11 @@ def test_source_hash_ignores_comments_only(bench, tmp_path, monkeypatch):
     assert bench._source_sha() == h0
     (csrc / "pa_decode.cu").write_text("int a = 1;\nint b = 3;\n")
     assert bench._source_sha() != h0
+
+
+def test_recorded_traffic_describes_the_current_decode_source(bench):
+    """The DRAM traffic recorded from ncu is reported only while the decode
+    kernel's code is the code it was taken on; a change to pa_decode.cu or
+    pa_device.cuh (beyond comments) needs a new capture, or the line carries
+    traffic null."""
+    assert bench._source_sha() == bench.NCU_TRAFFIC["source_sha256"]
