@@ -115,6 +115,49 @@ def test_equal_keys_give_running_mean(oracle_mod):
         assert np.allclose(out[j], p / 2.0, rtol=0, atol=1e-12)
 
 
+def test_zero_scale_gives_mean_of_visible_values(oracle_mod):
+    """softmax_scale 0: every visible key has logit 0, so query row p of a
+    chunk is the mean of V over tokens 0 .. p of its kv head (and a decode row
+    the mean over the whole context), computed here from the stored values."""
+    w = W.make("tiny_fp16")
+    kp, vp = _filled(oracle_mod, w)
+    chunks = [3, 17, 1, 40]
+    q, q_start = _queries(w, chunks)
+    pre = oracle_mod.paged_prefill("fp16", "fp16", w.num_blocks, 16, w.n_kv_heads, w.head_dim,
+                                   kp, vp, 1.0, 1.0, q, q_start, w.block_tables, w.ctx_lens, 0.0)
+    dec = oracle_mod.paged_attention("fp16", "fp16", w.num_blocks, 16, w.n_kv_heads, w.head_dim,
+                                     kp, vp, 1.0, 1.0, q[q_start[1:] - 1], w.block_tables,
+                                     w.ctx_lens, 0.0)
+    G = w.n_q_heads // w.n_kv_heads
+    for s, C in enumerate(chunks):
+        n = int(w.ctx_lens[s])
+        _, v = w.kv_bits(s, 0, n)
+        vals = v.view(np.float16).astype(np.float64)  # [n, Hkv, d]
+        run = np.cumsum(vals, axis=0) / np.arange(1, n + 1)[:, None, None]
+        for j in range(C):
+            want = np.repeat(run[n - C + j], G, axis=0)  # query head g reads kv head g // G
+            assert np.allclose(pre[q_start[s] + j], want, rtol=0, atol=1e-12)
+        assert np.allclose(dec[s], np.repeat(run[n - 1], G, axis=0), rtol=0, atol=1e-12)
+
+
+def test_negated_scale_equals_negated_queries(oracle_mod):
+    """softmax(-s q.k) = softmax(s (-q).k): a negative score scale is the
+    softmax of the negated scores, not of their magnitudes (negating fp16 q is
+    exact, so the two calls agree bit for bit)."""
+    w = W.make("tiny_fp16")
+    kp, vp = _filled(oracle_mod, w)
+    chunks = [4, 9, 1, 30]
+    q, q_start = _queries(w, chunks)
+    s = w.softmax_scale
+    args = ("fp16", "fp16", w.num_blocks, 16, w.n_kv_heads, w.head_dim, kp, vp, 1.0, 1.0)
+    a = oracle_mod.paged_prefill(*args, q, q_start, w.block_tables, w.ctx_lens, -s)
+    b = oracle_mod.paged_prefill(*args, q ^ np.uint16(0x8000), q_start, w.block_tables,
+                                 w.ctx_lens, s)
+    c = oracle_mod.paged_prefill(*args, q, q_start, w.block_tables, w.ctx_lens, s)
+    assert np.array_equal(a, b)
+    assert not np.allclose(a, c)  # the sign matters
+
+
 def test_invalid_chunk_rejected(oracle_mod):
     w = W.make("tiny_fp16")
     kp, vp = _filled(oracle_mod, w)
