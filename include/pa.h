@@ -303,7 +303,10 @@ PA_API int pa_decode_workspace_bytes(const pa_pool* pool, int S, int n_q_heads, 
  *   ctx_lens_dev      device int32 [S]: tokens of context of each sequence,
  *                     including the token written this step; 0 gives a zero
  *                     output row
- *   softmax_scale     multiplies q.k (usually 1/sqrt(head_dim))
+ *   softmax_scale     multiplies q.k (usually 1/sqrt(head_dim)); any finite
+ *                     value (0 weighs every visible token the same, a negative
+ *                     scale takes the softmax of the negated scores), else
+ *                     PA_ERR_INVALID
  *   num_splits        0 = automatic; else the number of splits along the pages
  *                     (a second kernel merges the partial results)
  *   workspace         device scratch of at least pa_decode_workspace_bytes
@@ -363,6 +366,7 @@ PA_API int pa_decode_no_alloc(pa_pool* pool, int layer, void* out, int out_dtype
  *                     chunk included (>= its chunk length)
  *   out               device [T][n_q_heads][head_dim], q's dtype or PA_FP32
  *   max_chunk         an upper bound on every chunk length (sizes the grid)
+ *   softmax_scale     as for pa_decode
  * Query row j of a chunk of C tokens sits at position ctx - C + j and attends
  * to tokens [0, ctx - C + j] of its sequence (grouped-query heads as in
  * pa_decode).  Invalid ids or lengths set PA_ERR_BOUNDS in the device error
