@@ -164,3 +164,48 @@ def test_invalid_chunk_rejected(oracle_mod):
     q, q_start = _queries(w, [1, 1, 1, 101])   # chunk longer than the context
     with pytest.raises(ValueError):
         _prefill(oracle_mod, w, kp, vp, q, q_start)
+
+
+def _tiny_of_kind(kv_dtype):
+    w = W.make("tiny_fp16")
+    w.kv_dtype = kv_dtype
+    if kv_dtype == "fp8_e4m3":
+        w.k_scale, w.v_scale = 2.0 ** -5, 2.0 ** -5  # N(0,1) values span many E4M3 binades
+    return w
+
+
+def _filled_kind(oracle_mod, w):
+    nbytes = oracle_mod.pool_bytes(w.kv_dtype, w.num_blocks, 16, w.n_kv_heads, w.head_dim)
+    kp, vp = np.zeros(nbytes, np.uint8), np.zeros(nbytes, np.uint8)
+    for s in range(w.S):
+        n = int(w.ctx_lens[s])
+        for lo in range(0, n, 7):  # several calls per sequence: block-scaled tiles re-encode
+            k, v = w.kv_bits(s, lo, min(n, lo + 7))
+            assert oracle_mod.reshape_and_cache(w.kv_dtype, w.num_blocks, 16, w.n_kv_heads,
+                                                w.head_dim, k, v, w.slots(s, lo, min(n, lo + 7)),
+                                                w.k_scale, w.v_scale, kp, vp) == 0
+    return kp, vp
+
+
+@pytest.mark.parametrize("kv_dtype", ["bf16", "fp8_e4m3", "fp8_e4m3_block"])
+def test_rows_are_decodes_for_every_pool_kind(oracle_mod, kv_dtype):
+    """On every pool kind, row j of a chunk ending at ctx equals a decode with
+    context ctx - C + j + 1 (one-token chunks are plain decode steps)."""
+    w = _tiny_of_kind(kv_dtype)
+    kp, vp = _filled_kind(oracle_mod, w)
+    chunks = [1, 17, 5, 40]
+    rng = np.random.default_rng(11)
+    q = W.f32_to_bf16_bits(rng.standard_normal((sum(chunks), w.n_q_heads, w.head_dim),
+                                               dtype=np.float32))
+    q_start = np.concatenate([[0], np.cumsum(chunks)]).astype(np.int32)
+    args = (kv_dtype, "bf16", w.num_blocks, 16, w.n_kv_heads, w.head_dim, kp, vp, w.k_scale,
+            w.v_scale)
+    pre = oracle_mod.paged_prefill(*args, q, q_start, w.block_tables, w.ctx_lens,
+                                   w.softmax_scale)
+    for s, C in enumerate(chunks):
+        for j in range(C):
+            r = q_start[s] + j
+            ctx = np.array([w.ctx_lens[s] - C + j + 1], np.int32)
+            dec = oracle_mod.paged_attention(*args, q[r:r + 1], w.block_tables[s:s + 1], ctx,
+                                             w.softmax_scale)
+            assert np.array_equal(pre[r], dec[0])
