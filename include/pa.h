@@ -115,12 +115,16 @@ PA_API int pa_kv_bytes_per_token(int n_layers, int n_kv_heads, int head_dim, int
 
 /* Bytes of device memory the caller must provide for the K region and for the
  * V region of a pool described by *desc (all layers; for PA_FP8_E4M3_BLOCK the
- * scale table included, the total rounded up to a multiple of 16). */
+ * scale table included, the total rounded up to a multiple of 16).
+ * PA_ERR_UNSUPPORTED if one layer would hold more than 2^31 - 1 token rows
+ * (num_blocks * n_kv_heads * 16): the kernels address a layer's region with
+ * the 32-bit signed row coordinates of the tensor copies. */
 PA_API int pa_pool_bytes(const pa_pool_desc* desc, size_t* k_bytes, size_t* v_bytes);
 
 /* Largest num_blocks whose K + V regions (tiles and, for PA_FP8_E4M3_BLOCK,
  * 2 * n_layers * n_kv_heads fp32 scales per block) fit in budget_bytes
- * (desc->num_blocks is ignored).  PA_ERR_NO_MEMORY if not even one block fits -- the "no
+ * (desc->num_blocks is ignored), and at most the 2^31 - 1 token rows per layer that
+ * pa_pool_bytes allows.  PA_ERR_NO_MEMORY if not even one block fits -- the "no
  * available memory for the cache blocks" start-up failure ("Optimización de KV
  * Cache ...", section 6.1). */
 PA_API int pa_pool_blocks_for_budget(const pa_pool_desc* desc, size_t budget_bytes, int* num_blocks);
@@ -128,7 +132,8 @@ PA_API int pa_pool_blocks_for_budget(const pa_pool_desc* desc, size_t budget_byt
 /* Creates a pool over caller-owned device regions k_cache and v_cache (each at
  * least the pa_pool_bytes size, 16-byte aligned).  The host allocator starts
  * with every block free; its LIFO free list hands out 0, 1, 2, ... first.
- * The pool does not own the device memory. */
+ * The pool does not own the device memory.  The same limit of 2^31 - 1 token
+ * rows per layer as pa_pool_bytes (PA_ERR_UNSUPPORTED). */
 PA_API int pa_pool_create(const pa_pool_desc* desc, void* k_cache, void* v_cache, pa_pool** out);
 
 /* Destroys the host state of a pool (device memory is untouched). NULL is OK. */

@@ -58,6 +58,22 @@ int check_desc_shape(const pa_pool_desc* d) {
   return PA_OK;
 }
 
+// The kernels address a layer's K or V region as rows of one token of one KV
+// head, with the 32-bit signed coordinates of the tensor copies: one layer
+// may hold at most this many blocks.
+long long max_blocks_per_layer(const pa_pool_desc* d) {
+  return 0x7FFFFFFFll / ((long long)d->n_kv_heads * d->block_size);
+}
+
+int check_rows(const pa_pool_desc* d) {
+  if ((long long)d->num_blocks > max_blocks_per_layer(d))
+    return pa::fail(PA_ERR_UNSUPPORTED,
+                    "%d blocks x %d kv heads x 16 token rows exceed the 2^31 - 1 rows one layer "
+                    "may hold (at most %lld blocks)",
+                    d->num_blocks, d->n_kv_heads, max_blocks_per_layer(d));
+  return PA_OK;
+}
+
 size_t tile_bytes_all_layers(const pa_pool_desc* d) {
   // K + V codes, every layer, one block
   return 2ull * (size_t)d->n_layers * (size_t)d->n_kv_heads * (size_t)d->block_size *
@@ -116,6 +132,8 @@ int pa_pool_bytes(const pa_pool_desc* desc, size_t* k_bytes, size_t* v_bytes) {
   int st = check_desc_shape(desc);
   if (st) return st;
   if (desc->num_blocks < 1) return pa::fail(PA_ERR_INVALID, "num_blocks must be >= 1");
+  st = check_rows(desc);
+  if (st) return st;
   size_t half = tile_bytes_all_layers(desc) / 2 * (size_t)desc->num_blocks;
   half += (scale_bytes_per_block(desc) / 2 * (size_t)desc->num_blocks + 15) / 16 * 16;
   if (k_bytes) *k_bytes = half;
@@ -133,6 +151,7 @@ int pa_pool_blocks_for_budget(const pa_pool_desc* desc, size_t budget_bytes, int
   auto total = [&](size_t nb) {
     return tile_bytes_all_layers(desc) * nb + 2 * ((scale_bytes_per_block(desc) / 2 * nb + 15) / 16 * 16);
   };
+  n = std::min<size_t>(n, (size_t)max_blocks_per_layer(desc));
   while (n > 0 && total(n) > budget_bytes) --n;
   if (n == 0)
     return pa::fail(PA_ERR_NO_MEMORY,
@@ -148,6 +167,8 @@ int pa_pool_create(const pa_pool_desc* desc, void* k_cache, void* v_cache, pa_po
   if (!out) return pa::fail(PA_ERR_INVALID, "null output handle");
   *out = nullptr;
   if (desc->num_blocks < 1) return pa::fail(PA_ERR_NO_MEMORY, "num_blocks must be >= 1");
+  st = check_rows(desc);
+  if (st) return st;
   if (!k_cache || !v_cache) return pa::fail(PA_ERR_INVALID, "null cache region");
   if (((uintptr_t)k_cache | (uintptr_t)v_cache) & 15u)
     return pa::fail(PA_ERR_INVALID, "cache regions must be 16-byte aligned");

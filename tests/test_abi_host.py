@@ -229,3 +229,26 @@ def test_last_error_message(pool):
         N.pa_block_free(pool, [3])
     assert "double free" in str(e.value) or "below refcount" in str(e.value)
     assert "double free" in N.last_error()
+
+
+def test_rows_per_layer_limit(lib):
+    """A layer holds at most 2^31 - 1 token rows (blocks x KV heads x 16), the
+    range of the kernels' 32-bit tile coordinates: sizing, budget and creation
+    agree on the boundary."""
+    heads = 64
+    top = (2**31 - 1) // (heads * 16)                  # 2,097,151 blocks
+    ok = N.make_desc(1, top, heads, 64, N.PA_FP8_E4M3, 1.0, 1.0)
+    over = N.make_desc(1, top + 1, heads, 64, N.PA_FP8_E4M3, 1.0, 1.0)
+    kb, _ = N.pa_pool_bytes(ok)
+    assert kb == top * heads * 16 * 64
+    with pytest.raises(N.PAError) as e:
+        N.pa_pool_bytes(over)
+    assert e.value.code == N.PA_ERR_UNSUPPORTED
+    with pytest.raises(N.PAError) as e:
+        N.pa_pool_create(over, FAKE_K, FAKE_V)
+    assert e.value.code == N.PA_ERR_UNSUPPORTED
+    h = N.pa_pool_create(ok, FAKE_K, FAKE_V)
+    N.pa_pool_destroy(h)
+    assert N.pa_pool_blocks_for_budget(ok, 1 << 50) == top
+    assert N.pa_pool_blocks_for_budget(ok, 2 * kb) == top
+    assert N.pa_pool_blocks_for_budget(ok, 2 * kb - 1) == top - 1
