@@ -370,7 +370,8 @@ PA_API int pa_decode_no_alloc(pa_pool* pool, int layer, void* out, int out_dtype
  *   ctx_lens_dev      device int32 [S]: tokens of each sequence in the cache,
  *                     chunk included (>= its chunk length)
  *   out               device [T][n_q_heads][head_dim], q's dtype or PA_FP32
- *   max_chunk         an upper bound on every chunk length (sizes the grid)
+ *   max_chunk         an upper bound on every chunk length (sizes the grid;
+ *                     rows of a longer chunk past max_chunk are not written)
  *   softmax_scale     as for pa_decode
  * Query row j of a chunk of C tokens sits at position ctx - C + j and attends
  * to tokens [0, ctx - C + j] of its sequence (grouped-query heads as in
