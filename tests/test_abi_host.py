@@ -252,3 +252,39 @@ def test_rows_per_layer_limit(lib):
     assert N.pa_pool_blocks_for_budget(ok, 1 << 50) == top
     assert N.pa_pool_blocks_for_budget(ok, 2 * kb) == top
     assert N.pa_pool_blocks_for_budget(ok, 2 * kb - 1) == top - 1
+
+
+def _c_kind(param: str):
+    param = param.strip()
+    if "*" in param:
+        return "ptr"
+    ctype = param.rsplit(None, 1)[0].replace("const", "").strip()
+    return {"int": ("int", 4), "int32_t": ("int", 4), "size_t": ("int", 8),
+            "uint64_t": ("int", 8), "float": ("float", 4)}[ctype]
+
+
+def _py_kind(t):
+    import ctypes
+    if t in (ctypes.c_void_p, ctypes.c_char_p) or hasattr(t, "_type_") and issubclass(
+            t, ctypes._Pointer):
+        return "ptr"
+    if t is ctypes.c_float:
+        return ("float", 4)
+    return ("int", ctypes.sizeof(t))
+
+
+def test_binding_signatures_match_header(lib):
+    """Every entry point's argument list in the ctypes binding has the header's
+    arity and, position by position, the same kind (pointer, 32- or 64-bit
+    integer, float): a mismatch would pass garbage across the ABI."""
+    decls = {}
+    inc = os.path.join(ROOT, "include")
+    for f in sorted(os.listdir(inc)):
+        if f.endswith(".h"):
+            text = open(os.path.join(inc, f)).read()
+            for name, params in re.findall(r"PA_API\s+int\s+(pa_\w+)\s*\(([^)]*)\)\s*;", text):
+                decls[name] = [_c_kind(p) for p in params.split(",")]
+    sigs = dict(N._SIGS)
+    assert set(sigs) == set(decls)
+    for name, kinds in decls.items():
+        assert [_py_kind(t) for t in sigs[name]] == kinds, name
