@@ -286,15 +286,32 @@ PA_API int pa_swap_in(pa_pool* pool, int n, const int32_t* ids_dev, const void* 
 PA_API int pa_reshape_and_cache(pa_pool* pool, int layer, const void* k, const void* v,
                          const int64_t* slot_mapping_dev, int T, void* stream);
 
+/* num_splits value that asks pa_decode for the balanced schedule (batches of
+ * at most 4096 sequences, else PA_ERR_UNSUPPORTED): one CTA per resident slot
+ * of the GPU, at most four per SM; the pages of every (sequence, kv head)
+ * pair, taken in (sequence, kv head, page) order, are cut into equal
+ * contiguous ranges, one per CTA, from the context lengths on the device, so
+ * every CTA streams the same number of pages whatever the mix of lengths, and
+ * streams from one pair to the next without draining its pipeline.  A pair
+ * whose pages span several CTAs is merged by a second kernel. */
+#define PA_SPLITS_BALANCED (-1)
+
 /* Number of splits pa_decode uses along each sequence's pages for this batch
  * shape when num_splits = 0 (auto): enough (sequence, KV head, split) work
- * units to fill the GPU, each split still covering several pages.
- * Uses the current CUDA device. */
+ * units to fill the GPU, each split still covering several pages (every
+ * sequence is taken as max_blocks_per_seq pages long: the lengths live on the
+ * device).  Uses the current CUDA device. */
 PA_API int pa_decode_num_splits(const pa_pool* pool, int S, int n_q_heads, int max_blocks_per_seq,
                          int* num_splits);
 
-/* Device scratch bytes pa_decode needs for this shape and split count
- * (num_splits = 0: the automatic choice).  0 when one split is used. */
+/* Device scratch bytes pa_decode needs for this shape and num_splits
+ * (0: the automatic count).  Fixed splits: S * n_q_heads * splits *
+ * (head_dim + 2) * 4 (each split's partial softmax states), or 0 for one
+ * split, where splits is num_splits resolved against the table (at most
+ * max_blocks_per_seq, and ceil(max_blocks_per_seq / ceil(max_blocks_per_seq /
+ * num_splits))).  PA_SPLITS_BALANCED: ctas * (2 * G * (head_dim + 2) * 4 + 16),
+ * two partial slots and one merge job per CTA, with ctas the schedule's CTAs
+ * on the current device and G = n_q_heads / n_kv_heads. */
 PA_API int pa_decode_workspace_bytes(const pa_pool* pool, int S, int n_q_heads, int max_blocks_per_seq,
                               int num_splits, size_t* bytes);
 
@@ -312,8 +329,10 @@ PA_API int pa_decode_workspace_bytes(const pa_pool* pool, int S, int n_q_heads, 
  *                     value (0 weighs every visible token the same, a negative
  *                     scale takes the softmax of the negated scores), else
  *                     PA_ERR_INVALID
- *   num_splits        0 = automatic; else the number of splits along the pages
- *                     (a second kernel merges the partial results)
+ *   num_splits        0 = automatic (see pa_decode_num_splits); > 0: the
+ *                     number of splits along the pages (a second kernel merges
+ *                     the partial results); PA_SPLITS_BALANCED: the balanced
+ *                     schedule
  *   workspace         device scratch of at least pa_decode_workspace_bytes
  *                     (may be NULL when that size is 0)
  * Query head g reads KV head g / (n_q_heads / n_kv_heads) (grouped-query
@@ -344,17 +363,25 @@ PA_API int pa_decode(pa_pool* pool, int layer, void* out, int out_dtype, const v
  * keeps the split partials in a fixed array inside the library instead, of
  * PA_NOALLOC_SCRATCH_BYTES.  It allocates nothing and frees nothing.
  *
- *  - num_splits = 0: the automatic split count, lowered if needed until the
- *    partials fit the array (one split needs no scratch at all).  An explicit
- *    num_splits whose partials, S * n_q_heads * num_splits * (head_dim + 2) * 4
- *    bytes, exceed PA_NOALLOC_SCRATCH_BYTES is rejected with PA_ERR_INVALID.
+ *  - num_splits = 0: the automatic split count, lowered until its partials
+ *    fit the array (one split needs no scratch at all).
+ *  - num_splits = PA_SPLITS_BALANCED: at most PA_NOALLOC_SCRATCH_BYTES /
+ *    (2 * G * (head_dim + 2) * 4 + 16) CTAs (more than the resident slots of
+ *    a GB300 for every supported shape, so the same launch as pa_decode).
+ *  - num_splits > 0: resolved against the table as for
+ *    pa_decode_workspace_bytes; a resolved count whose partials,
+ *    S * n_q_heads * splits * (head_dim + 2) * 4 bytes, exceed
+ *    PA_NOALLOC_SCRATCH_BYTES is rejected with PA_ERR_INVALID.
  *  - The first call on a device looks up the array's device address with that
- *    device current; make that first call before any stream capture.
+ *    device current and keeps it for the life of the process; make that first
+ *    call before any stream capture, and make no call after a cudaDeviceReset
+ *    of that device (the kept address would be stale).
  *  - Every call on a device shares the one array and overwrites it.  Each call
  *    writes every partial its merge reads before reading it, so nothing needs
  *    clearing between calls, but calls whose kernels overlap on the GPU (on
  *    different streams, or from different threads) race on it: serialise them.
- * Results equal pa_decode's for the same split count. */
+ *  - Arguments are checked as pa_decode checks them, in the same order.
+ * Results equal pa_decode's for the same schedule: bit for bit. */
 PA_API int pa_decode_no_alloc(pa_pool* pool, int layer, void* out, int out_dtype, const void* q,
                               const int32_t* block_tables_dev, int max_blocks_per_seq,
                               const int32_t* ctx_lens_dev, int S, int n_q_heads,
@@ -366,12 +393,16 @@ PA_API int pa_decode_no_alloc(pa_pool* pool, int layer, void* out, int out_dtype
  * The chunk's K/V must already be in the cache (pa_reshape_and_cache).
  *   q                 device [T][n_q_heads][head_dim], the pool's query dtype;
  *                     sequence s's chunk is rows q_start[s] .. q_start[s+1]-1
- *   q_start_dev       device int32 [S+1], non-decreasing, q_start[0] = 0
+ *   q_start_dev       device int32 [S+1], non-decreasing, q_start[0] = 0,
+ *                     q_start[S] = T (a negative entry or a decreasing pair
+ *                     sets PA_ERR_BOUNDS and that sequence is skipped; entries
+ *                     above T cannot be detected and address past q and out)
  *   ctx_lens_dev      device int32 [S]: tokens of each sequence in the cache,
  *                     chunk included (>= its chunk length)
  *   out               device [T][n_q_heads][head_dim], q's dtype or PA_FP32
  *   max_chunk         an upper bound on every chunk length (sizes the grid;
- *                     rows of a longer chunk past max_chunk are not written)
+ *                     rows of a longer chunk past the grid are not written
+ *                     and PA_ERR_BOUNDS is set)
  *   softmax_scale     as for pa_decode
  * Query row j of a chunk of C tokens sits at position ctx - C + j and attends
  * to tokens [0, ctx - C + j] of its sequence (grouped-query heads as in
@@ -381,6 +412,17 @@ PA_API int pa_prefill(pa_pool* pool, int layer, void* out, int out_dtype, const 
                       const int32_t* q_start_dev, const int32_t* block_tables_dev,
                       int max_blocks_per_seq, const int32_t* ctx_lens_dev, int S, int n_q_heads,
                       int max_chunk, float softmax_scale, void* stream);
+
+/* For tests of the timeout path only: sets, for the current device, how long
+ * the kernels' pipeline waits (a stage's data, a free stage, a hand-off
+ * between warp roles) spin before they give up, record PA_ERR_TIMEOUT and
+ * unwind.  0 restores the default of 2 s.  The waits that drain copies
+ * already in flight before a CTA exits always keep 2 s.  Blocking: it copies
+ * the value into each kernel module's device variable; it holds for every
+ * later launch in the process until it is set again.  (The pages have no
+ * counterpart: the bound itself is what keeps a stalled pipeline from hanging
+ * the GPU.) */
+PA_API int pa_set_pipeline_wait_limit_ns(uint64_t ns);
 
 /* Synchronises `stream`, then reads and clears the current device's error word.
  * *code = PA_OK or the first PA_ERR_* a kernel recorded since the last read.

@@ -30,6 +30,8 @@ PA_FP8_E4M3 = 2
 PA_FP32 = 3
 PA_FP8_E4M3_BLOCK = 4
 
+PA_SPLITS_BALANCED = -1  # num_splits: the balanced decode schedule
+
 ERROR_NAMES = {PA_OK: "PA_OK", PA_ERR_INVALID: "PA_ERR_INVALID",
                PA_ERR_UNSUPPORTED: "PA_ERR_UNSUPPORTED",
                PA_ERR_OUT_OF_BLOCKS: "PA_ERR_OUT_OF_BLOCKS", PA_ERR_NO_MEMORY: "PA_ERR_NO_MEMORY",
@@ -88,6 +90,7 @@ _SIGS = [
     ("pa_decode", [_P, _I, _P, _I, _P, _P, _I, _P, _I, _I, ctypes.c_float, _I, _P, _SZ, _P]),
     ("pa_prefill", [_P, _I, _P, _I, _P, _P, _P, _I, _P, _I, _I, _I, ctypes.c_float, _P]),
     ("pa_decode_no_alloc", [_P, _I, _P, _I, _P, _P, _I, _P, _I, _I, ctypes.c_float, _I, _P]),
+    ("pa_set_pipeline_wait_limit_ns", [ctypes.c_uint64]),
     ("pa_get_device_error", [_P, ctypes.POINTER(_I), _P]),
 ]
 
@@ -312,6 +315,11 @@ def pa_decode_no_alloc(pool: int, layer: int, out_ptr: int, out_dtype: int, q_pt
     _check(lib().pa_decode_no_alloc(pool, layer, out_ptr, out_dtype, q_ptr, tables_ptr,
                                     max_blocks_per_seq, ctx_lens_ptr, S, n_q_heads, softmax_scale,
                                     num_splits, stream))
+
+
+def pa_set_pipeline_wait_limit_ns(ns: int) -> None:
+    """Test-only: the limit of the kernels' pipeline waits in ns (0 = the default 2 s)."""
+    _check(lib().pa_set_pipeline_wait_limit_ns(int(ns)))
 
 
 def pa_get_device_error(pool: int, stream: int) -> int:

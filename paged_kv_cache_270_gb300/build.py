@@ -60,9 +60,11 @@ def build(force: bool = False, verbose: bool = False) -> str:
     for src in cu:
         obj = os.path.join(obj_dir, os.path.basename(src) + ".o")
         jobs.append([nvcc, *ARCH, *NVCC_FLAGS, "-c", src, "-o", obj])
+    # the toolkit's headers (NVTX v3, header-only) for the host translation unit
+    cuda_include = os.path.join(os.path.dirname(os.path.dirname(os.path.realpath(nvcc))), "include")
     for src in cpp:
         obj = os.path.join(obj_dir, os.path.basename(src) + ".o")
-        jobs.append(["g++", *CXX_FLAGS, "-c", src, "-o", obj])
+        jobs.append(["g++", *CXX_FLAGS, "-I", cuda_include, "-c", src, "-o", obj])
 
     def run(cmd):
         r = subprocess.run(cmd, capture_output=True, text=True)
@@ -75,7 +77,7 @@ def build(force: bool = False, verbose: bool = False) -> str:
     with ThreadPoolExecutor(max_workers=max(1, min(len(jobs), os.cpu_count() or 1))) as ex:
         objs = list(ex.map(run, jobs))
     tmp = LIB + f".tmp{os.getpid()}"
-    link = [nvcc, *ARCH, "-shared", "-cudart", "static", "-o", tmp, *objs]
+    link = [nvcc, *ARCH, "-shared", "-cudart", "static", "-o", tmp, *objs, "-ldl"]
     r = subprocess.run(link, capture_output=True, text=True)
     if r.returncode:
         sys.stderr.write(" ".join(link) + "\n" + r.stdout + r.stderr)

@@ -352,6 +352,7 @@ extern "C" {
 
 int pa_reshape_and_cache(pa_pool* pool, int layer, const void* k, const void* v,
                          const int64_t* slot_mapping_dev, int T, void* stream) {
+  pa::TraceRange trace_("pa_reshape_and_cache");
   int st = check_pool_layer(pool, layer);
   if (st) return st;
   if (T < 0) return fail(PA_ERR_INVALID, "T must be >= 0");
@@ -393,6 +394,7 @@ int pa_reshape_and_cache(pa_pool* pool, int layer, const void* k, const void* v,
 }
 
 int pa_copy_blocks(pa_pool* pool, int layer, const int32_t* pairs_dev, int n_pairs, void* stream) {
+  pa::TraceRange trace_("pa_copy_blocks");
   int st = check_pool_layer(pool, layer);
   if (st) return st;
   if (n_pairs < 0) return fail(PA_ERR_INVALID, "n_pairs must be >= 0");
@@ -424,14 +426,17 @@ int pa_swap_block_bytes(const pa_pool* pool, size_t* bytes) {
 }
 
 int pa_swap_out(pa_pool* pool, int n, const int32_t* ids_dev, void* host_buf, void* stream) {
+  pa::TraceRange trace_("pa_swap_out");
   return swap_common(pool, n, ids_dev, host_buf, 1, stream);
 }
 
 int pa_swap_in(pa_pool* pool, int n, const int32_t* ids_dev, const void* host_buf, void* stream) {
+  pa::TraceRange trace_("pa_swap_in");
   return swap_common(pool, n, ids_dev, host_buf, 0, stream);
 }
 
 int pa_get_device_error(pa_pool* pool, int* code, void* stream) {
+  pa::TraceRange trace_("pa_get_device_error");
   (void)pool;
   if (!code) return fail(PA_ERR_INVALID, "null output");
   *code = PA_OK;

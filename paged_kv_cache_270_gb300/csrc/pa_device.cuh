@@ -4,6 +4,7 @@
 #pragma once
 
 #include <cuda_bf16.h>
+#include <cuda_runtime.h>
 #include <cuda_fp16.h>
 #include <cuda_fp8.h>
 #include <stdint.h>
@@ -28,6 +29,12 @@ __device__ __forceinline__ uint64_t global_ns() {
 // Every spin-wait in the library gives up after this long and reports
 // PA_ERR_TIMEOUT instead of hanging the GPU.
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s
+
+// The limit of the pipeline waits (a stage's data, a free stage, a role's
+// hand-off).  Tests of the timeout path lower it through
+// pa_set_pipeline_wait_limit_ns; the waits that drain copies already in flight
+// before a CTA exits keep kWaitLimitNs.  One copy per translation unit.
+static __device__ unsigned long long g_pipe_wait_ns = kWaitLimitNs;
 
 // ---------------------------------------------------------------- mbarrier
 __device__ __forceinline__ uint32_t smem_addr(const void* p) {
@@ -66,14 +73,23 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
 }
 
 // Waits for the phase with the given parity to complete; false after
-// kWaitLimitNs (the caller then records PA_ERR_TIMEOUT and unwinds).
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
+// `limit` ns (the caller then records PA_ERR_TIMEOUT and unwinds).  The drain
+// waits use the default; the pipeline waits pass pipe_wait_limit().
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint64_t limit = kWaitLimitNs) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = global_ns();
   while (!mbar_try_wait(bar, parity)) {
-    if (global_ns() - t0 > kWaitLimitNs) return false;
+    if (global_ns() - t0 > limit) return false;
   }
   return true;
+}
+
+__device__ __forceinline__ uint64_t pipe_wait_limit() { return g_pipe_wait_ns; }
+
+// Host side: sets this translation unit's pipeline wait limit (0: the default).
+static inline cudaError_t set_pipe_wait_limit_here(unsigned long long ns) {
+  const unsigned long long v = ns ? ns : kWaitLimitNs;
+  return cudaMemcpyToSymbol(g_pipe_wait_ns, &v, sizeof(v));
 }
 
 // ---------------------------------------------------------------- bulk copy
@@ -107,6 +123,12 @@ __device__ __forceinline__ void tma_load_3d(void* dst, const void* tmap, int c0,
       "l"(reinterpret_cast<uint64_t>(tmap)), "r"(c0), "r"(c1), "r"(c2), "r"(smem_addr(bar)),
       "l"(policy)
       : "memory");
+}
+
+// Orders this thread's earlier generic-proxy accesses to shared memory before
+// later async-proxy (bulk copy) accesses to it, once the threads meet at a barrier.
+__device__ __forceinline__ void fence_proxy_async_shared() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
 __device__ __forceinline__ void prefetch_tensormap(const void* tmap) {

@@ -20,7 +20,28 @@
 #include <string>
 #include <unordered_map>
 
+#include <nvtx3/nvToolsExt.h>
+
 #include "pa_internal.h"
+
+namespace pa {
+// NVTX v3 is header-only: with no tool attached each call is a no-op.
+static nvtxDomainHandle_t trace_domain() {
+  static nvtxDomainHandle_t d = nvtxDomainCreateA("pagedkv");
+  return d;
+}
+
+TraceRange::TraceRange(const char* name) {
+  nvtxEventAttributes_t e = {};
+  e.version = NVTX_VERSION;
+  e.size = NVTX_EVENT_ATTRIB_STRUCT_SIZE;
+  e.messageType = NVTX_MESSAGE_TYPE_ASCII;
+  e.message.ascii = name;
+  nvtxDomainRangePushEx(trace_domain(), &e);
+}
+
+TraceRange::~TraceRange() { nvtxDomainRangePop(trace_domain()); }
+}  // namespace pa
 
 namespace {
 thread_local std::string g_last_error;

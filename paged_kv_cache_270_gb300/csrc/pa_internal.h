@@ -50,6 +50,14 @@ struct pa_pool {
 
 namespace pa {
 
+// An NVTX range (domain "pagedkv") around one library call: it shows in a
+// profiler's timeline with the kernels the call launched.  NVTX does nothing
+// unless a profiling tool is attached to the process.
+struct TraceRange {
+  explicit TraceRange(const char* name);
+  ~TraceRange();
+};
+
 // Records `msg` as the calling thread's last error and returns `code`.
 int fail(int code, const char* fmt, ...);
 
@@ -76,6 +84,12 @@ int layer_maps(pa_pool* pool, int layer, const CUtensorMap_st** tk, const CUtens
 // The same regions for 16-bit pools as rows of 256 bytes with a 128-byte box,
 // so one page is loaded as two 64-element halves (x = 0 and x = 128 bytes).
 int layer_half_maps(pa_pool* pool, int layer, const CUtensorMap_st** tk, const CUtensorMap_st** tv);
+
+// Set the pipeline wait limit of each translation unit's kernels (see
+// pa_set_pipeline_wait_limit_ns); they return a cudaError_t value.
+int decode_set_wait_limit(unsigned long long ns);
+int prefill_set_wait_limit(unsigned long long ns);
+int prefill_tc_set_wait_limit(unsigned long long ns);
 
 // Chunked prefill on the tcgen05 tensor cores, for the shapes it covers
 // (head_dim 128, 1, 2, 4 or 8 query heads per KV head; FP8 or bfloat16 pools with bf16 or

@@ -131,10 +131,19 @@ __global__ void __launch_bounds__((kMaxGroup + 1) * 32) prefill_kernel(
   const int G = a.G;
   const int q0 = a.q_start[seq];
   const int Cn = a.q_start[seq + 1] - q0;
+  // a negative start or a decreasing pair: the sequence is skipped
+  if (q0 < 0 || Cn < 0) {
+    if (threadIdx.x == 0) record_error(a.err, PA_ERR_BOUNDS);
+    return;
+  }
+  // a chunk longer than the grid covers (max_chunk): its rows past the grid
+  // are not written; the CTA of the last tile reports it
+  if (qt == (int)gridDim.x - 1 && Cn > 16 * (int)gridDim.x && threadIdx.x == 0)
+    record_error(a.err, PA_ERR_BOUNDS);
   const int tok_lo = 16 * qt;
   if (tok_lo >= Cn) return;
   const int ctx = a.ctx[seq];
-  if (Cn < 0 || ctx < Cn || ctx > a.max_blocks * 16) {
+  if (ctx < Cn || ctx > a.max_blocks * 16) {
     if (threadIdx.x == 0) record_error(a.err, PA_ERR_BOUNDS);
     return;
   }
@@ -187,7 +196,7 @@ __global__ void __launch_bounds__((kMaxGroup + 1) * 32) prefill_kernel(
         int stop = 0;
         if (lane == 0) {
           const int k = base + j, stage = k % C::kStages;
-          if (k >= C::kStages && !mbar_wait(&empty[stage], ((k / C::kStages) - 1) & 1)) {
+          if (k >= C::kStages && !mbar_wait(&empty[stage], ((k / C::kStages) - 1) & 1, pipe_wait_limit())) {
             record_error(a.err, PA_ERR_TIMEOUT);
             stop = 1;
           } else {
@@ -281,7 +290,7 @@ __global__ void __launch_bounds__((kMaxGroup + 1) * 32) prefill_kernel(
 
   for (int k = 0; k < npages; ++k) {
     const int stage = k % C::kStages;
-    if (!__all_sync(kFullMask, mbar_wait(&full[stage], (k / C::kStages) & 1))) {
+    if (!__all_sync(kFullMask, mbar_wait(&full[stage], (k / C::kStages) & 1, pipe_wait_limit()))) {
       if (lane == 0) record_error(a.err, PA_ERR_TIMEOUT);
       break;
     }
@@ -559,6 +568,8 @@ int pconfigure(PInfo& pi) {
 }
 
 }  // namespace
+int prefill_set_wait_limit(unsigned long long ns) { return (int)set_pipe_wait_limit_here(ns); }
+
 }  // namespace pa
 
 using namespace pa;
@@ -569,6 +580,7 @@ int pa_prefill(pa_pool* pool, int layer, void* out, int out_dtype, const void* q
                const int32_t* q_start_dev, const int32_t* block_tables_dev, int max_blocks_per_seq,
                const int32_t* ctx_lens_dev, int S, int n_q_heads, int max_chunk,
                float softmax_scale, void* stream) {
+  pa::TraceRange trace_("pa_prefill");
   int st = check_pool_layer(pool, layer);
   if (st) return st;
   const pa_pool_desc& d = pool->desc;

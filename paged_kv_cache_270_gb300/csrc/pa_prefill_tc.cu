@@ -225,7 +225,7 @@ __device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, vo
   const uint64_t t0 = global_ns();
   while (!mbar_try_wait(bar, parity)) {
     if (*abort_flag) return false;
-    if (global_ns() - t0 > kWaitLimitNs) {
+    if (global_ns() - t0 > pipe_wait_limit()) {
       *abort_flag = 1;
       record_error(err, PA_ERR_TIMEOUT);
       return false;
@@ -275,10 +275,19 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const TcArgs a,
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int q0 = a.q_start[seq];
   const int Cn = a.q_start[seq + 1] - q0;
+  // a negative start or a decreasing pair: the sequence is skipped
+  if (q0 < 0 || Cn < 0) {
+    if (threadIdx.x == 0) record_error(a.err, PA_ERR_BOUNDS);
+    return;
+  }
+  // a chunk longer than the grid covers (max_chunk): its rows past the grid
+  // are not written; the CTA of the last tile reports it
+  if (qt == (int)gridDim.x - 1 && Cn > ((int)gridDim.x << (7 - a.lg)) && threadIdx.x == 0)
+    record_error(a.err, PA_ERR_BOUNDS);
   const int tok_lo = qt << (7 - a.lg);  // a tile holds 128 / G query tokens
   if (tok_lo >= Cn) return;
   const int ctx = a.ctx[seq];
-  if (Cn < 0 || ctx < Cn || ctx > a.max_blocks * 16) {
+  if (ctx < Cn || ctx > a.max_blocks * 16) {
     if (threadIdx.x == 0) record_error(a.err, PA_ERR_BOUNDS);
     return;
   }
@@ -903,5 +912,7 @@ int prefill_tc(pa_pool* pool, int layer, void* out, int out_dtype, const void* q
   if (e != cudaSuccess) return fail(PA_ERR_CUDA, "prefill (tcgen05) launch: %s", cudaGetErrorString(e));
   return PA_OK;
 }
+
+int prefill_tc_set_wait_limit(unsigned long long ns) { return (int)set_pipe_wait_limit_here(ns); }
 
 }  // namespace pa
