@@ -15,6 +15,7 @@ import numpy as np
 import torch
 
 import oracle
+from paged_kv_cache_270_gb300 import _native as N
 from paged_kv_cache_270_gb300 import workloads as W
 from paged_kv_cache_270_gb300.pool import KVPool
 
@@ -151,3 +152,45 @@ def pool_bytes_equal(pool: KVPool, opools, blocks=None):
             if not np.array_equal(ds, rs):
                 bad = np.argwhere(ds != rs)
                 raise AssertionError(f"{which} scales differ at {len(bad)} tiles, first {bad[:4]}")
+
+
+def full_size_sampled_check(name, sample):
+    """A full-size 70B-shaped decode in the launches the benchmark times (the
+    automatic split count) and with the balanced schedule; the oracle
+    checks the sampled sequences one by one: their blocks bit for bit (block
+    scales too), their bf16 and fp32 outputs within tolerance."""
+    w = W.make(name)
+    w.compute_fp8_scales()
+    pool = new_pool(w, None)
+    fill_both(w, pool, None, chunk_tokens=1 << 17)
+    q = w.q_bits()
+    outs = [(gpu_decode(w, pool, q, num_splits=ns),
+             gpu_decode(w, pool, q, out_dtype=torch.float32, num_splits=ns))
+            for ns in (0, N.PA_SPLITS_BALANCED)]
+    assert pool.device_error() == N.PA_OK
+    for s in sample:
+        n = int(w.ctx_lens[s])
+        ids = w.block_tables[s, :-(-n // 16)]
+        ow = W.Workload(**{**w.__dict__, "ctx_lens": w.ctx_lens[s:s + 1],
+                           "block_tables": np.arange(len(ids), dtype=np.int32)[None, :],
+                           "num_blocks": len(ids)})
+        op = oracle_pools(ow, 0)
+        for lo in range(0, n, 1 << 16):
+            hi = min(n, lo + (1 << 16))
+            k, v = w.kv_bits(s, lo, hi)
+            oracle.reshape_and_cache(w.kv_dtype, len(ids), 16, w.n_kv_heads, w.head_dim, k, v,
+                                     np.arange(lo, hi, dtype=np.int64), w.k_scale, w.v_scale, *op)
+        ref = oracle_decode(ow, op, q[s:s + 1])
+        for out, out32 in outs:
+            check_half(out[s:s + 1], ref, vmax_of(ow, op))
+            check_fp32(out32[s:s + 1], ref)
+        tile = w.n_kv_heads * 16 * w.head_dim
+        for which, o in (("k", op[0]), ("v", op[1])):
+            dev = pool.layer_view(which)[torch.from_numpy(ids.astype(np.int64)).cuda()]
+            assert np.array_equal(dev.cpu().numpy().ravel(), o[:len(ids) * tile]), \
+                f"{which} cache bytes differ (sequence {s})"
+            if w.block_scaled:
+                dsc = pool.scale_view(which)[torch.from_numpy(ids.astype(np.int64)).cuda()]
+                assert np.array_equal(dsc.cpu().numpy(),
+                                      oracle.tile_scales(w.kv_dtype, len(ids), 16, w.n_kv_heads,
+                                                         w.head_dim, o))

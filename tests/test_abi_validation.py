@@ -56,7 +56,7 @@ def _decode(pool, **kw):
     (dict(out_dtype=N.PA_BF16), INV),          # neither the query dtype nor fp32
     (dict(scale=math.nan), INV), (dict(scale=math.inf), INV),
     (dict(out=0), INV), (dict(q=A + 8), INV),  # null, misaligned
-    (dict(num_splits=-1), INV),
+    (dict(num_splits=-2), INV),
     (dict(num_splits=2), INV),                 # two splits need a workspace
     (dict(num_splits=2, ws=A, ws_bytes=16), INV),
 ])
@@ -64,9 +64,31 @@ def test_decode_rejects(pool, kw, code):
     assert _code(_decode, pool, **kw) == code
 
 
+def _decode_no_alloc(pool, **kw):
+    a = dict(layer=0, out=A, out_dtype=N.PA_FP16, q=A, tables=A, max_blocks=4, ctx=A, S=3,
+             Hq=4, scale=0.125, num_splits=1)
+    a.update(kw)
+    N.pa_decode_no_alloc(pool, a["layer"], a["out"], a["out_dtype"], a["q"], a["tables"],
+                         a["max_blocks"], a["ctx"], a["S"], a["Hq"], a["scale"], a["num_splits"], 0)
+
+
+@pytest.mark.parametrize("kw, code", [
+    (dict(layer=2), INV), (dict(Hq=3), INV), (dict(Hq=18), UNS), (dict(S=70000), UNS),
+    (dict(S=-1), INV), (dict(max_blocks=0), INV), (dict(out_dtype=N.PA_BF16), INV),
+    (dict(scale=math.nan), INV), (dict(out=0), INV), (dict(q=A + 8), INV),
+    (dict(num_splits=-2), INV),
+    # an empty batch is still checked for its output type and scale, as pa_decode does
+    (dict(S=0, out_dtype=N.PA_BF16), INV), (dict(S=0, scale=math.inf), INV),
+])
+def test_decode_no_alloc_checks_match_decode(pool, kw, code):
+    assert _code(_decode, pool, **kw) == code
+    assert _code(_decode_no_alloc, pool, **kw) == code
+
+
 def test_decode_empty_batch_is_accepted(pool):
     _decode(pool, S=0)
     _decode(pool, S=0, out=0, q=0)  # nothing is read or written
+    _decode_no_alloc(pool, S=0, out=0, q=0)
 
 
 @pytest.mark.parametrize("B, s, splits", [(10, 1, 1), (10, 3, 3), (10, 4, 4), (10, 6, 5),

@@ -8,8 +8,9 @@ import pytest
 import torch
 
 import oracle
-from gpu_harness import (bits_to_torch, check_fp32, check_half, fill_both, gpu_decode, new_pool,
-                         oracle_decode, oracle_pools, pool_bytes_equal, vmax_of)
+from gpu_harness import (bits_to_torch, check_fp32, check_half, fill_both, full_size_sampled_check,
+                         gpu_decode, new_pool, oracle_decode, oracle_pools, pool_bytes_equal,
+                         vmax_of)
 from paged_kv_cache_270_gb300 import _native as N
 from paged_kv_cache_270_gb300 import workloads as W
 from paged_kv_cache_270_gb300.pool import KVPool
@@ -316,35 +317,14 @@ def test_multi_layer_scales_stay_in_their_layer():
 
 
 @pytest.mark.slow
-def test_llama70b_block_b_full_size_sampled():
-    """256 sequences x 4,096 tokens, 70B shapes, block-scaled FP8, the launch
-    the benchmark times: sampled sequences' outputs and blocks vs the oracle."""
-    w = W.make("llama3_70b_fp8_block_b")
-    pool = new_pool(w, None)
-    fill_both(w, pool, None)
-    q = w.q_bits()
-    out = gpu_decode(w, pool, q)
-    out32 = gpu_decode(w, pool, q, out_dtype=torch.float32)
-    assert pool.device_error() == N.PA_OK
-    for s in (0, 77, 255):
-        ids = w.block_tables[s, :-(-int(w.ctx_lens[s]) // 16)]
-        ow = W.Workload(**{**w.__dict__, "ctx_lens": w.ctx_lens[s:s + 1],
-                           "block_tables": np.arange(len(ids), dtype=np.int32)[None, :],
-                           "num_blocks": len(ids)})
-        op = oracle_pools(ow, 0)
-        k, v = w.kv_bits(s, 0, int(w.ctx_lens[s]))
-        oracle.reshape_and_cache(DT, len(ids), 16, 8, 128, k, v,
-                                 np.arange(int(w.ctx_lens[s]), dtype=np.int64), 1.0, 1.0, *op)
-        ref = oracle.paged_attention(DT, "bf16", len(ids), 16, 8, 128, op[0], op[1], 1.0, 1.0,
-                                     q[s:s + 1], ow.block_tables, ow.ctx_lens, w.softmax_scale)
-        check_half(out[s:s + 1], ref, vmax_of(ow, op))
-        check_fp32(out32[s:s + 1], ref)
-        # the sequence's tiles and scales, bit for bit
-        for which, o in (("k", op[0]), ("v", op[1])):
-            dev = pool.layer_view(which)[torch.from_numpy(ids.astype(np.int64)).cuda()]
-            assert np.array_equal(dev.cpu().numpy().ravel(), o[:len(ids) * 8 * 16 * 128])
-            dsc = pool.scale_view(which)[torch.from_numpy(ids.astype(np.int64)).cuda()]
-            assert np.array_equal(dsc.cpu().numpy(), oracle.tile_scales(DT, len(ids), 16, 8, 128, o))
+@pytest.mark.parametrize("name,sample", [("llama3_70b_fp8_block_a", [0, 1, 2, 3]),
+                                         ("llama3_70b_fp8_block_b", [0, 77, 128, 255])])
+def test_llama70b_block_full_size_sampled(name, sample):
+    """Block-scaled FP8 at the benchmark's full sizes: every sequence of the 4 x
+    131072 batch (19 automatic splits: the one-wave launch that takes the
+    four-CTA register build) and sampled sequences of the 256 x 4096 batch,
+    tiles and scales bit for bit, outputs within tolerance, both schedules."""
+    full_size_sampled_check(name, sample)
 
 
 def test_no_alloc_entry_point_on_block_scaled_pools():

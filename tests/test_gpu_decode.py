@@ -7,8 +7,9 @@ import pytest
 import torch
 
 import oracle
-from gpu_harness import (bits_to_torch, check_fp32, check_half, fill_both, gpu_decode, new_pool,
-                         oracle_decode, oracle_pools, pool_bytes_equal, vmax_of)
+from gpu_harness import (bits_to_torch, check_fp32, check_half, fill_both, full_size_sampled_check,
+                         gpu_decode, new_pool, oracle_decode, oracle_pools, pool_bytes_equal,
+                         vmax_of)
 from paged_kv_cache_270_gb300 import _native as N
 from paged_kv_cache_270_gb300 import workloads as W
 from paged_kv_cache_270_gb300.pool import KVPool
@@ -143,40 +144,16 @@ def _compact(w, seqs):
     return np.array(ids), tables
 
 
+B_SAMPLE = sorted({0, 255} | set(int(x) for x in np.random.default_rng(1234).choice(256, 30,
+                                                                                    replace=False)))
+
+
 @pytest.mark.slow
-@pytest.mark.parametrize("name,sample", [("llama3_70b_fp8_a", [2]),
-                                         ("llama3_70b_fp8_b", [0, 77, 255])])
+@pytest.mark.parametrize("name,sample", [("llama3_70b_fp8_a", [0, 1, 2, 3]),
+                                         ("llama3_70b_fp8_b", B_SAMPLE)])
 def test_llama70b_fp8_full_size_sampled(name, sample):
-    """Full-size long-context FP8 decode in the launch configuration the
-    benchmark times (automatic splits); the oracle checks sampled sequences:
-    their cache blocks bit for bit and their outputs within tolerance."""
-    w = W.make(name)
-    w.compute_fp8_scales()
-    pool = new_pool(w, None)
-    fill_both(w, pool, None, chunk_tokens=1 << 17)
-    q = w.q_bits()
-    out = gpu_decode(w, pool, q)
-    out32 = gpu_decode(w, pool, q, out_dtype=torch.float32)
-    assert pool.device_error() == N.PA_OK
-    ids, tables = _compact(w, sample)
-    ow = W.Workload(**{**w.__dict__, "ctx_lens": w.ctx_lens[sample], "block_tables": tables,
-                       "num_blocks": len(ids)})
-    op = oracle_pools(ow, 0)
-    for r, s in enumerate(sample):
-        n = int(w.ctx_lens[s])
-        for lo in range(0, n, 1 << 16):
-            hi = min(n, lo + (1 << 16))
-            k, v = w.kv_bits(s, lo, hi)
-            pos = np.arange(lo, hi, dtype=np.int64)
-            slots = tables[r, pos // 16].astype(np.int64) * 16 + pos % 16
-            oracle.reshape_and_cache("fp8_e4m3", len(ids), 16, 8, 128, k, v, slots, w.k_scale,
-                                     w.v_scale, *op)
-    for which, o in (("k", op[0]), ("v", op[1])):
-        dev = pool.layer_view(which)[torch.from_numpy(ids).cuda()].cpu().numpy()
-        assert np.array_equal(dev.ravel(), o), f"{which} cache bytes differ"
-    ref = oracle_decode(ow, op, q[sample])
-    check_half(out[sample], ref, vmax_of(ow, op))
-    check_fp32(out32[sample], ref)
+    """Every sequence of the 4 x 131072 batch and 32 of the 256 x 4096 batch."""
+    full_size_sampled_check(name, sample)
 
 
 def test_permutation_invariance_bit_exact_on_gpu():

@@ -186,3 +186,21 @@ def test_prefill_bounds_reported():
     assert pool.device_error() == N.PA_ERR_BOUNDS
     _gpu_prefill(w, pool, q, q_start)
     assert pool.device_error() == N.PA_OK
+    t = torch.from_numpy(w.block_tables).cuda()
+    c = torch.from_numpy(w.ctx_lens).cuda()
+    q40, qs40 = _chunk_queries(w, [40], seed=3)
+    # a chunk longer than the grid max_chunk sizes: the rows the grid covers
+    # are written, the rest are not, and the error is reported
+    out = torch.full((40, w.n_q_heads, w.head_dim), float("nan"), dtype=torch.float16, device="cuda")
+    pool.prefill(bits_to_torch(q40, "fp16"), torch.from_numpy(qs40).cuda(), t, c, max_chunk=16,
+                 out=out)
+    assert pool.device_error() == N.PA_ERR_BOUNDS
+    assert torch.isfinite(out[:16]).all() and torch.isnan(out[16:]).all()
+    # a negative start and a decreasing pair: the sequence is skipped
+    for bad_start in ([-4, 10], [10, 4]):
+        pool.prefill(bits_to_torch(q40, "fp16"), torch.tensor(bad_start, dtype=torch.int32,
+                                                               device="cuda"),
+                     t, c, max_chunk=16, out=out)
+        assert pool.device_error() == N.PA_ERR_BOUNDS
+    _gpu_prefill(w, pool, q, q_start)
+    assert pool.device_error() == N.PA_OK

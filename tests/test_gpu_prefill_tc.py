@@ -146,4 +146,18 @@ def test_bounds_still_reported():
                  torch.from_numpy(w.block_tables).cuda(), torch.from_numpy(w.ctx_lens).cuda(),
                  max_chunk=60)
     assert pool.device_error() == N.PA_ERR_BOUNDS
+    # a chunk longer than the grid max_chunk sizes (one tile of 128 / G = 16
+    # rows here): those rows are written, the rest are not, and the error is reported
+    args = (torch.from_numpy(w.block_tables).cuda(), torch.from_numpy(w.ctx_lens).cuda())
+    q40 = W.f32_to_bf16_bits(np.ones((40, 16, 128), np.float32))
+    out = torch.full((40, 16, 128), float("nan"), dtype=torch.bfloat16, device="cuda")
+    pool.prefill(bits_to_torch(q40, "bf16"), torch.tensor([0, 40], dtype=torch.int32, device="cuda"),
+                 *args, max_chunk=10, out=out)
+    assert pool.device_error() == N.PA_ERR_BOUNDS
+    assert torch.isfinite(out[:16]).all() and torch.isnan(out[16:]).all()
+    # a negative start and a decreasing pair: the sequence is skipped
+    for bad_start in ([-4, 10], [10, 4]):
+        pool.prefill(bits_to_torch(q40, "bf16"), torch.tensor(bad_start, dtype=torch.int32, device="cuda"),
+                     *args, max_chunk=16, out=out)
+        assert pool.device_error() == N.PA_ERR_BOUNDS
     _run(w, pool, op, q, q_start, chunks)

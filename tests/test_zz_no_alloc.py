@@ -4,16 +4,19 @@ loop that must not allocate once running).  It keeps its split partials in a
 fixed array inside the library instead of a caller workspace.
 
 Checked here through the C ABI: two calls in a row, on different shapes, each
-against pa_decode with a caller workspace and the same split count, within the
-tolerances the other decode tests use; and the clear error for a split count
-whose partials exceed the fixed array.  This file is collected last.
+bit for bit against pa_decode with a caller workspace and the same schedule,
+and against the fp64 oracle within the tolerances the other decode tests use;
+an automatic split count that must be lowered to fit the fixed array; and the
+clear error for an explicit split count whose partials exceed it.  This file is
+collected last.
 """
 import numpy as np
 import pytest
 import torch
 
 import oracle
-from gpu_harness import check_fp32, check_half, fill_both, new_pool, oracle_pools, vmax_of
+from gpu_harness import (check_fp32, check_half, fill_both, new_pool, oracle_decode, oracle_pools,
+                         vmax_of)
 from paged_kv_cache_270_gb300 import _native as N
 from paged_kv_cache_270_gb300 import workloads as W
 
@@ -56,8 +59,10 @@ def _both(w, pool, q, t, c, out_dtype, num_splits):
     return ref, got
 
 
-def _as_ref(t):
-    return t.double().cpu().numpy()
+def _same_bits(a, b):
+    """Bit-for-bit equality of two outputs of the same dtype."""
+    view = torch.int32 if a.dtype == torch.float32 else torch.int16
+    return torch.equal(a.view(view), b.view(view))
 
 
 def test_no_alloc_matches_decode_on_two_calls_in_a_row():
@@ -68,24 +73,77 @@ def test_no_alloc_matches_decode_on_two_calls_in_a_row():
     op1 = oracle_pools(w1, 0)
     fill_both(w1, p1, op1)
     q1, t1, c1 = _inputs(w1)
+    want1 = oracle_decode(w1, op1, w1.q_bits())
     ref, got = _both(w1, p1, q1, t1, c1, torch.bfloat16, 24)
-    check_half(got, _as_ref(ref), vmax_of(w1, op1))
+    assert _same_bits(got, ref)
+    check_half(got, want1, vmax_of(w1, op1))
     ref32, got32 = _both(w1, p1, q1, t1, c1, torch.float32, 24)
-    check_fp32(got32, _as_ref(ref32))
+    assert _same_bits(got32, ref32)
+    check_fp32(got32, want1)
 
-    # call 2: another shape and dtype right after, automatic splits; stale
-    # partials of call 1 are still in the array and must not leak in
+    # call 2: another shape and dtype right after, the balanced schedule, the
+    # automatic split count and fixed splits; stale partials of call 1 are still
+    # in the array and must not leak in
     w2 = W.make("llama3_8b_bf16", scale_down=4)
     p2 = new_pool(w2, 0)
     op2 = oracle_pools(w2, 0)
     fill_both(w2, p2, op2)
     q2, t2, c2 = _inputs(w2)
-    for ns in (0, 3):
+    want2 = oracle_decode(w2, op2, w2.q_bits())
+    for ns in (N.PA_SPLITS_BALANCED, 0, 3):
         ref, got = _both(w2, p2, q2, t2, c2, torch.bfloat16, ns)
-        check_half(got, _as_ref(ref), vmax_of(w2, op2))
-    ref32, got32 = _both(w2, p2, q2, t2, c2, torch.float32, 3)
-    check_fp32(got32, _as_ref(ref32))
+        assert _same_bits(got, ref)
+        check_half(got, want2, vmax_of(w2, op2))
+        ref32, got32 = _both(w2, p2, q2, t2, c2, torch.float32, ns)
+        assert _same_bits(got32, ref32)
+        check_fp32(got32, want2)
     assert p1.device_error() == N.PA_OK
+
+
+def test_no_alloc_lowers_an_automatic_split_count_to_fit():
+    """The automatic split count here is two (4100 single-head sequences
+    against 760 resident CTAs, every one taken as 2048 pages long); its partials (2 x 4100 x 8 heads x (128 + 2)
+    floats, 34 MB) do not fit the 8 MiB array, so the entry point takes the
+    largest count that fits (one split, no partials), and matches pa_decode at
+    that count."""
+    rng = np.random.default_rng(31)
+    S, Hkv, G, d, max_blocks = 4100, 1, 8, 128, 2048
+    ctx = rng.integers(1, 60, S).astype(np.int32)
+    need = -(-ctx // 16)
+    nb = int(need.sum())
+    perm = rng.permutation(nb).astype(np.int32)
+    tables = np.zeros((S, max_blocks), np.int32)
+    used = 0
+    for s, k in enumerate(need):
+        tables[s, :k] = perm[used:used + k]
+        used += int(k)
+    w = W.Workload(name="lowered", index=9, kv_dtype="fp8_e4m3", n_q_heads=Hkv * G,
+                   n_kv_heads=Hkv, head_dim=d, ctx_lens=ctx, num_blocks=nb, block_tables=tables,
+                   kv_seed=31)
+    w.compute_fp8_scales()
+    pool = new_pool(w, 0)
+    op = oracle_pools(w, 0)
+    fill_both(w, pool, op)
+    q, t, c = _inputs(w)
+    auto = N.pa_decode_num_splits(pool.handle, S, w.n_q_heads, max_blocks)
+    per_split = S * w.n_q_heads * (d + 2) * 4
+    assert auto >= 2 and auto * per_split > N.PA_NOALLOC_SCRATCH_BYTES, \
+        f"the automatic count ({auto}) should need more than the array here"
+    fit = max(s for s in range(1, auto + 1)
+              if N.pa_decode_workspace_bytes(pool.handle, S, w.n_q_heads, max_blocks, s)
+              <= N.PA_NOALLOC_SCRATCH_BYTES)
+    stream = torch.cuda.current_stream().cuda_stream
+    got = torch.full((S, w.n_q_heads, d), float("nan"), dtype=torch.bfloat16, device="cuda")
+    N.pa_decode_no_alloc(pool.handle, 0, got.data_ptr(), N.PA_BF16, q.data_ptr(), t.data_ptr(),
+                         max_blocks, c.data_ptr(), S, w.n_q_heads, w.softmax_scale, 0, stream)
+    ref = pool.decode(q, t, c, num_splits=fit, softmax_scale=w.softmax_scale)
+    torch.cuda.synchronize()
+    assert _same_bits(got, ref)
+    rows = np.sort(rng.choice(S, 64, replace=False))
+    sub = W.Workload(**{**w.__dict__, "ctx_lens": ctx[rows], "block_tables": tables[rows]})
+    want = oracle_decode(sub, op, w.q_bits()[rows])
+    check_half(got[torch.from_numpy(rows).cuda()], want, vmax_of(w, op))
+    assert pool.device_error() == N.PA_OK
 
 
 def test_no_alloc_rejects_scratch_beyond_its_maximum():
