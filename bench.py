@@ -90,12 +90,12 @@ DESCRIPTION = {
 # measured.
 NCU_TRAFFIC = {
     # hash of the decode source with comments and blank lines removed (see _source_sha)
-    "source_sha256": "d6b7fd0ca4115ea4ec99e80f0a4cdbb1e920f223cf536e76419cf92fbe376762",
+    "source_sha256": "b574fe2c6b5e8fa870cb1f83251857df4c3f72565e291885e0266998434460aa",
     # dram__bytes_read.sum + dram__bytes_write.sum of one decode launch
-    "bytes_per_launch": {"llama3_70b_fp8_a": 1073976576 + 3272960,
-                         "llama3_70b_fp8_b": 2151992320 + 4573184,
-                         "llama3_70b_fp8_block_a": 1076082944 + 3091968,
-                         "llama3_70b_fp8_block_b": 2156268288 + 5209088},
+    "bytes_per_launch": {"llama3_70b_fp8_a": 1073977856 + 3256576,
+                         "llama3_70b_fp8_b": 2152047360 + 4622336,
+                         "llama3_70b_fp8_block_a": 1076084224 + 2768128,
+                         "llama3_70b_fp8_block_b": 2156265216 + 5187328},
 }
 
 # --------------------------------------------------------------------- workers
@@ -283,7 +283,7 @@ class ClockSampler:
 class Batch:
     """One workload batch resident on the GPU: filled pool plus the step's inputs."""
 
-    def __init__(self, name, pool_procs):
+    def __init__(self, name, pool_procs, num_splits=0):
         import torch
 
         from paged_kv_cache_270_gb300 import _native as N
@@ -341,15 +341,19 @@ class Batch:
         self.d_tables = self.h_tables.cuda()
         self.d_ctx = self.h_ctx.cuda()
         self.d_out = torch.empty((S, Hq, D), dtype=in_t, device="cuda")
-        self.splits = self.pool.num_splits(S, Hq, self.max_blocks)
-        self.ws_bytes = self.pool.workspace_bytes(S, Hq, self.max_blocks, 0)
+        # 0: the library's automatic schedule; else a fixed split count
+        self.num_splits = num_splits
+        self.splits = num_splits or self.pool.num_splits(S, Hq, self.max_blocks)
+        self.ws_bytes = self.pool.workspace_bytes(S, Hq, self.max_blocks, num_splits)
         self.ws = torch.empty(max(self.ws_bytes, 16), dtype=torch.uint8, device="cuda")
         self.kv_bytes = w.kv_bytes()
         self.h2d_bytes = sum(t.numel() * t.element_size() for t in
                              (self.h_q, self.h_k, self.h_v, self.h_slots, self.h_tables,
                               self.h_ctx))
         self.d2h_bytes = self.d_out.numel() * self.d_out.element_size()
-        self.launches = 2 + (1 if self.splits > 1 else 0)
+        # cache write + decode, + the merge: always with the balanced schedule
+        # (splits -1), with fixed splits when there are several
+        self.launches = 2 + (1 if self.splits != 1 else 0)
         self.softmax_scale = w.softmax_scale
         self.out_code = N.PA_FP16 if w.in_dtype == "fp16" else N.PA_BF16
 
@@ -360,7 +364,7 @@ class Batch:
     def decode(self, stream):
         self.N.pa_decode(self.pool.handle, 0, self.d_out.data_ptr(), self.out_code,
                          self.d_q.data_ptr(), self.d_tables.data_ptr(), self.max_blocks,
-                         self.d_ctx.data_ptr(), self.S, self.Hq, self.softmax_scale, 0,
+                         self.d_ctx.data_ptr(), self.S, self.Hq, self.softmax_scale, self.num_splits,
                          self.ws.data_ptr(), self.ws_bytes, stream)
 
 
@@ -432,8 +436,9 @@ def _max_over_ranks(x, world):
     return float(t.item())
 
 
-def cpu_baseline(names, scales, seconds, procs, pool):
-    """Time the oracle on a bounded sample of the workload's sequences."""
+def cpu_baseline(names, scales, seconds, procs, pool, single_core=True):
+    """Time the oracle on a bounded sample of the workload's sequences, one
+    process per core (and, with single_core, in one process on a smaller sample)."""
     # calibrate: one short sequence set first, then size the sample
     from paged_kv_cache_270_gb300 import workloads as W
     jobs = []
@@ -456,9 +461,328 @@ def cpu_baseline(names, scales, seconds, procs, pool):
         sample_desc.append(f"{name}: {n} of {w.S} sequences")
     total = sum(r[0] for r in results)
     wall = max(r[2] for r in results) - min(r[1] for r in results)
-    return {"value": total / wall / 1e9, "unit": "GB/s", "cores": procs, "kind": "oracle",
-            "sample": "; ".join(sample_desc) + f" ({total / 1e6:.0f} MB of K+V, "
-                      f"{wall:.1f} s wall, fp64 gather + softmax attention)"}
+    rec = {"value": total / wall / 1e9, "unit": "GB/s", "cores": procs, "kind": "oracle",
+           "cpu_model": _cpu_model(), "host_cores": os.cpu_count(),
+           "sample": "; ".join(sample_desc) + f" ({total / 1e6:.0f} MB of K+V, "
+                     f"{wall:.1f} s wall, fp64 gather + softmax attention, one process per core)"}
+    if single_core:
+        # the same oracle in one process (one core), on a sample of about seconds / 2
+        name, w, order = jobs[-1]
+        n1 = max(1, min(w.S, int(seconds / 2 / max(w.kv_bytes(w.ctx_lens[:1]) * per_byte, 1e-9))))
+        one = pool.map(_oracle_worker, [(name, [int(s) for s in order[:n1]], *scales[name])])[0]
+        rec["single_core"] = {"value": one[0] / (one[2] - one[1]) / 1e9, "unit": "GB/s", "cores": 1,
+                              "sample": f"{name}: {n1} of {w.S} sequences ({one[0] / 1e6:.0f} MB "
+                                        f"of K+V, {one[2] - one[1]:.1f} s)"}
+    return rec
+
+
+_ARM_PARTS = {"0xd0c": "Neoverse-N1", "0xd40": "Neoverse-V1", "0xd49": "Neoverse-N2",
+              "0xd4f": "Neoverse-V2", "0xd8e": "Neoverse-N3", "0xd84": "Neoverse-V3"}
+
+
+def _cpu_model():
+    """The host CPU's model from /proc/cpuinfo (x86: "model name"; Arm: the
+    implementer and part numbers, named for the Neoverse cores)."""
+    try:
+        with open("/proc/cpuinfo") as f:
+            info = f.read()
+    except OSError:
+        return None
+    m = re.search(r"^model name\s*:\s*(.+)$", info, re.M)
+    if m:
+        return m.group(1).strip()
+    impl = re.search(r"^CPU implementer\s*:\s*(\S+)", info, re.M)
+    part = re.search(r"^CPU part\s*:\s*(\S+)", info, re.M)
+    if part:
+        name = _ARM_PARTS.get(part.group(1).lower(), "Arm core")
+        return f"{name} (implementer {impl.group(1) if impl else '?'}, part {part.group(1)})"
+    return None
+
+
+# ----------------------------------------------------------- config records
+# The default run also measures the other decode configurations (one record
+# each, in the line's "configs"): the headline value stays on the 70B batches.
+def _bt(a, dtype):
+    """uint16 bit patterns -> a CUDA tensor of the 16-bit dtype."""
+    import torch
+    t = torch.from_numpy(np.ascontiguousarray(a).view(np.int16))
+    return t.view(torch.float16 if dtype == "fp16" else torch.bfloat16).cuda()
+
+
+def _decode_call(pool, q, tables, ctx, out, ws, ws_bytes, stream, scale, num_splits=0):
+    from paged_kv_cache_270_gb300 import _native as N
+    S, Hq, _ = q.shape
+    N.pa_decode(pool.handle, 0, out.data_ptr(), pool.in_code, q.data_ptr(), tables.data_ptr(),
+                tables.shape[-1], ctx.data_ptr(), S, Hq, scale, num_splits,
+                ws.data_ptr() if ws_bytes else 0, ws_bytes, stream)
+
+
+def _median_ms(fn, iters, warmup, stream):
+    """Median time of fn() in ms, each call between CUDA events on `stream`."""
+    import torch
+    for _ in range(warmup):
+        fn()
+    torch.cuda.synchronize()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(iters)]
+    for e0, e1 in ev:
+        e0.record(stream)
+        fn()
+        e1.record(stream)
+    torch.cuda.synchronize()
+    return statistics.median(e0.elapsed_time(e1) for e0, e1 in ev)
+
+
+def record_8b_bf16(pool_procs, peak):
+    """Config 1: Llama-3.1-8B-shaped bf16 decode, 64 sequences of U[512, 4096]."""
+    import torch
+    from paged_kv_cache_270_gb300 import _native as N
+    b = Batch("llama3_8b_bf16", pool_procs)
+    stream = torch.cuda.current_stream()
+    sh = int(stream.cuda_stream)
+    rec = {"workload": DESCRIPTION["llama3_8b_bf16"], "kv_bytes": b.kv_bytes,
+           "timing": "median of 50 decode calls, CUDA events"}
+    for key, ns in (("automatic", 0), ("balanced", N.PA_SPLITS_BALANCED)):
+        ws_bytes = b.pool.workspace_bytes(b.S, b.Hq, b.max_blocks, ns)
+        ws = torch.empty(max(ws_bytes, 16), dtype=torch.uint8, device="cuda")
+        ms = _median_ms(lambda: _decode_call(b.pool, b.d_q, b.d_tables, b.d_ctx, b.d_out, ws, ws_bytes,
+                                             sh, b.softmax_scale, ns), 50, 10, stream)
+        rec[key] = {"schedule": f"{b.splits} splits" if ns == 0 else "balanced",
+                    "decode_ms_median": round(ms, 5), "decode_kv_gbs": round(b.kv_bytes / ms / 1e6, 1),
+                    "frac_of_measured_peak": round(b.kv_bytes / ms / 1e6 / peak, 4),
+                    "tokens_per_s": round(b.S / ms * 1e3, 1)}
+    rec["device_error"] = b.pool.device_error()
+    b.pool.close()
+    return rec
+
+
+def record_8b_fp8_steps(pool_procs, peak):
+    """Config 2: the 8B shapes over an FP8 cache (per-tensor scales amax/448, 1%
+    of K x8), 32 decode steps of (write one token per sequence, decode), new
+    blocks taken from the pool's spare blocks when a sequence crosses a block
+    boundary.  Every step's inputs are resident before the timed region."""
+    import torch
+    from paged_kv_cache_270_gb300 import workloads as W
+    from paged_kv_cache_270_gb300.pool import KVPool
+    w = W.make("llama3_8b_fp8")
+    S, steps, D, Hkv = w.S, w.steps, w.head_dim, w.n_kv_heads
+    fin = w.final_ctx()
+    amax_chunks = [(w.name, s, lo, min(int(n), lo + 16384)) for s, n in enumerate(fin)
+                   for lo in range(0, int(n), 16384)]
+    ka = va = 0.0
+    for a_, b_ in pool_procs.imap_unordered(_gen_amax, amax_chunks, chunksize=4):
+        ka, va = max(ka, a_), max(va, b_)
+    k_scale = float(np.float32(ka) / np.float32(448.0))
+    v_scale = float(np.float32(va) / np.float32(448.0))
+    pool = KVPool(1, w.num_blocks, Hkv, D, "fp8_e4m3", k_scale, v_scale)
+    ctx0 = w.ctx_lens
+    fill = [(w.name, s, lo, min(int(n), lo + 16384)) for s, n in enumerate(ctx0)
+            for lo in range(0, int(n), 16384)]
+    for s, lo, hi, k, v in pool_procs.imap(_gen_bits, fill, chunksize=2):
+        pos = np.arange(lo, hi, dtype=np.int64)
+        slots = w.block_tables[s, pos // 16].astype(np.int64) * 16 + pos % 16
+        pool.reshape_and_cache(_bt(k, "bf16"), _bt(v, "bf16"), torch.from_numpy(slots).cuda())
+    tables = w.block_tables.copy()
+    spare = list(w.spare_blocks)
+    t_all, s_all, c_all, q_all = [], [], [], []
+    new_blocks = 0
+    for j in range(steps):
+        pos = ctx0 + j
+        for s in np.nonzero(pos % 16 == 0)[0]:
+            tables[s, pos[s] // 16] = spare.pop(0)
+            new_blocks += 1
+        s_all.append(tables[np.arange(S), pos // 16].astype(np.int64) * 16 + pos % 16)
+        t_all.append(tables.copy())
+        c_all.append(pos + 1)
+        q_all.append(w.q_bits(j))
+    # the new tokens of every step: [steps][S][Hkv][D]
+    kv = [w.kv_bits(s, int(ctx0[s]), int(ctx0[s]) + steps) for s in range(S)]
+    k_all = np.stack([k for k, _ in kv], axis=1)
+    v_all = np.stack([v for _, v in kv], axis=1)
+    d_t = torch.from_numpy(np.stack(t_all).astype(np.int32)).cuda()
+    d_s = torch.from_numpy(np.stack(s_all)).cuda()
+    d_c = torch.from_numpy(np.stack(c_all).astype(np.int32)).cuda()
+    d_k, d_v, d_q = _bt(k_all, "bf16"), _bt(v_all, "bf16"), _bt(np.stack(q_all), "bf16")
+    out = torch.empty((S, w.n_q_heads, D), dtype=torch.bfloat16, device="cuda")
+    stream = torch.cuda.current_stream()
+    sh = int(stream.cuda_stream)
+    from paged_kv_cache_270_gb300 import _native as N
+    kv_bytes = int(sum(int(c.sum()) for c in c_all)) * 2 * Hkv * D
+    rec = {"workload": DESCRIPTION["llama3_8b_fp8"] + ", 32 steps of (write one token per "
+                                                       "sequence, decode)",
+           "steps": steps, "new_blocks": new_blocks, "kv_bytes_all_steps": kv_bytes,
+           "timing": "median of 5 runs of the 32-step loop (CUDA events); decode calls timed "
+                     "one by one in one more run"}
+    for key, ns in (("automatic", 0), ("balanced", N.PA_SPLITS_BALANCED)):
+        ws_bytes = pool.workspace_bytes(S, w.n_q_heads, w.max_blocks, ns)
+        ws = torch.empty(max(ws_bytes, 16), dtype=torch.uint8, device="cuda")
+        dec_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                  for _ in range(steps)]
+
+        def run(evs=None):
+            for j in range(steps):
+                N.pa_reshape_and_cache(pool.handle, 0, d_k[j].data_ptr(), d_v[j].data_ptr(),
+                                       d_s[j].data_ptr(), S, sh)
+                if evs:
+                    evs[j][0].record(stream)
+                _decode_call(pool, d_q[j], d_t[j], d_c[j], out, ws, ws_bytes, sh, w.softmax_scale, ns)
+                if evs:
+                    evs[j][1].record(stream)
+
+        loop_ms = _median_ms(run, 5, 2, stream)
+        run(dec_ev)
+        torch.cuda.synchronize()
+        dec_ms = [e0.elapsed_time(e1) for e0, e1 in dec_ev]
+        rec[key] = {"schedule": (f"{pool.num_splits(S, w.n_q_heads, w.max_blocks)} splits" if ns == 0
+                                 else "balanced"),
+                    "step_ms": round(loop_ms / steps, 5),
+                    "step_kv_gbs": round(kv_bytes / loop_ms / 1e6, 1),
+                    "decode_ms_median": round(statistics.median(dec_ms), 5),
+                    "decode_kv_gbs": round(kv_bytes / sum(dec_ms) / 1e6, 1),
+                    "decode_frac_of_measured_peak": round(kv_bytes / sum(dec_ms) / 1e6 / peak, 4),
+                    "tokens_per_s": round(S * steps / loop_ms * 1e3, 1)}
+    rec["device_error"] = pool.device_error()
+    pool.close()
+    return rec
+
+
+def record_prefix_share(peak):
+    """Config 4: 64 requests sharing a 2048-token prefix (128 refcounted blocks)
+    plus a U[128, 1024] suffix each, one decode; and best-of-8 over a 2008-token
+    prompt: copy-on-write of the shared tail block, then 64 steps of (write one
+    token per branch, decode).  Logical bytes count every sequence's pages,
+    unique bytes each physical page once (the 8 MiB prefix can stay in L2)."""
+    import torch
+    from paged_kv_cache_270_gb300 import _native as N
+    from paged_kv_cache_270_gb300 import workloads as W
+    from paged_kv_cache_270_gb300.pool import KVPool
+    ps = W.PrefixShare()
+    stream = torch.cuda.current_stream()
+    sh = int(stream.cuda_stream)
+    R, P, Hkv, D = ps.n_requests, ps.prefix_tokens, ps.n_kv_heads, ps.head_dim
+    tok_bytes = 2 * Hkv * D * 2
+    pool = KVPool(1, 4096, Hkv, D, "bf16")
+    prefix = pool.alloc(P // 16)
+    kp, vp = ps.prefix_kv()
+    pos = np.arange(P, dtype=np.int64)
+    pool.reshape_and_cache(_bt(kp, "bf16"), _bt(vp, "bf16"),
+                           torch.from_numpy(prefix[pos // 16].astype(np.int64) * 16 + pos % 16).cuda())
+    suf = ps.suffix_lens()
+    ctx = (P + suf).astype(np.int32)
+    tables = np.zeros((R, -(-int(ctx.max()) // 16)), np.int32)
+    for r in range(R):
+        if r:
+            pool.incref(prefix)
+        own = pool.alloc(-(-int(suf[r]) // 16))
+        tables[r, :len(prefix)] = prefix
+        tables[r, len(prefix):len(prefix) + len(own)] = own
+        k, v = ps.suffix_kv(r, int(suf[r]))
+        p_ = np.arange(int(suf[r]), dtype=np.int64)
+        pool.reshape_and_cache(_bt(k, "bf16"), _bt(v, "bf16"),
+                               torch.from_numpy(own[p_ // 16].astype(np.int64) * 16 + p_ % 16).cuda())
+    used, _, shared = pool.stats()
+    q = _bt(ps.q_bits(R), "bf16")
+    d_t, d_c = torch.from_numpy(tables).cuda(), torch.from_numpy(ctx).cuda()
+    out = torch.empty((R, ps.n_q_heads, D), dtype=torch.bfloat16, device="cuda")
+    ws_bytes = pool.workspace_bytes(R, ps.n_q_heads, tables.shape[1], 0)
+    ws = torch.empty(max(ws_bytes, 16), dtype=torch.uint8, device="cuda")
+    scale = 1.0 / math.sqrt(D)
+    ms = _median_ms(lambda: _decode_call(pool, q, d_t, d_c, out, ws, ws_bytes, sh, scale), 50, 10,
+                    stream)
+    logical = int(ctx.sum()) * tok_bytes
+    unique = (P + int(suf.sum())) * tok_bytes
+    err = pool.device_error()
+    pool.close()
+    shared_rec = {"requests": R, "blocks_used": used, "blocks_shared": shared,
+                  "blocks_unshared_layout": int(np.sum(-(-ctx // 16))),
+                  "logical_kv_bytes": logical, "unique_kv_bytes": unique,
+                  "decode_ms_median": round(ms, 5),
+                  "logical_gbs": round(logical / ms / 1e6, 1),
+                  "unique_gbs": round(unique / ms / 1e6, 1),
+                  "unique_frac_of_measured_peak": round(unique / ms / 1e6 / peak, 4),
+                  "device_error": err}
+
+    # best of 8 over a 2008-token prompt (its tail block holds 8 tokens)
+    prompt, branches, new_tok = 2008, 8, 64
+    pool = KVPool(1, 512, Hkv, D, "bf16")
+    nb = -(-prompt // 16)
+    pblocks = pool.alloc(nb)
+    kp, vp = ps.prefix_kv(prompt)
+    pos = np.arange(prompt, dtype=np.int64)
+    pool.reshape_and_cache(_bt(kp, "bf16"), _bt(vp, "bf16"),
+                           torch.from_numpy(pblocks[pos // 16].astype(np.int64) * 16 + pos % 16).cuda())
+    width = -(-(prompt + new_tok) // 16)
+    tables = np.zeros((branches, width), np.int32)
+    for b in range(branches):
+        if b:
+            pool.incref(pblocks)
+        tables[b, :nb] = pblocks
+    pairs = []
+    for b in range(branches):
+        row = np.ascontiguousarray(tables[b])
+        got = pool.cow_prepare(row, prompt)
+        tables[b] = row
+        if got:
+            pairs.append(got)
+    d_pairs = torch.from_numpy(np.array(pairs, np.int32)).cuda()
+    copy_ms = _median_ms(lambda: pool.copy_blocks(d_pairs), 20, 3, stream)
+    t_all, s_all, c_all = [], [], []
+    c = np.full(branches, prompt, np.int32)
+    for j in range(new_tok):
+        for b in range(branches):
+            if c[b] % 16 == 0:
+                tables[b, c[b] // 16] = pool.alloc(1)[0]
+        s_all.append(tables[np.arange(branches), c // 16].astype(np.int64) * 16 + c % 16)
+        t_all.append(tables.copy())
+        c = c + 1
+        c_all.append(c.copy())
+    used, _, shared = pool.stats()
+    d_t = torch.from_numpy(np.stack(t_all)).cuda()
+    d_s = torch.from_numpy(np.stack(s_all)).cuda()
+    d_c = torch.from_numpy(np.stack(c_all)).cuda()
+    kq = [ps.suffix_kv(1000 + j, branches) for j in range(new_tok)]
+    d_k = _bt(np.stack([k for k, _ in kq]), "bf16")
+    d_v = _bt(np.stack([v for _, v in kq]), "bf16")
+    d_q = _bt(np.stack([ps.q_bits(branches, j) for j in range(new_tok)]), "bf16")
+    out = torch.empty((branches, ps.n_q_heads, D), dtype=torch.bfloat16, device="cuda")
+    ws_bytes = pool.workspace_bytes(branches, ps.n_q_heads, width, 0)
+    ws = torch.empty(max(ws_bytes, 16), dtype=torch.uint8, device="cuda")
+
+    def steps():
+        for j in range(new_tok):
+            N.pa_reshape_and_cache(pool.handle, 0, d_k[j].data_ptr(), d_v[j].data_ptr(),
+                                   d_s[j].data_ptr(), branches, sh)
+            _decode_call(pool, d_q[j], d_t[j], d_c[j], out, ws, ws_bytes, sh, scale)
+
+    loop_ms = _median_ms(steps, 5, 2, stream)
+    err = pool.device_error()
+    pool.close()
+    logical = int(sum(int(x.sum()) for x in c_all)) * tok_bytes
+    return {"workload": "Llama-3.1-8B-shaped bf16 (Hq 32 / Hkv 8 / d 128): 64 requests sharing "
+                        "a 2048-token prefix, each with a U[128,1024] suffix; best-of-8 over a "
+                        "2008-token prompt with copy-on-write of the shared tail block",
+            "shared_prefix_decode": shared_rec,
+            "best_of_8": {"prompt_tokens": prompt, "branches": branches, "cow_copies": len(pairs),
+                          "blocks_used": used, "blocks_unshared_layout": branches * width,
+                          "copy_blocks_ms": round(copy_ms, 5),
+                          "step_ms": round(loop_ms / new_tok, 5),
+                          "tokens_per_s": round(branches * new_tok / loop_ms * 1e3, 1),
+                          "logical_gbs": round(logical / loop_ms / 1e6, 1),
+                          "device_error": err},
+            "timing": "CUDA events; decode: median of 50 calls; best-of-8: median of 5 runs of "
+                      "the 64-step loop; the copy: median of 20 calls"}
+
+
+def config_records(pool_procs, peak):
+    recs = {}
+    for name, fn in (("llama3_8b_bf16", lambda: record_8b_bf16(pool_procs, peak)),
+                     ("llama3_8b_fp8_steps", lambda: record_8b_fp8_steps(pool_procs, peak)),
+                     ("prefix_share_bf16", lambda: record_prefix_share(peak))):
+        recs[name] = fn()
+        if recs[name].get("device_error") or \
+                any(v.get("device_error") for v in recs[name].values() if isinstance(v, dict)):
+            raise RuntimeError(f"device error in the {name} record")
+    return recs
 
 
 # ------------------------------------------------------------------- arms
@@ -467,9 +791,9 @@ def run_gb300(args, rank, world, local_rank):
     torch.cuda.set_device(local_rank)
     names = WORKLOADS[args.workload]
     ctx_mp = mp.get_context("spawn")
-    procs = max(1, min(os.cpu_count() or 1, 16))
+    procs = max(1, os.cpu_count() or 1)
     with ctx_mp.Pool(procs) as pool_procs:
-        batches = [Batch(n, pool_procs) for n in names]
+        batches = [Batch(n, pool_procs, args.decode_splits) for n in names]
         staging = Staging(batches)
         scales = {b.w.name: (b.w.k_scale, b.w.v_scale) for b in batches}
         stream = torch.cuda.current_stream()
@@ -535,6 +859,10 @@ def run_gb300(args, rank, world, local_rank):
             if err:
                 raise RuntimeError(f"device error {err} in {b.w.name}")
 
+        configs = None
+        if args.workload == "llama3_70b_fp8" and world == 1 and not args.no_configs:
+            configs = config_records(pool_procs, _measured_peak()[0])
+
         cpu = None
         if rank == 0 and world == 1 and not args.no_cpu:
             cpu = cpu_baseline(names, scales, args.cpu_seconds, procs, pool_procs)
@@ -555,7 +883,8 @@ def run_gb300(args, rank, world, local_rank):
     for b, d in zip(batches, dec_ms):
         per_batch[b.w.name] = {
             "sequences": b.S, "tokens_per_seq": int(b.w.ctx_lens.max()), "kv_bytes": b.kv_bytes,
-            "splits": b.splits, "decode_ms_median": statistics.median(d),
+            "splits": b.splits, "schedule": "balanced" if b.splits < 0 else "fixed splits",
+            "decode_ms_median": statistics.median(d),
             "decode_ms_p10_p90": _p10_p90(d),
             "decode_kv_gbs": b.kv_bytes / (statistics.median(d) / 1e3) / 1e9}
     launches = K * sum(b.launches for b in batches)
@@ -575,7 +904,7 @@ def run_gb300(args, rank, world, local_rank):
         "frac_of_spec_8tbs": round(value / SPEC_HBM_GBS, 4),
         "frac_of_measured_peak": round(value / peak, 4),
         "batches": per_batch,
-        "roofline": {"kernel": "pa_decode (decode kernel + split merge when splits > 1)",
+        "roofline": {"kernel": "pa_decode (decode kernel + its merge kernel)",
                      "bound": "hbm", "achieved": round(achieved, 1), "peak": peak,
                      "peak_kind": f"{peak_kind} (hbm_gbs)", "unit": "GB/s",
                      "frac": round(achieved / peak, 4), "traffic": traffic,
@@ -583,6 +912,7 @@ def run_gb300(args, rank, world, local_rank):
         "cpu_baseline": cpu,
         "e2e": e2e,
         "gpu_launches": launches,
+        "configs": configs,
         "clocks": sampler.summary(),
     }
     print(json.dumps(line), flush=True)
@@ -607,7 +937,7 @@ def run_prefill(args, rank, world, local_rank):
     torch.cuda.set_device(local_rank)
     name = args.workload
     w = W.make(name)
-    procs = max(1, min(os.cpu_count() or 1, 16))
+    procs = max(1, os.cpu_count() or 1)
     with mp.get_context("spawn").Pool(procs) as pp:
         chunks = [(name, s, lo, min(int(w.ctx_lens[s]), lo + 16384))
                   for s in range(w.S) for lo in range(0, int(w.ctx_lens[s]), 16384)]
@@ -961,7 +1291,7 @@ def run_reference(args, rank, world):
         return
     names = WORKLOADS[args.workload]
     from paged_kv_cache_270_gb300 import workloads as W
-    procs = max(1, min(os.cpu_count() or 1, 16))
+    procs = max(1, os.cpu_count() or 1)
     ctx_mp = mp.get_context("spawn")
     scales = {}
     with ctx_mp.Pool(procs) as pool:
@@ -979,12 +1309,12 @@ def run_reference(args, rank, world):
                 scales[name] = (1.0, 1.0)
         per_step = max(2.0, min(20.0, 150.0 / max(1, args.steps + args.warmup)))
         for _ in range(args.warmup):
-            cpu_baseline(names, scales, per_step / 4, procs, pool)
+            cpu_baseline(names, scales, per_step / 4, procs, pool, single_core=False)
         vals, t_total = [], 0.0
         last = None
         for _ in range(args.steps):
             t0 = time.time()
-            last = cpu_baseline(names, scales, per_step, procs, pool)
+            last = cpu_baseline(names, scales, per_step, procs, pool, single_core=False)
             t_total += time.time() - t0
             vals.append(last["value"])
     value = statistics.fmean(vals)
@@ -996,7 +1326,8 @@ def run_reference(args, rank, world):
             "config": {"workload": DESCRIPTION[args.workload],
                        "sample_per_step": last["sample"] if last else None},
             "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": procs,
-                             "kind": "oracle", "sample": last["sample"] if last else None},
+                             "kind": "oracle", "sample": last["sample"] if last else None,
+                             "cpu_model": _cpu_model()},
             "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": 0},
             "gpu_launches": 0}
@@ -1013,6 +1344,11 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--decode-splits", type=int, default=0,
+                    help="decode with this fixed split count (or -1: the balanced schedule) "
+                         "instead of the automatic split count")
+    ap.add_argument("--no-configs", action="store_true",
+                    help="skip the records of the other decode configurations (default workload)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
