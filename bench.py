@@ -90,12 +90,12 @@ DESCRIPTION = {
 # measured.
 NCU_TRAFFIC = {
     # hash of the decode source with comments and blank lines removed (see _source_sha)
-    "source_sha256": "b574fe2c6b5e8fa870cb1f83251857df4c3f72565e291885e0266998434460aa",
+    "source_sha256": "c5bde61ed985227340053045cdb3f1586febb3c101f53bf868b4d4a74e1d137e",
     # dram__bytes_read.sum + dram__bytes_write.sum of one decode launch
-    "bytes_per_launch": {"llama3_70b_fp8_a": 1073977856 + 3256576,
-                         "llama3_70b_fp8_b": 2152047360 + 4622336,
-                         "llama3_70b_fp8_block_a": 1076084224 + 2768128,
-                         "llama3_70b_fp8_block_b": 2156265216 + 5187328},
+    "bytes_per_launch": {"llama3_70b_fp8_a": 1074033152 + 3508480,
+                         "llama3_70b_fp8_b": 2152017152 + 4891136,
+                         "llama3_70b_fp8_block_a": 1076088064 + 2924800,
+                         "llama3_70b_fp8_block_b": 2156267264 + 5160704},
 }
 
 # --------------------------------------------------------------------- workers

@@ -288,7 +288,7 @@ PA_API int pa_reshape_and_cache(pa_pool* pool, int layer, const void* k, const v
 
 /* num_splits value that asks pa_decode for the balanced schedule (batches of
  * at most 4096 sequences, else PA_ERR_UNSUPPORTED): one CTA per resident slot
- * of the GPU, at most four per SM; the pages of every (sequence, kv head)
+ * of the GPU, four per SM (the kernel's shared memory keeps a fifth off); the pages of every (sequence, kv head)
  * pair, taken in (sequence, kv head, page) order, are cut into equal
  * contiguous ranges, one per CTA, from the context lengths on the device, so
  * every CTA streams the same number of pages whatever the mix of lengths, and
@@ -300,7 +300,13 @@ PA_API int pa_reshape_and_cache(pa_pool* pool, int layer, const void* k, const v
  * shape when num_splits = 0 (auto): enough (sequence, KV head, split) work
  * units to fill the GPU, each split still covering several pages (every
  * sequence is taken as max_blocks_per_seq pages long: the lengths live on the
- * device).  Uses the current CUDA device. */
+ * device).  When that count s is at least 2 and its CTAs take more than one
+ * wave of the GPU, the automatic layout is guided instead: min(2 s, 8) splits
+ * whose shares of the table fall geometrically (ratio 0.55), handed out split
+ * by split (every sequence's first split before any second one), so the CTAs
+ * that run last, as the grid drains, are short; this returns that count.  An
+ * explicit num_splits always cuts the table into equal splits.  Uses the
+ * current CUDA device. */
 PA_API int pa_decode_num_splits(const pa_pool* pool, int S, int n_q_heads, int max_blocks_per_seq,
                          int* num_splits);
 
@@ -329,10 +335,10 @@ PA_API int pa_decode_workspace_bytes(const pa_pool* pool, int S, int n_q_heads, 
  *                     value (0 weighs every visible token the same, a negative
  *                     scale takes the softmax of the negated scores), else
  *                     PA_ERR_INVALID
- *   num_splits        0 = automatic (see pa_decode_num_splits); > 0: the
- *                     number of splits along the pages (a second kernel merges
- *                     the partial results); PA_SPLITS_BALANCED: the balanced
- *                     schedule
+ *   num_splits        0 = automatic (see pa_decode_num_splits: equal splits,
+ *                     or the guided layout); > 0: that many equal splits along
+ *                     the pages (a second kernel merges the partial results);
+ *                     PA_SPLITS_BALANCED: the balanced schedule
  *   workspace         device scratch of at least pa_decode_workspace_bytes
  *                     (may be NULL when that size is 0)
  * Query head g reads KV head g / (n_q_heads / n_kv_heads) (grouped-query

@@ -112,6 +112,19 @@ struct Cfg {
 // The balanced schedule gives every CTA at least this many pages.
 constexpr int kMinPagesPerCta = 8;
 
+// Fixed splits: how a sequence's pages are cut.  Uniform: split k covers pages
+// [k pps, (k + 1) pps).  Guided (the automatic layout of launches of several
+// waves): split k covers [b[k], b[k + 1]), sizes falling geometrically, and
+// the split index is the slowest grid dimension, so the block scheduler hands
+// out every sequence's first (largest) split first and the small last splits
+// last: the CTAs still running as the grid drains are short ones.
+constexpr int kGuidedSplits = 8;
+struct SplitLayout {
+  int splits, pps;
+  int guided;
+  int b[kGuidedSplits + 1];
+};
+
 struct DecodeArgs {
   const uint16_t* q;     // [S][Hq][D]
   void* out;             // [S][Hq][D]
@@ -124,7 +137,8 @@ struct DecodeArgs {
   const int32_t* ctx;
   int max_blocks;
   int S, Hq, Hkv, G, num_blocks;
-  int splits, pages_per_split;  // fixed splits
+  int splits, pages_per_split;  // fixed splits (uniform layout)
+  SplitLayout sl;               // fixed splits: the layout (uniform or guided)
   int ctas;                     // balanced schedule: CTAs of the launch
   float qk_scale_log2;  // softmax_scale * log2(e) (* k_scale for FP8)
   float v_scale;        // 1 for 16-bit and block-scaled pools
@@ -134,6 +148,25 @@ struct DecodeArgs {
 };
 
 __device__ __forceinline__ int clamp_ctx(int c, int max_blocks) { return c < 0 ? 0 : min(c, max_blocks * 16); }
+
+// Pages [pb, pe) of split k (the guided bounds are read with constant indices,
+// so the layout stays in the parameter space).
+__device__ __forceinline__ void split_pages(const SplitLayout& L, int k, int& pb, int& pe) {
+  if (L.guided) {
+    pb = 0;
+    pe = 0;
+#pragma unroll
+    for (int i = 0; i < kGuidedSplits; ++i)
+      if (i == k) {
+        pb = L.b[i];
+        pe = L.b[i + 1];
+      }
+  } else {
+    pb = k * L.pps;
+    pe = pb + L.pps;
+  }
+}
+__device__ __forceinline__ int first_split_pages(const SplitLayout& L) { return L.guided ? L.b[1] : L.pps; }
 
 
 // Exclusive prefix sum over the CTA's threads (every thread must call it);
@@ -429,7 +462,10 @@ __global__ void __launch_bounds__(kThreads, MINB) decode_kernel(const DecodeArgs
   float2* stage_scale =
       reinterpret_cast<float2*>(smem + C::kDataBytes + 2 * C::kStages * 8 + C::kQBytes);
 
-  const int split = blockIdx.x, h = blockIdx.y, seq = blockIdx.z;
+  // grid (split, kv head, sequence), or (kv head, sequence, split) for the guided layout
+  const int split = a.sl.guided ? blockIdx.z : blockIdx.x;
+  const int h = a.sl.guided ? blockIdx.x : blockIdx.y;
+  const int seq = a.sl.guided ? blockIdx.y : blockIdx.z;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   grid_dependency_wait();  // the kernel before may still write q, tables, pages
 
@@ -439,14 +475,15 @@ __global__ void __launch_bounds__(kThreads, MINB) decode_kernel(const DecodeArgs
     ctx = ctx < 0 ? 0 : a.max_blocks * 16;
   }
   const int npages = (ctx + 15) >> 4;
-  const int p_begin = split * a.pages_per_split;
-  const int n_local = max(0, min(npages, p_begin + a.pages_per_split) - p_begin);
+  int p_begin, p_end;
+  split_pages(a.sl, split, p_begin, p_end);
+  const int n_local = max(0, min(npages, p_end) - p_begin);
   // A split past the end of this sequence's pages has nothing to do: no partial
   // is written for it and the merge never reads one.  Split 0 always runs (it
   // writes the zero row of an empty context).
   if (split > 0 && n_local == 0) return;
   // Sequences that fit in one split are finished here, without a merge.
-  const bool direct = a.splits == 1 || npages <= a.pages_per_split;
+  const bool direct = a.splits == 1 || npages <= first_split_pages(a.sl);
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < C::kStages; ++s) {
@@ -702,6 +739,14 @@ struct BalCfg {
   // the staged unit's descriptor, then each consumer warp's copy of its current one
   static constexpr int kOffScale = kOffDesc + (1 + kConsumerWarps) * 32;  // block-scaled: [stages] scales
   static constexpr int kSmem = kOffScale + C::kScaleBytes + C::kAlign;
+  // The launch asks for at least 48 KiB, so at most four CTAs share an SM
+  // (five would need 5 x (48 + 1) KiB, more than the SM's 228 KiB).  The grid
+  // is four CTAs per SM with equal page counts; a build that fits five would
+  // let the block scheduler put five on some SMs and three on others whenever
+  // other work holds part of the GPU as the grid starts (a dependent launch
+  // starts before the kernel ahead of it has finished), and the CTAs of a
+  // five-CTA SM stream 4/5 as fast, which sets the time of the whole grid.
+  static constexpr int kLaunchSmem = kSmem > 48 * 1024 ? kSmem : 48 * 1024;
   static_assert(kOffFrag % 16 == 0 && kOffQStage % 16 == 0, "bulk-copy destinations are 16-byte aligned");
 };
 
@@ -1130,50 +1175,74 @@ __global__ void __launch_bounds__(kThreads, MINB) decode_bal_kernel(const Decode
 // Merge of the per-split partial states, M = max m_i, L = sum l_i 2^(m_i - M),
 // O = sum o_i 2^(m_i - M) / L, over the splits the sequence used (rows of
 // sequences that fit one split were written by the decode kernel itself).
-__device__ __forceinline__ int used_splits(const int32_t* ctx, int seq, int max_blocks, int pps) {
+__device__ __forceinline__ int used_splits(const int32_t* ctx, int seq, int max_blocks, const SplitLayout& L) {
   int c = ctx[seq];
   c = c < 0 ? 0 : min(c, max_blocks * 16);
-  return ((c + 15) / 16 + pps - 1) / pps;
+  const int np = (c + 15) / 16;
+  if (!L.guided) return (np + L.pps - 1) / L.pps;
+  int n = 0;
+#pragma unroll
+  for (int i = 0; i < kGuidedSplits; ++i) n += (i < L.splits && L.b[i] < np) ? 1 : 0;
+  return n;
 }
 
-// Few splits: one warp per (sequence, query head), splits walked in a loop.
+// Few splits (at most 8): one warp per (sequence, query head).  Lane s reads
+// split s's (m, l), so M and L are one load and a warp reduction away; the
+// lanes then read every split's slice of O (D / 32 values each) at once, and
+// add them up in split order.
 template <int D, int OUT>
 __global__ void __launch_bounds__(128) reduce_rows_kernel(const float* __restrict__ ws_o,
                                                           const float* __restrict__ ws_ml,
                                                           const int32_t* __restrict__ ctx,
                                                           void* out, int rows, int Hq, int splits,
-                                                          int max_blocks, int pps, float v_scale) {
+                                                          int max_blocks, const SplitLayout sl, float v_scale) {
   grid_dependency_wait();  // the partials come from the decode kernel just before
   const int row = blockIdx.x * 4 + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
   if (row >= rows) return;
-  const int n = min(splits, used_splits(ctx, row / Hq, max_blocks, pps));
+  const int n = min(splits, used_splits(ctx, row / Hq, max_blocks, sl));
   if (n <= 1) return;
   constexpr int PER = D / 32;
-  const float* ml = ws_ml + (size_t)row * splits * 2;
-  float M = -INFINITY;
-  for (int s = 0; s < n; ++s) M = fmaxf(M, ml[2 * s]);
-  float L = 0.f, O[PER];
+  float ms = -INFINITY, ls = 0.f;
+  if (lane < n) {
+    const float2 v = reinterpret_cast<const float2*>(ws_ml)[(size_t)row * splits + lane];
+    ms = v.x;
+    ls = v.y;
+  }
+  float M = ms;
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(kFull, M, off));
+  const float w = (ms == -INFINITY) ? 0.f : fast_exp2(ms - M);  // 0 for lanes >= n
+  float L = w * ls;
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) L += __shfl_xor_sync(kFull, L, off);
+  float O[PER];
 #pragma unroll
   for (int j = 0; j < PER; ++j) O[j] = 0.f;
-  if (M != -INFINITY) {
-    const float* po = ws_o + (size_t)row * splits * D + lane * PER;
-#pragma unroll 4
-    for (int s = 0; s < n; ++s) {
-      const float ms = ml[2 * s];
-      const float f = (ms == -INFINITY) ? 0.f : fast_exp2(ms - M);
-      L += f * ml[2 * s + 1];
+  const float* po = ws_o + (size_t)row * splits * D + lane * PER;
+  float v[8][PER];
+#pragma unroll
+  for (int s = 0; s < 8; ++s) {
+    if (s < n) {
       if constexpr (PER == 4) {
-        const float4 v = *reinterpret_cast<const float4*>(po + (size_t)s * D);
-        O[0] += f * v.x;
-        O[1] += f * v.y;
-        O[2] += f * v.z;
-        O[3] += f * v.w;
+        const float4 x = *reinterpret_cast<const float4*>(po + (size_t)s * D);
+        v[s][0] = x.x;
+        v[s][1] = x.y;
+        v[s][2] = x.z;
+        v[s][3] = x.w;
       } else {
-        const float2 v = *reinterpret_cast<const float2*>(po + (size_t)s * D);
-        O[0] += f * v.x;
-        O[1] += f * v.y;
+        const float2 x = *reinterpret_cast<const float2*>(po + (size_t)s * D);
+        v[s][0] = x.x;
+        v[s][1] = x.y;
       }
+    }
+  }
+#pragma unroll
+  for (int s = 0; s < 8; ++s) {
+    const float f = __shfl_sync(kFull, w, s);
+    if (s < n) {
+#pragma unroll
+      for (int j = 0; j < PER; ++j) O[j] += f * v[s][j];
     }
   }
   const float inv = L > 0.f ? v_scale / L : 0.f;
@@ -1189,12 +1258,12 @@ __global__ void __launch_bounds__(128) reduce_wide_kernel(const float* __restric
                                                           const float* __restrict__ ws_ml,
                                                           const int32_t* __restrict__ ctx,
                                                           void* out, int Hq, int splits,
-                                                          int max_blocks, int pps, float v_scale) {
+                                                          int max_blocks, const SplitLayout sl, float v_scale) {
   grid_dependency_wait();
   __shared__ float wsh[128];
   __shared__ float red[4];
   const int row = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int n = min(splits, used_splits(ctx, row / Hq, max_blocks, pps));
+  const int n = min(splits, used_splits(ctx, row / Hq, max_blocks, sl));
   if (n <= 1) return;
   const float* ml = ws_ml + (size_t)row * splits * 2;
   float m = -INFINITY;
@@ -1341,7 +1410,7 @@ struct Launcher {
   // the balanced-schedule build
   static KernelInfo& info_bal() {
     static KernelInfo ki = {reinterpret_cast<const void*>(&decode_bal_kernel<KV, D, OUT, kPsplit, kMinB>),
-                            BalCfg<KV, D>::kSmem,
+                            BalCfg<KV, D>::kLaunchSmem,
                             {}};
     return ki;
   }
@@ -1363,7 +1432,7 @@ struct Launcher {
     cfg.numAttrs = 1;
     if (bal) {
       cfg.gridDim = dim3(a.ctas);
-      cfg.dynamicSmemBytes = BalCfg<KV, D>::kSmem;
+      cfg.dynamicSmemBytes = BalCfg<KV, D>::kLaunchSmem;
       cudaError_t e = cudaLaunchKernelEx(&cfg, decode_bal_kernel<KV, D, OUT, kPsplit, kMinB>, a, *tk, *tv);
       if (e != cudaSuccess) return e;
       cfg.gridDim = dim3(a.ctas, a.G);
@@ -1372,7 +1441,7 @@ struct Launcher {
       return cudaLaunchKernelEx(&cfg, merge_jobs_kernel<D, OUT>, (const float*)a.ws_o, (const float*)a.ws_ml,
                                 (const int4*)a.jobs, a.out, a.Hq, a.G, a.v_scale);
     }
-    cfg.gridDim = dim3(a.splits, a.Hkv, S);
+    cfg.gridDim = a.sl.guided ? dim3(a.Hkv, S, a.splits) : dim3(a.splits, a.Hkv, S);
     cudaError_t e = low ? cudaLaunchKernelEx(&cfg, decode_kernel<KV, D, OUT, kPsplit, kMinBLow>, a, *tk, *tv)
                         : cudaLaunchKernelEx(&cfg, decode_kernel<KV, D, OUT, kPsplit, kMinB>, a, *tk, *tv);
     if (e != cudaSuccess || a.splits == 1) return e;
@@ -1382,11 +1451,11 @@ struct Launcher {
     if (a.splits <= 8) {
       cfg.gridDim = dim3((rows + 3) / 4);
       e = cudaLaunchKernelEx(&cfg, reduce_rows_kernel<D, OUT>, (const float*)a.ws_o, (const float*)a.ws_ml,
-                             a.ctx, a.out, rows, a.Hq, a.splits, a.max_blocks, a.pages_per_split, a.v_scale);
+                             a.ctx, a.out, rows, a.Hq, a.splits, a.max_blocks, a.sl, a.v_scale);
     } else {
       cfg.gridDim = dim3(rows);
       e = cudaLaunchKernelEx(&cfg, reduce_wide_kernel<D, OUT>, (const float*)a.ws_o, (const float*)a.ws_ml,
-                             a.ctx, a.out, a.Hq, a.splits, a.max_blocks, a.pages_per_split, a.v_scale);
+                             a.ctx, a.out, a.Hq, a.splits, a.max_blocks, a.sl, a.v_scale);
     }
     return e;
   }
@@ -1584,16 +1653,24 @@ int check_shape(const pa_pool* pool, int S, int n_q_heads, int max_blocks) {
 // The contexts live on the device, so every unit is taken as full: a batch with
 // a few sequences much longer than the rest is better served by an explicit
 // split count.
-int auto_splits(const pa_pool* pool, int S, int max_blocks, int* out) {
+// SMs of the current device and resident CTAs per SM of the decode kernel's
+// default build for this pool (the query dtype's output).
+int decode_residency(const pa_pool* pool, int* sms, int* occ) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return fail(PA_ERR_CUDA, "cudaGetDevice: %s", cudaGetErrorString(e));
-  int sms = 0;
-  e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  e = cudaDeviceGetAttribute(sms, cudaDevAttrMultiProcessorCount, dev);
   if (e != cudaSuccess) return fail(PA_ERR_CUDA, "SM count: %s", cudaGetErrorString(e));
   Dispatch d = pick(pool->desc.kv_dtype, pool->desc.head_dim, in_dtype_of(pool->desc.kv_dtype));
-  int occ = configure(*d.info, dev);
-  if (occ <= 0) return fail(PA_ERR_CUDA, "decode kernel occupancy query failed");
+  *occ = configure(*d.info, dev);
+  if (*occ <= 0) return fail(PA_ERR_CUDA, "decode kernel occupancy query failed");
+  return PA_OK;
+}
+
+int auto_splits(const pa_pool* pool, int S, int max_blocks, int* out) {
+  int sms = 0, occ = 0;
+  int st = decode_residency(pool, &sms, &occ);
+  if (st) return st;
   const double slots = (double)sms * occ;
   const double k_sat = std::min(4, occ);
   const double units = (double)std::max(S, 1) * pool->desc.n_kv_heads;
@@ -1616,6 +1693,27 @@ int auto_splits(const pa_pool* pool, int S, int max_blocks, int* out) {
   }
   *out = best;
   return PA_OK;
+}
+
+// Guided layout over `max_blocks` table columns in `want` <= kGuidedSplits
+// splits: split k's share of the columns is proportional to kGuidedRatio^k
+// (fewer splits when the table is too narrow for all of them to hold a
+// column).  Returns the split count n; b[0] = 0 < b[1] < ... < b[n] = max_blocks.
+// The ratio: on the 8B-shaped ragged FP8 batch (64 sequences of 512 to 4096
+// tokens, two and a half waves of CTAs) 0.55 measured best among 0.5 .. 0.65.
+constexpr double kGuidedRatio = 0.55;
+int guided_bounds(int max_blocks, int want, int* b) {
+  double w[kGuidedSplits], sum = 0.0;
+  for (int k = 0; k < want; ++k) sum += (w[k] = std::pow(kGuidedRatio, k));
+  int n = 0;
+  b[0] = 0;
+  double cum = 0.0;
+  for (int k = 0; k < want; ++k) {
+    cum += w[k];
+    const int e = k == want - 1 ? max_blocks : (int)std::lround(cum / sum * max_blocks);
+    if (e > b[n]) b[++n] = e;
+  }
+  return n;
 }
 
 int resolve_splits(const pa_pool* pool, int S, int max_blocks, int num_splits, int* splits,
@@ -1643,6 +1741,8 @@ constexpr int kBalancedMaxSeqs = 4096;
 struct Plan {
   bool bal = false;
   int splits = 1, pps = 1;  // fixed splits
+  bool guided = false;      // fixed splits in the guided layout, bounds b
+  int b[kGuidedSplits + 1] = {};
   int ctas = 0;             // balanced schedule
   size_t ws_bytes = 0;
 };
@@ -1714,6 +1814,27 @@ int make_plan(const pa_pool* pool, int S, int n_q_heads, int max_blocks, int num
       if (row_bytes * p->splits <= cap) break;
     }
   }
+  // The automatic count s, on a launch of more than one wave: the guided
+  // layout (min(2 s, kGuidedSplits) splits whose sizes fall by kGuidedRatio,
+  // so the CTAs handed out last, as the grid drains, are short), when its
+  // partials fit.  On batches of equal lengths it streams about as fast as s
+  // uniform splits (the waves then end together anyway); on ragged ones the
+  // drain is what it shortens.
+  if (num_splits == 0 && p->splits >= 2) {
+    int sms = 0, occ = 0;
+    st = decode_residency(pool, &sms, &occ);
+    if (st) return st;
+    if ((long long)S * pool->desc.n_kv_heads * p->splits > (long long)occ * sms) {
+      int b[kGuidedSplits + 1];
+      const int n = guided_bounds(max_blocks, std::min(2 * p->splits, kGuidedSplits), b);
+      if (n >= 2 && (cap == 0 || row_bytes * n <= cap)) {
+        p->guided = true;
+        p->splits = n;
+        p->pps = b[1];
+        for (int i = 0; i <= kGuidedSplits; ++i) p->b[i] = i <= n ? b[i] : max_blocks;
+      }
+    }
+  }
   p->ws_bytes = fixed_ws_bytes(S, n_q_heads, p->splits, D);
   return PA_OK;
 }
@@ -1770,6 +1891,10 @@ int decode_with_plan(pa_pool* pool, int layer, void* out, int out_dtype, const v
   a.num_blocks = d.num_blocks;
   a.splits = plan.splits;
   a.pages_per_split = plan.pps;
+  a.sl.splits = plan.splits;
+  a.sl.pps = plan.pps;
+  a.sl.guided = plan.guided ? 1 : 0;
+  for (int i = 0; i <= kGuidedSplits; ++i) a.sl.b[i] = plan.b[i];
   a.ctas = plan.ctas;
   const float log2e = 1.4426950408889634f;
   a.qk_scale_log2 = softmax_scale * log2e * (d.kv_dtype == PA_FP8_E4M3 ? d.k_scale : 1.f);

@@ -101,11 +101,12 @@ def test_no_alloc_matches_decode_on_two_calls_in_a_row():
 
 
 def test_no_alloc_lowers_an_automatic_split_count_to_fit():
-    """The automatic split count here is two (4100 single-head sequences
-    against 760 resident CTAs, every one taken as 2048 pages long); its partials (2 x 4100 x 8 heads x (128 + 2)
-    floats, 34 MB) do not fit the 8 MiB array, so the entry point takes the
-    largest count that fits (one split, no partials), and matches pa_decode at
-    that count."""
+    """The automatic split count here is two uniform splits (4100 single-head
+    sequences against 760 resident CTAs, every one taken as 2048 pages long),
+    which pa_decode runs as four guided splits; neither's partials (2 x 4100 x
+    8 heads x (128 + 2) floats, 34 MB, for two) fit the 8 MiB array, so the
+    entry point takes the largest uniform count that fits (one split, no
+    partials), and matches pa_decode at that count."""
     rng = np.random.default_rng(31)
     S, Hkv, G, d, max_blocks = 4100, 1, 8, 128, 2048
     ctx = rng.integers(1, 60, S).astype(np.int32)
