@@ -218,12 +218,30 @@ __device__ __forceinline__ float max16(const float* v) {
   return fmaxf(fmax3f(a, b, c), fmax3f(d, e, v[15]));
 }
 
-// Bounded wait that also gives up as soon as another role has aborted.
+// As mbar_try_wait, but a thread whose phase is not complete may be suspended
+// for up to `hint_ns` (woken as soon as the phase completes) instead of the
+// hardware's own short limit.
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t* bar, uint32_t parity, uint32_t hint_ns) {
+  uint32_t done;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(done)
+      : "r"(smem_addr(bar)), "r"(parity), "r"(hint_ns)
+      : "memory");
+  return done != 0;
+}
+
+// Bounded wait that also gives up as soon as another role has aborted.  Its
+// retries sleep (up to 20 us each, woken when the phase completes), so the
+// waiting warps leave the issue slots of their scheduler to the warps that
+// work, the single MMA-issuing thread above all.
 __device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
                                               unsigned int* err) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = global_ns();
-  while (!mbar_try_wait(bar, parity)) {
+  while (!mbar_try_wait_sleep(bar, parity, 20000u)) {
     if (*abort_flag) return false;
     if (global_ns() - t0 > pipe_wait_limit()) {
       *abort_flag = 1;
@@ -415,23 +433,29 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const TcArgs a,
   } else if (warp == 1) {
     // ---------------------------------------------------------- MMA issue
     if (lane == 0 && wait_or_abort(&ctl->q_ready, 0, abort_flag, a.err)) {
+      // Descriptors are computed once: moving an operand by X bytes adds X / 16
+      // to the descriptor's start-address field (shared addresses stay below
+      // 256 KiB, so the field never carries), which keeps the issuing thread's
+      // work between two MMAs to a few instructions.
+      const uint64_t kdesc0 = kmajor(smem_addr(sm + L::kKRing));
+      const uint64_t vdesc0 = mnmajor(smem_addr(sm + (F8 ? L::kVT : L::kVRing)));
       // S(j) = Q K(j)^T into S buffer j % 2
       auto issue_qk = [&](int j) {
         const int sb = j & 1;
         if constexpr (!F8)
           if (j == nblk - 1) mbar_arrive(&ctl->tail_ready);  // its pages have landed
-        const uint32_t kb = smem_addr(sm + L::kKRing + (j % R) * L::kSlot);
+        const uint64_t kd = kdesc0 + (uint64_t)((j % R) * (L::kSlot >> 4));
         if constexpr (F8) {
 #pragma unroll
           for (int t = 0; t < 2; ++t)
 #pragma unroll
             for (int k = 0; k < 4; ++k)
-              mma_f8_ts(tmem + sb * 128, tmem + (t ? kQLoCol : kQHiCol) + 8 * k, kmajor(kb + 32 * k), kIdescQK,
+              mma_f8_ts(tmem + sb * 128, tmem + (t ? kQLoCol : kQHiCol) + 8 * k, kd + 2 * k, kIdescQK,
                         (uint32_t)(t | k));
         } else {  // 16 dims per MMA: dim half k / 4, 32 bytes into its rows
 #pragma unroll
           for (int k = 0; k < 8; ++k)
-            mma_f16_ts(tmem + sb * 128, tmem + kQHiCol + 8 * k, kmajor(kb + (k >> 2) * 16384 + (k & 3) * 32),
+            mma_f16_ts(tmem + sb * 128, tmem + kQHiCol + 8 * k, kd + (k >> 2) * (16384 >> 4) + (k & 3) * 2,
                        kIdescQK | (BF ? kBf16Types : 0u), (uint32_t)k);
         }
         mma_commit(&ctl->s_full[sb]);
@@ -459,13 +483,13 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const TcArgs a,
         }
         tc_fence_after();
         // B: the binary16 V block (FP8 pools) or the V ring slot itself (16-bit pools)
-        const uint32_t vt = F8 ? smem_addr(sm + L::kVT + vb * 32768) : smem_addr(sm + L::kVRing + (i % R) * L::kSlot);
+        const uint64_t vd = vdesc0 + (uint64_t)(F8 ? vb * (32768 >> 4) : (i % R) * (L::kSlot >> 4));
 #pragma unroll
         for (int part = 0; part < (PSPLIT ? 2 : 1); ++part)
 #pragma unroll
           for (int k = 0; k < 8; ++k)
             mma_f16_ts(tmem + kOCol, tmem + vb * 128 + 32 * (k >> 1) + 16 * part + 8 * (k & 1),
-                       mnmajor(vt + k * 2048), kIdescPV | (BF ? kBf16Types : 0u), (uint32_t)(i | k | part));
+                       vd + k * (2048 >> 4), kIdescPV | (BF ? kBf16Types : 0u), (uint32_t)(i | k | part));
         mma_commit(&ctl->o_done);
         if constexpr (F8) mma_commit(&ctl->vt_empty[vb]);
         else mma_commit(&ctl->kv_empty[i % R]);  // K and V of block i are read
