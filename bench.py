@@ -612,7 +612,9 @@ def record_8b_fp8_steps(pool_procs, peak):
                                                        "sequence, decode)",
            "steps": steps, "new_blocks": new_blocks, "kv_bytes_all_steps": kv_bytes,
            "timing": "median of 5 runs of the 32-step loop (CUDA events); decode calls timed "
-                     "one by one in one more run"}
+                     "one by one in one more run (an event between each cache write and its "
+                     "decode, so no launch overlap); back to back: the last step's decode "
+                     "called 50 times in a row between two events, median of 5 such runs"}
     for key, ns in (("automatic", 0), ("balanced", N.PA_SPLITS_BALANCED)):
         ws_bytes = pool.workspace_bytes(S, w.n_q_heads, w.max_blocks, ns)
         ws = torch.empty(max(ws_bytes, 16), dtype=torch.uint8, device="cuda")
@@ -633,6 +635,14 @@ def record_8b_fp8_steps(pool_procs, peak):
         run(dec_ev)
         torch.cuda.synchronize()
         dec_ms = [e0.elapsed_time(e1) for e0, e1 in dec_ev]
+        last = steps - 1
+
+        def back_to_back():
+            for _ in range(50):
+                _decode_call(pool, d_q[last], d_t[last], d_c[last], out, ws, ws_bytes, sh, w.softmax_scale, ns)
+
+        b2b_ms = _median_ms(back_to_back, 5, 1, stream) / 50
+        b2b_bytes = int(c_all[last].sum()) * 2 * Hkv * D
         rec[key] = {"schedule": (f"{pool.num_splits(S, w.n_q_heads, w.max_blocks)} splits" if ns == 0
                                  else "balanced"),
                     "step_ms": round(loop_ms / steps, 5),
@@ -640,6 +650,9 @@ def record_8b_fp8_steps(pool_procs, peak):
                     "decode_ms_median": round(statistics.median(dec_ms), 5),
                     "decode_kv_gbs": round(kv_bytes / sum(dec_ms) / 1e6, 1),
                     "decode_frac_of_measured_peak": round(kv_bytes / sum(dec_ms) / 1e6 / peak, 4),
+                    "decode_back_to_back_ms": round(b2b_ms, 5),
+                    "decode_back_to_back_kv_gbs": round(b2b_bytes / b2b_ms / 1e6, 1),
+                    "decode_back_to_back_frac_of_measured_peak": round(b2b_bytes / b2b_ms / 1e6 / peak, 4),
                     "tokens_per_s": round(S * steps / loop_ms * 1e3, 1)}
     rec["device_error"] = pool.device_error()
     pool.close()
@@ -926,6 +939,25 @@ def _peak_tflops():
         return 1900.0, "fallback"
 
 
+def _prefill_mma_work(w):
+    """The MMA work the tcgen05 prefill kernel issues for this packet, by kind.
+    A CTA holds 128 rows (128 / G query tokens x the G heads of one kv head)
+    and walks the 128-key blocks up to its last query's position; per block it
+    issues S = Q K^T as two E4M3 passes (the query's two E4M3 terms) and
+    O += P V as one binary16 pass, each M = N = K = 128 (masked keys of the
+    diagonal blocks included).  Returns (e4m3 flops, f16 flops, blocks)."""
+    G = w.n_q_heads // w.n_kv_heads
+    tok = 128 // G
+    blocks = 0
+    for n in (int(x) for x in w.ctx_lens):
+        for lo in range(0, w.chunk, tok):
+            pos_last = n - w.chunk + min(w.chunk, lo + tok) - 1
+            blocks += (pos_last // 16 + 1 + 7) // 8
+    blocks *= w.n_kv_heads
+    per_pass = 2 * 128 * 128 * 128
+    return 2 * per_pass * blocks, per_pass * blocks, blocks
+
+
 def run_prefill(args, rank, world, local_rank):
     """Chunked prefill: per step, write the chunk's K/V into its slots, then the
     causal attention of the chunk's queries over each sequence's pages."""
@@ -1087,6 +1119,14 @@ def run_prefill(args, rank, world, local_rank):
     flops = w.prefill_flops()
     peak, peak_kind = _peak_tflops()
     achieved = flops / (statistics.fmean(pre_ms) / 1e3) / 1e12
+    # against the peaks of the MMA kinds issued: e4m3 at twice the measured
+    # bf16 rate (the nominal dense ratio, 4.5 / 2.25 PFLOP/s), binary16 at it
+    f8_fl, f16_fl, blocks = _prefill_mma_work(w)
+    t_peak = f8_fl / (2 * peak * 1e12) + f16_fl / (peak * 1e12)
+    t_kernel = statistics.fmean(pre_ms) / 1e3
+    mix = {"e4m3_flops_issued": f8_fl, "f16_flops_issued": f16_fl, "blocks": blocks,
+           "e4m3_peak_tflops": round(2 * peak, 1), "f16_peak_tflops": peak,
+           "ms_at_peak": round(t_peak * 1e3, 4), "frac": round(t_peak / t_kernel, 4)}
     line = {
         "metric": PREFILL_METRIC, "value": round(world * flops * K / t_max / 1e12, 2),
         "unit": "TFLOP/s", "n_gpus": world, "steps": K, "warmup": args.warmup,
@@ -1104,7 +1144,8 @@ def run_prefill(args, rank, world, local_rank):
         "roofline": {"kernel": "prefill_tc_kernel (tcgen05)", "bound": "tensor", "achieved": round(achieved, 1),
                      "peak": peak, "peak_kind": peak_kind, "unit": "TFLOP/s",
                      "frac": round(achieved / peak, 4), "traffic": None,
-                     "algorithmic_flops_per_step": flops},
+                     "algorithmic_flops_per_step": flops,
+                     "mma_mix": mix},
         "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": 2 * K, "clocks": sampler.summary(),
     }
     print(json.dumps(line), flush=True)
