@@ -370,7 +370,8 @@ PA_API int pa_decode(pa_pool* pool, int layer, void* out, int out_dtype, const v
  * PA_NOALLOC_SCRATCH_BYTES.  It allocates nothing and frees nothing.
  *
  *  - num_splits = 0: the automatic split count, lowered until its partials
- *    fit the array (one split needs no scratch at all).
+ *    fit the array (one split needs no scratch at all); the guided layout of
+ *    pa_decode_num_splits when its partials fit.
  *  - num_splits = PA_SPLITS_BALANCED: at most PA_NOALLOC_SCRATCH_BYTES /
  *    (2 * G * (head_dim + 2) * 4 + 16) CTAs (more than the resident slots of
  *    a GB300 for every supported shape, so the same launch as pa_decode).
