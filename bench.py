@@ -51,6 +51,7 @@ WORKLOADS = {
     "llama3_70b_fp8_block_b": ["llama3_70b_fp8_block_b"],
     "llama3_8b_bf16": ["llama3_8b_bf16"],
     "llama3_8b_fp8": ["llama3_8b_fp8"],
+    "llama3_8b_fp8_long_short": ["llama3_8b_fp8_long_short"],
     "llama3_70b_fp8_prefill": ["llama3_70b_fp8_prefill"],
     "prefix_cache_bf16": ["prefix_cache_bf16"],
     "kv_swap_fp8": ["kv_swap_fp8"],
@@ -73,6 +74,8 @@ DESCRIPTION = {
     "llama3_70b_fp8_block_b": "Llama-3.1-70B-shaped block-scaled FP8 decode, 256 x 4096 tokens",
     "llama3_8b_bf16": "Llama-3.1-8B-shaped bf16 decode, 64 seqs, ctx U[512,4096]",
     "llama3_8b_fp8": "Llama-3.1-8B-shaped FP8 decode, 64 seqs, ctx U[512,4096], 1% K outliers",
+    "llama3_8b_fp8_long_short": "Llama-3.1-8B-shaped FP8 decode, one 131072-token sequence among "
+                                "127 of U[128,1024] tokens",
     "kv_swap_fp8": "Llama-3.1-70B-shaped FP8 pool (Hkv 8, d 128, 16384 blocks of 32 KiB): each "
                    "step swaps 8192 scattered blocks (256 MiB) out to pinned host memory and back "
                    "into 8192 other blocks",
@@ -556,6 +559,37 @@ def record_8b_bf16(pool_procs, peak):
     return rec
 
 
+def record_long_short(pool_procs, peak):
+    """A batch whose lengths differ by orders of magnitude (8B shapes, FP8): one
+    131072-token sequence among 127 short ones.  The automatic split count
+    takes every sequence as the table's width (the lengths live on the
+    device), so the long sequence's few CTAs set the time; the balanced
+    schedule cuts all pages into equal ranges.  Decode calls back to back."""
+    import torch
+    from paged_kv_cache_270_gb300 import _native as N
+    b = Batch("llama3_8b_fp8_long_short", pool_procs)
+    stream = torch.cuda.current_stream()
+    sh = int(stream.cuda_stream)
+    rec = {"workload": DESCRIPTION["llama3_8b_fp8_long_short"], "kv_bytes": b.kv_bytes,
+           "timing": "20 decode calls back to back between two events, median of 5 runs"}
+    for key, ns in (("automatic", 0), ("balanced", N.PA_SPLITS_BALANCED)):
+        ws_bytes = b.pool.workspace_bytes(b.S, b.Hq, b.max_blocks, ns)
+        ws = torch.empty(max(ws_bytes, 16), dtype=torch.uint8, device="cuda")
+
+        def calls():
+            for _ in range(20):
+                _decode_call(b.pool, b.d_q, b.d_tables, b.d_ctx, b.d_out, ws, ws_bytes, sh, b.softmax_scale, ns)
+
+        ms = _median_ms(calls, 5, 1, stream) / 20
+        rec[key] = {"schedule": (f"{b.pool.num_splits(b.S, b.Hq, b.max_blocks)} splits" if ns == 0
+                                 else "balanced"),
+                    "decode_ms": round(ms, 5), "decode_kv_gbs": round(b.kv_bytes / ms / 1e6, 1),
+                    "frac_of_measured_peak": round(b.kv_bytes / ms / 1e6 / peak, 4)}
+    rec["device_error"] = b.pool.device_error()
+    b.pool.close()
+    return rec
+
+
 def record_8b_fp8_steps(pool_procs, peak):
     """Config 2: the 8B shapes over an FP8 cache (per-tensor scales amax/448, 1%
     of K x8), 32 decode steps of (write one token per sequence, decode), new
@@ -790,7 +824,8 @@ def config_records(pool_procs, peak):
     recs = {}
     for name, fn in (("llama3_8b_bf16", lambda: record_8b_bf16(pool_procs, peak)),
                      ("llama3_8b_fp8_steps", lambda: record_8b_fp8_steps(pool_procs, peak)),
-                     ("prefix_share_bf16", lambda: record_prefix_share(peak))):
+                     ("prefix_share_bf16", lambda: record_prefix_share(peak)),
+                     ("llama3_8b_fp8_long_short", lambda: record_long_short(pool_procs, peak))):
         recs[name] = fn()
         if recs[name].get("device_error") or \
                 any(v.get("device_error") for v in recs[name].values() if isinstance(v, dict)):

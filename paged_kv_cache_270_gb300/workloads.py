@@ -31,6 +31,9 @@ Workloads (shapes follow the model families the pages name: Llama-3.1 8B and
   prefix_share_bf16    Hq 32 / Hkv 8, d 128, bf16: 64 requests sharing a
                        2048-token prefix, each with a U[128, 1024] suffix
                        (tables come from the block allocator, not from here)
+  llama3_8b_fp8_long_short  8B shapes, FP8: one 131072-token sequence among 127
+                       of U[128, 1024] tokens (a batch whose lengths differ by
+                       orders of magnitude)
 """
 from __future__ import annotations
 
@@ -42,7 +45,7 @@ import numpy as np
 BLOCK = 16
 CHUNK = 256  # tokens per independently seeded draw
 
-NAMES = ("tiny_fp16", "llama3_8b_bf16", "llama3_8b_fp8", "llama3_70b_fp8_a",
+NAMES = ("tiny_fp16", "llama3_8b_bf16", "llama3_8b_fp8", "llama3_8b_fp8_long_short", "llama3_70b_fp8_a",
          "llama3_70b_fp8_b", "llama3_70b_fp8_prefill", "prefix_share_bf16")
 
 
@@ -260,6 +263,11 @@ def make(name: str, scale_down: int = 1, steps: int | None = None) -> Workload:
         w = _paged(2, name, "fp8_e4m3", 32, 8, 128, ctx, slack=1.25,
                    steps=32 if steps is None else steps, outlier_frac=0.01)
         return w
+    if name == "llama3_8b_fp8_long_short":
+        rng = np.random.default_rng([1006, 5])
+        ctx = np.concatenate([[131072 // sd], rng.integers(128, 1024, size=max(1, 127 // sd),
+                                                           endpoint=True) // sd])
+        return _paged(6, name, "fp8_e4m3", 32, 8, 128, np.maximum(1, ctx).astype(np.int32))
     if name == "llama3_70b_fp8_a":
         return _paged(3, name, "fp8_e4m3", 64, 8, 128, [131072 // sd] * 4)
     if name == "llama3_70b_fp8_b":

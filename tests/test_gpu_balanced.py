@@ -159,3 +159,11 @@ def test_bad_ids_and_lengths_are_reported():
     assert pool.device_error() == N.PA_ERR_BOUNDS
     gpu_decode(w, pool, q, num_splits=BAL)
     assert pool.device_error() == N.PA_OK
+
+
+def test_one_long_sequence_among_short_ones():
+    """The 8B-shaped FP8 batch of one 131072-token sequence among 127 short ones,
+    scaled down 16 times (one of 8192 tokens among 7 short): balanced and the
+    automatic split count against the oracle, every row."""
+    w = W.make("llama3_8b_fp8_long_short", scale_down=16)
+    _check(w, splits=(BAL, 0))
