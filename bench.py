@@ -93,12 +93,12 @@ DESCRIPTION = {
 # measured.
 NCU_TRAFFIC = {
     # hash of the decode source with comments and blank lines removed (see _source_sha)
-    "source_sha256": "c5bde61ed985227340053045cdb3f1586febb3c101f53bf868b4d4a74e1d137e",
+    "source_sha256": "1fffa0627ca9a67c2af353fbfdac22678835d4f261f9384f609d9a64fae42a63",
     # dram__bytes_read.sum + dram__bytes_write.sum of one decode launch
-    "bytes_per_launch": {"llama3_70b_fp8_a": 1074033152 + 3508480,
-                         "llama3_70b_fp8_b": 2152017152 + 4891136,
-                         "llama3_70b_fp8_block_a": 1076088064 + 2924800,
-                         "llama3_70b_fp8_block_b": 2156267264 + 5160704},
+    "bytes_per_launch": {"llama3_70b_fp8_a": 1073987328 + 3501568,
+                         "llama3_70b_fp8_b": 2151997952 + 4874240,
+                         "llama3_70b_fp8_block_a": 1076081664 + 2970112,
+                         "llama3_70b_fp8_block_b": 2156272128 + 4859136},
 }
 
 # --------------------------------------------------------------------- workers

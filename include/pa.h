@@ -288,12 +288,16 @@ PA_API int pa_reshape_and_cache(pa_pool* pool, int layer, const void* k, const v
 
 /* num_splits value that asks pa_decode for the balanced schedule (batches of
  * at most 4096 sequences, else PA_ERR_UNSUPPORTED): one CTA per resident slot
- * of the GPU, four per SM (the kernel's shared memory keeps a fifth off); the pages of every (sequence, kv head)
- * pair, taken in (sequence, kv head, page) order, are cut into equal
- * contiguous ranges, one per CTA, from the context lengths on the device, so
- * every CTA streams the same number of pages whatever the mix of lengths, and
- * streams from one pair to the next without draining its pipeline.  A pair
- * whose pages span several CTAs is merged by a second kernel. */
+ * of the GPU, four per SM (the kernel's shared memory keeps a fifth off); the
+ * (sequence, kv head) pairs, taken in (sequence, kv head, page) order, are cut
+ * into contiguous ranges of equal cost, one per CTA, from the context lengths
+ * on the device: a pair of n pages costs n plus a fixed 12 pages (FP8 pools;
+ * 6 for 16-bit pools), what finishing a pair costs a CTA.  Every CTA thus
+ * streams about as long whatever the mix of lengths, and streams from one
+ * pair to the next without draining its pipeline.  A pair whose pages span
+ * several CTAs is merged by a second kernel.  For batches whose lengths differ
+ * by orders of magnitude, which the automatic split count (sized from the
+ * table width) serves badly. */
 #define PA_SPLITS_BALANCED (-1)
 
 /* Number of splits pa_decode uses along each sequence's pages for this batch

@@ -747,6 +747,11 @@ struct BalCfg {
   // starts before the kernel ahead of it has finished), and the CTAs of a
   // five-CTA SM stream 4/5 as fast, which sets the time of the whole grid.
   static constexpr int kLaunchSmem = kSmem > 48 * 1024 ? kSmem : 48 * 1024;
+  // What finishing a unit costs a CTA, in page-times (per-unit traces of a
+  // batch of 28-page units: ~3-4 us for the merge, the output rows and the next
+  // unit's start, against ~0.3 us a page for FP8 and about twice that for
+  // 16-bit pages).
+  static constexpr int kUnitCostPages = C::kFp8 ? 12 : 6;
   static_assert(kOffFrag % 16 == 0 && kOffQStage % 16 == 0, "bulk-copy destinations are 16-byte aligned");
 };
 
@@ -801,7 +806,7 @@ __global__ void __launch_bounds__(kThreads, MINB) decode_bal_kernel(const Decode
   constexpr int QW = D / 8;  // 32-bit query words per thread
   extern __shared__ __align__(16) uint8_t smem_raw[];
   __shared__ long long s_warp_sums[kThreads / 32];
-  __shared__ long long s_start_off;
+  __shared__ long long s_start_off, s_rbegin, s_rend;
   __shared__ int s_start_seq;
   __shared__ int s_abort;
   __shared__ int s_go;
@@ -824,23 +829,34 @@ __global__ void __launch_bounds__(kThreads, MINB) decode_bal_kernel(const Decode
   grid_dependency_wait();  // the kernel before may still write q, tables, pages
 
   // ---------------------------------------------------------------- schedule
-  // Pages of every sequence (a contiguous share of the sequences per thread)
-  // and their prefix sum: sequence s's units start at position
-  // Hkv * (pages of the sequences before s).
+  // Cost of every sequence (a contiguous share of the sequences per thread)
+  // and its prefix sum.  A unit (sequence, kv head) of n pages costs n + kUnit
+  // page-times: finishing a unit (the warps' merge, the output rows, the next
+  // unit's query rows) costs a CTA about kUnit pages' worth of streaming, so a
+  // range of short units gets fewer pages.  Positions: sequence s's units
+  // start at the cost of the sequences before s; within a unit the first kUnit
+  // positions hold no page, page p sits at kUnit + p.  The ranges are cut in
+  // cost; the real pages of position x are R(x) = Hkv * (pages before s) +
+  // h * n + max(0, v - kUnit) for x in unit h of s at offset v.
+  constexpr int kUnit = B::kUnitCostPages;
   const int per = (a.S + kThreads - 1) / kThreads;
   const int s0 = min(a.S, (int)threadIdx.x * per), s1 = min(a.S, s0 + per);
-  long long mine = 0;
+  long long mine = 0, mine_pg = 0;
   for (int s = s0; s < s1; ++s) {
     int c = a.ctx[s];
     if (c < 0 || c > a.max_blocks * 16) {
       record_error(a.err, PA_ERR_BOUNDS);
       c = clamp_ctx(c, a.max_blocks);
     }
-    mine += (c + 15) >> 4;
+    const int np = (c + 15) >> 4;
+    mine_pg += np;
+    mine += np > 0 ? (long long)a.Hkv * (np + kUnit) : 0;
   }
-  long long total;
+  long long total, total_pg;
   const long long before = block_exclusive_scan<kThreads>(mine, s_warp_sums, total);
-  const long long ptot = total * a.Hkv;
+  __syncthreads();  // the scan's partial sums are read before the second scan writes them
+  const long long before_pg = block_exclusive_scan<kThreads>(mine_pg, s_warp_sums, total_pg);
+  const long long ptot = total;  // in cost
   const long long T = max((ptot + a.ctas - 1) / a.ctas, (long long)kMinPagesPerCta);
   const long long pos_begin = (long long)blockIdx.x * T;
   const long long pos_end = min(ptot, pos_begin + T);
@@ -849,23 +865,37 @@ __global__ void __launch_bounds__(kThreads, MINB) decode_bal_kernel(const Decode
     if (a.ctx[s] > 0) continue;
     for (int i = threadIdx.x; i < a.Hq * D; i += kThreads) store_out<OUT>(a.out, (size_t)s * a.Hq * D + i, 0.f);
   }
-  if (pos_begin >= pos_end) {  // no pages for this CTA: no partial and no merge job
-    if (threadIdx.x == 0) a.jobs[blockIdx.x] = make_int4(-1, 0, 0, 0);
-    return;
-  }
-  const int n_pages = (int)(pos_end - pos_begin);  // pages of this CTA
-  // the thread whose sequences hold position pos_begin finds the one it falls in
-  if (before * a.Hkv <= pos_begin && pos_begin < (before + mine) * a.Hkv) {
-    long long cum = before * a.Hkv;
+  // The thread whose sequences hold a boundary finds its sequence and real page.
+  auto locate = [&](long long x, bool start) {
+    long long cum = before, cum_pg = before_pg * a.Hkv;
     for (int s = s0; s < s1; ++s) {
-      const long long n = (long long)((clamp_ctx(a.ctx[s], a.max_blocks) + 15) >> 4) * a.Hkv;
-      if (pos_begin < cum + n) {
-        s_start_seq = s;
-        s_start_off = pos_begin - cum;
-        break;
+      const long long np = (clamp_ctx(a.ctx[s], a.max_blocks) + 15) >> 4;
+      const long long n = np > 0 ? a.Hkv * (np + kUnit) : 0;
+      if (x < cum + n) {
+        const long long off = x - cum, hh = off / (np + kUnit), v = off - hh * (np + kUnit);
+        const long long r = cum_pg + hh * np + max(0LL, v - kUnit);
+        if (start) {
+          s_start_seq = s;
+          s_start_off = off;
+          s_rbegin = r;
+        } else {
+          s_rend = r;
+        }
+        return;
       }
       cum += n;
+      cum_pg += np * a.Hkv;
     }
+  };
+  if (before <= pos_begin && pos_begin < before + mine) locate(pos_begin, true);
+  if (before <= pos_end && pos_end < before + mine) locate(pos_end, false);
+  if (threadIdx.x == 0 && pos_end >= ptot) s_rend = total_pg * a.Hkv;
+  if (threadIdx.x == 0 && pos_begin >= ptot) s_rbegin = total_pg * a.Hkv;
+  __syncthreads();
+  const int n_pages = (int)(s_rend - s_rbegin);  // real pages of this CTA
+  if (n_pages <= 0) {  // no pages for this CTA: no partial and no merge job
+    if (threadIdx.x == 0) a.jobs[blockIdx.x] = make_int4(-1, 0, 0, 0);
+    return;
   }
   if (threadIdx.x == 0) {
     s_abort = 0;
@@ -890,14 +920,16 @@ __global__ void __launch_bounds__(kThreads, MINB) decode_bal_kernel(const Decode
     int seq = s_start_seq;
     int ctx = clamp_ctx(a.ctx[seq], a.max_blocks);
     int npages = (ctx + 15) >> 4;
-    int h = (int)(s_start_off / npages);
-    int pg0 = (int)(s_start_off % npages);
-    long long pos = pos_begin;
+    int h = (int)(s_start_off / (npages + kUnit));
+    const int v0 = (int)(s_start_off - (long long)h * (npages + kUnit));
+    int pg0 = max(0, v0 - kUnit);
+    long long ucost = pos_begin - v0;  // cost position of the current unit's start
+    int left = n_pages;                // real pages still to stream
     int kb = 0;  // CTA-local index of the unit's first page
     int issued = 0, nq = 0;  // page copies and query-row copies issued (lane 0)
     bool abort = false;
     for (int j = 0; !abort; ++j) {
-      const int len = (int)min((long long)(npages - pg0), pos_end - pos);
+      const int len = min(npages - pg0, left);
       // the unit's descriptor and query rows, once the consumers hold the previous ones
       int stop = 0;
       if (lane == 0) {
@@ -911,7 +943,7 @@ __global__ void __launch_bounds__(kThreads, MINB) decode_bal_kernel(const Decode
           sd.len = len;
           sd.ctx = ctx;
           sd.npages = npages;
-          sd.last_cta = (int)((pos - pg0 + npages - 1) / T);  // the CTA of the unit's last page
+          sd.last_cta = (int)((ucost + kUnit + npages - 1) / T);  // the CTA of the unit's last page
           *desc = sd;
           const uint32_t qbytes = (uint32_t)(a.G * D * 2);
           mbar_arrive_expect_tx(q_full, qbytes);
@@ -968,9 +1000,10 @@ __global__ void __launch_bounds__(kThreads, MINB) decode_bal_kernel(const Decode
       }
       if (abort) break;
       kb += len;
-      pos += len;
-      if (pos >= pos_end) break;
+      left -= len;
+      if (left <= 0) break;
       // the next unit, from its first page
+      ucost += npages + kUnit;
       pg0 = 0;
       if (++h == a.Hkv) {
         h = 0;
