@@ -627,7 +627,7 @@ __global__ void __launch_bounds__(kThreads, MINB) decode_kernel(const DecodeArgs
 
     for (int k = warp; k < n_local; k += kConsumerWarps) {
       const int stage = k % C::kStages;
-      // every lane waits (acquiring the TMA writes); the verdict is made warp-uniform
+      // every lane waits (acquiring the TMA writes); the outcome is made warp-uniform
       if (!__all_sync(kFull, mbar_wait(&full[stage], (k / C::kStages) & 1, pipe_wait_limit()))) {
         if (lane == 0) record_error(a.err, PA_ERR_TIMEOUT);
         break;
