@@ -418,7 +418,10 @@ PA_API int pa_decode_no_alloc(pa_pool* pool, int layer, void* out, int out_dtype
  * Query row j of a chunk of C tokens sits at position ctx - C + j and attends
  * to tokens [0, ctx - C + j] of its sequence (grouped-query heads as in
  * pa_decode).  Invalid ids or lengths set PA_ERR_BOUNDS in the device error
- * word (those rows are then not written).  No scratch memory is needed. */
+ * word (those rows are then not written).  The tensor-core kernel of FP8
+ * pools takes its whole-tensor-memory allocation to start at column 0; a CTA
+ * that finds otherwise sets PA_ERR_UNSUPPORTED and writes nothing.  No
+ * scratch memory is needed. */
 PA_API int pa_prefill(pa_pool* pool, int layer, void* out, int out_dtype, const void* q,
                       const int32_t* q_start_dev, const int32_t* block_tables_dev,
                       int max_blocks_per_seq, const int32_t* ctx_lens_dev, int S, int n_q_heads,

@@ -237,20 +237,25 @@ __device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t* bar, uint32_t pari
 // Bounded wait that also gives up as soon as another role has aborted.  Its
 // retries sleep (up to 20 us each, woken when the phase completes), so the
 // waiting warps leave the issue slots of their scheduler to the warps that
-// work, the single MMA-issuing thread above all.
+// work, the single MMA-issuing thread above all.  The wait gives up before a
+// sleep that could take it past the limit, so a limit shorter than one sleep
+// gives up as soon as the first (briefly blocking) test finds the phase
+// incomplete.
 __device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
                                               unsigned int* err) {
+  constexpr uint32_t kSleepNs = 20000u;
   if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t limit = pipe_wait_limit();
   const uint64_t t0 = global_ns();
-  while (!mbar_try_wait_sleep(bar, parity, 20000u)) {
+  for (;;) {
     if (*abort_flag) return false;
-    if (global_ns() - t0 > pipe_wait_limit()) {
+    if (global_ns() - t0 + kSleepNs > limit) {
       *abort_flag = 1;
       record_error(err, PA_ERR_TIMEOUT);
       return false;
     }
+    if (mbar_try_wait_sleep(bar, parity, kSleepNs)) return true;
   }
-  return true;
 }
 
 // causal limit of a row: the position of its query token (rows past the
@@ -351,9 +356,18 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const TcArgs a,
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  const uint32_t tmem = ctl->tmem;
+  // A 512-column allocation spans the whole tensor memory, so its base is lane
+  // 0, column 0.  FP8 pools take that base as a constant: every tensor-memory
+  // operand of the MMA-issuing thread is then an immediate (3% faster on the
+  // 8,192-token packet; 16-bit pools measured 2% slower with it, so they keep
+  // the allocated address).  A different base is reported and the CTA skips
+  // its work.
+  const uint32_t tmem_base = ctl->tmem;
+  const uint32_t tmem = F8 ? 0u : tmem_base;
 
-  if (warp == 0) {
+  if (F8 && tmem_base != 0) {
+    if (threadIdx.x == 0) record_error(a.err, PA_ERR_UNSUPPORTED);
+  } else if (warp == 0) {
     // ---------------------------------------------------------- TMA producer
     const int32_t* trow = a.tables + (size_t)seq * a.max_blocks;
     const uint64_t policy = l2_evict_first_policy();
@@ -880,7 +894,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const TcArgs a,
   __syncthreads();
   if (warp == 1) {
     tc_fence_after();
-    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTmemCols) : "memory");
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_base), "r"(kTmemCols) : "memory");
   }
 }
 
