@@ -74,7 +74,15 @@ enum Kind { K_E4M3 = 0, K_E4M3B = 1, K_BF16 = 2, K_F16 = 3 };
 
 struct Ctrl {
   uint64_t kv_full[3], kv_empty[3], s_full[2], vt_full[2], vt_empty[2];
-  uint64_t sc_full[2], sc_empty[2], q_ready, p_full, o_done, drain, xchg;
+  // p_full is two barriers (by block parity) although one P is consumed at a
+  // time: the softmax may store P(j) and P(j + 1) before the MMA thread wakes
+  // for P(j) (both S were issued before that wait), and one barrier would then
+  // have completed two phases, which a parity wait cannot tell from none (the
+  // thread waited out its limit on one such call).  P(j + 2) needs S(j + 2),
+  // issued only after P V(j), so a barrier per parity is never two phases
+  // ahead of its waiter.  (Every other barrier here has that property by
+  // construction.)
+  uint64_t sc_full[2], sc_empty[2], p_full[2], q_ready, o_done, drain, xchg;
   uint64_t tail_ready, tail_done;  // 16-bit pools: the last block's V rows past the tile are zeroed
   float2 sc[2][8];  // block-scaled pools: (K scale, V scale) of each page of a ring block
   float xbuf[2][128][2];  // the two half-row threads' partials (Q amax, block max, row sum)
@@ -333,9 +341,9 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const TcArgs a,
       mbar_init(&ctl->vt_empty[i], 1);
       mbar_init(&ctl->sc_full[i], 1);
       mbar_init(&ctl->sc_empty[i], 8);
+      mbar_init(&ctl->p_full[i], 8);
     }
     mbar_init(&ctl->q_ready, 8);
-    mbar_init(&ctl->p_full, 8);
     mbar_init(&ctl->o_done, 1);
     mbar_init(&ctl->drain, 1);
     mbar_init(&ctl->xchg, 8);
@@ -507,7 +515,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const TcArgs a,
         }
         auto step = [&](auto par, int i) -> bool {
           constexpr int P = decltype(par)::value;  // i % 2
-          if (!wait_or_abort(&ctl->p_full, P, abort_flag, a.err)) return false;
+          if (!wait_or_abort(&ctl->p_full[P], (i >> 1) & 1, abort_flag, a.err)) return false;
           if (!wait_or_abort(&ctl->vt_full[P], (i >> 1) & 1, abort_flag, a.err)) return false;
           tc_fence_after();
 #pragma unroll
@@ -540,7 +548,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const TcArgs a,
       }
       for (int i = 0; i < nblk && run; ++i) {
         const int vb = i & 1;
-        if (!wait_or_abort(&ctl->p_full, i & 1, abort_flag, a.err)) break;
+        if (!wait_or_abort(&ctl->p_full[i & 1], (i >> 1) & 1, abort_flag, a.err)) break;
         if constexpr (F8) {
           if (!wait_or_abort(&ctl->vt_full[vb], (i >> 1) & 1, abort_flag, a.err)) break;
         } else {
@@ -865,7 +873,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const TcArgs a,
       __syncwarp();
       if (lane == 0) {
         if constexpr (BLK) mbar_arrive(&ctl->sc_empty[sb]);
-        mbar_arrive(&ctl->p_full);
+        mbar_arrive(&ctl->p_full[sb]);
       }
     }
     // output rows: O / l (times the V scale), once every MMA is done.  (The
