@@ -82,7 +82,7 @@ struct Ctrl {
   // issued only after P V(j), so a barrier per parity is never two phases
   // ahead of its waiter.  (Every other barrier here has that property by
   // construction.)
-  uint64_t sc_full[2], sc_empty[2], p_full[2], q_ready, o_done, drain, xchg;
+  uint64_t sc_full[2], sc_empty[2], p_full[2], q_ready, drain, xchg;
   uint64_t tail_ready, tail_done;  // 16-bit pools: the last block's V rows past the tile are zeroed
   float2 sc[2][8];  // block-scaled pools: (K scale, V scale) of each page of a ring block
   float xbuf[2][128][2];  // the two half-row threads' partials (Q amax, block max, row sum)
@@ -344,7 +344,6 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const TcArgs a,
       mbar_init(&ctl->p_full[i], 8);
     }
     mbar_init(&ctl->q_ready, 8);
-    mbar_init(&ctl->o_done, 1);
     mbar_init(&ctl->drain, 1);
     mbar_init(&ctl->xchg, 8);
     mbar_init(&ctl->tail_ready, 1);
@@ -524,7 +523,6 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const TcArgs a,
             for (int k = 0; k < 8; ++k)
               mma_f16_ts(tmem + kOCol, tmem + P * 128 + 32 * (k >> 1) + 16 * part + 8 * (k & 1), pvb[P][k],
                          kIdescPV, (uint32_t)(i | k | part));
-          mma_commit(&ctl->o_done);
           mma_commit(&ctl->vt_empty[P]);
           if (i + 2 < nblk) {  // S(i + 2) into S buffer P, from ring slot P
             if (!wait_or_abort(&ctl->kv_full[P], ((i + 2) >> 1) & 1, abort_flag, a.err)) return false;
@@ -563,7 +561,6 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const TcArgs a,
           for (int k = 0; k < 8; ++k)
             mma_f16_ts(tmem + kOCol, tmem + vb * 128 + 32 * (k >> 1) + 16 * part + 8 * (k & 1),
                        vd + k * (2048 >> 4), kIdescPV | (BF ? kBf16Types : 0u), (uint32_t)(i | k | part));
-        mma_commit(&ctl->o_done);
         if constexpr (F8) mma_commit(&ctl->vt_empty[vb]);
         else mma_commit(&ctl->kv_empty[i % R]);  // K and V of block i are read
         if (i + 2 < nblk) {
@@ -796,13 +793,17 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const TcArgs a,
         ov *= alpha;
         m = mx;
       }
-      // O is rescaled once the previous block's P V is done (rarely needed).
-      // Phase distance: s_full(j) was committed after Q K^T(j), issued after
-      // P V(j - 2), and a commit tracks every earlier MMA of the thread, so
-      // P V(j - 2) is done; P V(j) needs this block's P.  So o_done has
-      // completed j - 1 or j phases here.
+      // O is rescaled once the previous block's P V is done (rarely needed),
+      // seen through the barrier committed right behind that P V: the binary16
+      // V buffer's (FP8) or the ring slot's (16-bit) release.  Phase distance:
+      // s_full(j) was committed after Q K^T(j), issued after P V(j - 2), and a
+      // commit tracks every earlier MMA of the thread, so that barrier's phase
+      // before P V(j - 1)'s is complete; its phase after needs P(j + 1) or
+      // later, which is not stored yet.  So the awaited phase is pending or just
+      // completed, never mistaken.
       if (ok && j > 0 && __any_sync(kAll, ov != 1.f)) {
-        ok = __all_sync(kAll, wait_or_abort(&ctl->o_done, (j - 1) & 1, abort_flag, a.err));
+        ok = __all_sync(kAll, F8 ? wait_or_abort(&ctl->vt_empty[(j - 1) & 1], ((j - 1) >> 1) & 1, abort_flag, a.err)
+                                 : wait_or_abort(&ctl->kv_empty[(j - 1) % R], ((j - 1) / R) & 1, abort_flag, a.err));
         if (ok) {
           tc_fence_after();
 #pragma unroll 1
@@ -876,10 +877,8 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const TcArgs a,
         mbar_arrive(&ctl->p_full[sb]);
       }
     }
-    // output rows: O / l (times the V scale), once every MMA is done.  (The
-    // final P V is awaited through the one-phase drain barrier: o_done may be
-    // two phases behind here, since it is only awaited to rescale O, and a
-    // parity wait tells phases apart only one phase ahead.)
+    // output rows: O / l (times the V scale), once every MMA is done (the
+    // one-phase drain barrier, committed behind the last P V)
     float l0, l1;
     exchange(l, l0, l1);
     const float L = l0 + l1;
