@@ -161,3 +161,30 @@ def test_bounds_still_reported():
                      *args, max_chunk=16, out=out)
         assert pool.device_error() == N.PA_ERR_BOUNDS
     _run(w, pool, op, q, q_start, chunks)
+
+
+@pytest.mark.parametrize("kv_dtype", ["fp8_e4m3", "bf16"])
+def test_back_to_back_launches_identical_and_error_free(kv_dtype):
+    """Thirty launches in a row on one stream, the first right after the pool
+    is filled (cold caches): each is bit-identical to the first and none
+    records an error.  A barrier awaited by parity that fell two phases
+    behind its producer would show as a wait running out its limit
+    (PA_ERR_TIMEOUT); a race on a buffer, as a different result.  The first
+    launch is also checked against the oracle."""
+    pairs = [(2000, 300), (500, 128), (0, 77), (3000, 16)]
+    w, pool, op, q, q_start, chunks = _setup(kv_dtype, pairs, seed=61)
+    args = (bits_to_torch(q, w.in_dtype), torch.from_numpy(q_start).cuda(),
+            torch.from_numpy(w.block_tables).cuda(), torch.from_numpy(w.ctx_lens).cuda())
+    first = pool.prefill(*args, max_chunk=max(chunks), softmax_scale=w.softmax_scale)
+    torch.cuda.synchronize()
+    assert pool.device_error() == N.PA_OK
+    ref = oracle.paged_prefill(w.kv_dtype, w.in_dtype, w.num_blocks, 16, w.n_kv_heads, 128, op[0],
+                               op[1], w.k_scale, w.v_scale, q, q_start, w.block_tables, w.ctx_lens,
+                               w.softmax_scale)
+    check_half(first, ref, vmax_of(w, op))
+    outs = [pool.prefill(*args, max_chunk=max(chunks), softmax_scale=w.softmax_scale)
+            for _ in range(30)]
+    torch.cuda.synchronize()
+    assert pool.device_error() == N.PA_OK
+    for i, out in enumerate(outs):
+        assert torch.equal(out.view(torch.int16), first.view(torch.int16)), f"launch {i + 1} differs"
