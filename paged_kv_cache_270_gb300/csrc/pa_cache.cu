@@ -54,6 +54,11 @@ __global__ void __launch_bounds__(256) reshape_and_cache_kernel(
     long long n_vec, int vec_per_token, int vec_per_row, int head_dim, long long num_slots,
     uint8_t* __restrict__ kpool, uint8_t* __restrict__ vpool, float k_scale, float v_scale,
     unsigned int* err) {
+  // A decode launched behind this kernel (programmatic stream serialization)
+  // may be scheduled now: it waits for this grid's completion and its writes
+  // before its first global access, so only its launch and CTA placement
+  // overlap this kernel.
+  grid_dependents_launch();
   long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x;
   if (i >= n_vec) return;
   const long long t = i / vec_per_token;
@@ -168,6 +173,7 @@ __global__ void __launch_bounds__(128) reshape_block_scaled_kernel(
     uint8_t* __restrict__ kpool, uint8_t* __restrict__ vpool, float* __restrict__ ksc,
     float* __restrict__ vsc, unsigned int* err) {
   __shared__ uint32_t red[2][4];
+  grid_dependents_launch();  // (as in reshape_and_cache_kernel)
   const int t = blockIdx.x, h = blockIdx.y;
   const int64_t slot = slots[t];
   if (slot < 0) return;
