@@ -130,8 +130,10 @@ class Agent:
         self.name, self.gen = name, gen
 
 
-def prefill_cta(rng, n, fp8, single_p, rescale_p=0.02):
-    """The barriers and roles of one CTA of the tcgen05 prefill over n blocks."""
+def prefill_cta(rng, n, fp8, single_p, rescale_p=0.02, blk=False):
+    """The barriers and roles of one CTA of the tcgen05 prefill over n blocks
+    (blk: a block-scaled FP8 pool, whose page scales go to the softmax warps
+    through a two-buffer hand-off of their own)."""
     R = 2 if fp8 else 3
     d = lambda lo, hi: ("delay", rng.uniform(lo, hi))
 
@@ -144,6 +146,8 @@ def prefill_cta(rng, n, fp8, single_p, rescale_p=0.02):
             sim.bar(f"vt_full{i}", 4)
             sim.bar(f"vt_empty{i}", 1)
             sim.bar(f"p_full{i}", 8)
+            sim.bar(f"sc_full{i}", 1)
+            sim.bar(f"sc_empty{i}", 8)
         sim.bar("p_full", 8)
         for name, c in (("q_ready", 8), ("drain", 1), ("xchg", 8), ("tail_ready", 1), ("tail_done", 4)):
             sim.bar(name, c)
@@ -155,6 +159,10 @@ def prefill_cta(rng, n, fp8, single_p, rescale_p=0.02):
         for j in range(n):
             if j >= R:
                 yield ("wait", f"kv_empty{j % R}", j // R - 1)
+            if blk:  # the block's page scales into buffer j % 2
+                if j >= 2:
+                    yield ("wait", f"sc_empty{j % 2}", j // 2 - 1)
+                yield ("arrive", [f"sc_full{j % 2}"])
             yield d(0.0, 0.3)
             yield ("tma", f"kv_full{j % R}")
         for x in range(max(0, n - R), n):  # no copy in flight at the end
@@ -212,6 +220,8 @@ def prefill_cta(rng, n, fp8, single_p, rescale_p=0.02):
         yield from exchange()
         yield ("arrive", ["q_ready"])
         for j in range(n):
+            if blk:
+                yield ("wait", f"sc_full{j % 2}", j // 2)
             yield ("wait", f"s_full{j % 2}", j // 2)
             yield d(0.1, 0.8)
             yield from exchange()
@@ -222,7 +232,7 @@ def prefill_cta(rng, n, fp8, single_p, rescale_p=0.02):
                     yield ("wait", f"kv_empty{(j - 1) % R}", (j - 1) // R)
             yield d(0.3, 1.5)
             name, _ = p_bar(j)
-            yield ("arrive", [name])
+            yield ("arrive", ([f"sc_empty{j % 2}"] if blk else []) + [name])
         yield from exchange()
         yield ("wait", "drain", 0)
 
@@ -232,19 +242,19 @@ def prefill_cta(rng, n, fp8, single_p, rescale_p=0.02):
     return bars, agents
 
 
-def run_once(seed, n, fp8, single_p, wake_max):
+def run_once(seed, n, fp8, single_p, wake_max, blk=False):
     rng = random.Random(seed)
     sim = Sim(rng, wake_max)
-    bars, agents = prefill_cta(rng, n, fp8, single_p)
+    bars, agents = prefill_cta(rng, n, fp8, single_p, blk=blk)
     bars(sim)
     sim.run(agents)
 
 
-@pytest.mark.parametrize("fp8", [True, False])
-def test_kernel_protocol_holds_on_random_schedules(fp8):
+@pytest.mark.parametrize("fp8,blk", [(True, False), (True, True), (False, False)])
+def test_kernel_protocol_holds_on_random_schedules(fp8, blk):
     for seed in range(600):
         for n in (1, 2, 3, 4, 5, 8):
-            run_once(seed * 31 + n, n, fp8, single_p=False, wake_max=25.0)
+            run_once(seed * 31 + n, n, fp8, single_p=False, wake_max=25.0, blk=blk)
 
 
 @pytest.mark.parametrize("fp8", [True, False])
